@@ -1,0 +1,497 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused ScaledMaskSoftmax on GB300.
+
+One step = one pass of the whole hot path over one batch: the forward
+(load + scale + mask + causal, row max, exp + sum, normalise + store) and the
+backward (row dot, gradient) through the C ABI, on inputs already resident in
+HBM.  Default workload: [8,32,1024,1024] fp32 scores with an [8,1,1024,1024]
+key-padding mask (-10000 fill), forward then backward with dy ~ N(0,1).
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
+instead, on bounded samples of the same workload.  ``--all`` additionally
+writes one JSON line per workload to the file given.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "fused masked-softmax fwd/bwd achieved HBM GB/s and % of GB300 peak; rows/s"
+DEFAULT_WORKLOAD = "keypad_f32_s1024"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+DTYPE_NAME = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}
+
+
+# ----------------------------------------------------------------- helpers ---
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _kernel_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "scaled_masked_softmax_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_record(workload: str, kernel: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("kernel_hash") != _kernel_hash():
+        return None
+    rec = d.get("workloads", {}).get(workload, {}).get(kernel)
+    if not rec:
+        return None
+    return rec.get("bytes_per_launch")
+
+
+def fwd_bytes(w, inp) -> int:
+    """Algorithmic bytes of one forward: x read (only j <= q under causal),
+    unique mask bytes read (same causal rule), y written in full."""
+    eb = w.elem_bytes
+    rows, S = w.rows, w.cols
+    if w.is_causal:
+        # row q reads q+1 elements
+        q = torch.arange(rows, dtype=torch.float64) % S
+        x_read = float((q + 1).sum()) * eb
+    else:
+        x_read = rows * S * eb
+    mask_read = 0.0
+    if inp["mask"] is not None:
+        if w.mask == "B1SS":
+            nb = math.ceil(rows / (w.H * S))
+            per_q = (torch.arange(S, dtype=torch.float64) + 1).sum() if w.is_causal else S * S
+            mask_read = float(nb * per_q) * eb
+        else:  # [S,S] (or full): rows touch min(rows, S) distinct mask rows per mask head
+            nq = min(rows, S)
+            per_q = float((torch.arange(nq, dtype=torch.float64) + 1).sum()) if w.is_causal else nq * S
+            mask_read = per_q * eb
+    return int(x_read + mask_read + rows * S * eb)
+
+
+def bwd_bytes(w) -> int:
+    """Algorithmic bytes of one backward: y and dy read (only j <= q with the
+    causal hint), dx written in full."""
+    eb = w.elem_bytes
+    rows, S = w.rows, w.cols
+    if w.is_causal:
+        q = torch.arange(rows, dtype=torch.float64) % S
+        read = float((q + 1).sum()) * 2 * eb
+    else:
+        read = rows * S * 2 * eb
+    return int(read + rows * S * eb)
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.sel = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            self.sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            self.sel = []
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi"] + self.sel + [f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], None, set()
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    s, m = float(parts[1]), float(parts[2])
+                except ValueError:
+                    continue
+                sm.append(s)
+                mx = m
+                for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                                   parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ ours ---
+
+def run_ours(args, rank, world, device):
+    import scaled_masked_softmax_gb300 as sms
+    from scaled_masked_softmax_gb300 import workloads
+
+    w = workloads.WORKLOADS[args.workload]
+    torch.cuda.set_device(device)
+    inp = workloads.make_inputs(w, device=device, with_dy=True)
+    x, mask, dy = inp["x"], inp["mask"], inp["dy"]
+    y = torch.empty_like(x)
+    dx = torch.empty_like(x)
+    stream = torch.cuda.current_stream(device)
+    st = stream.cuda_stream
+    dt = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}[x.dtype]
+    mptr = None if mask is None else mask.data_ptr()
+    mnum = 0 if mask is None else mask.numel()
+    L = sms.binding.lib()
+
+    def fwd():
+        rc = L.sms_forward(x.data_ptr(), mptr, mnum, inp["mask_stride_b"], inp["mask_stride_h"], inp["heads"],
+                           y.data_ptr(), w.rows, w.cols, w.scale, int(w.is_causal), dt, st)
+        if rc:
+            raise RuntimeError(sms.sms_last_error())
+
+    def bwd():
+        rc = L.sms_backward(y.data_ptr(), dy.data_ptr(), dx.data_ptr(), w.rows, w.cols, w.scale, int(w.is_causal),
+                            dt, st)
+        if rc:
+            raise RuntimeError(sms.sms_last_error())
+
+    fb, bb = fwd_bytes(w, inp), bwd_bytes(w)
+    step_bytes = fb + bb
+    working_set = (x.numel() * 4 * x.element_size()) + (0 if mask is None else mask.numel() * mask.element_size())
+    flush = working_set < 2 * L2_BYTES
+    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device) if flush else None
+
+    for _ in range(max(args.warmup, 3)):
+        fwd()
+        bwd()
+    torch.cuda.synchronize(device)
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(device)
+    if rank == 0:
+        clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    n_launch0 = sms.sms_launch_count()
+    t0.record(stream)
+    for i in range(K):
+        if flush:
+            scratch.add_(1.0)  # evict the previous step's data from L2 (outside the per-kernel events)
+        ev[i][0].record(stream)
+        fwd()
+        ev[i][1].record(stream)
+        bwd()
+        ev[i][2].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    if world > 1:
+        torch.distributed.barrier()
+    n_launch = sms.sms_launch_count() - n_launch0
+    clk = clocks.stop() if rank == 0 else None
+
+    fwd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    bwd_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    region_ms = t0.elapsed_time(t1)
+    kern_ms = sum(fwd_ms) + sum(bwd_ms)
+    # with an L2 flush between steps the step time is the kernels' own time
+    step_ms = (kern_ms if flush else region_ms) / K
+
+    if world > 1:
+        tt = torch.tensor([step_ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(tt.item())
+
+    peak, peak_kind = _peaks()
+    f_ms, b_ms = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
+    kernels = {
+        "forward": {"path": sms.PATH_NAMES[sms.sms_select_path(w.rows, w.cols, dt, False)], "ms": round(f_ms, 4),
+                    "alg_bytes": fb, "gbs": round(fb / f_ms / 1e6, 1), "frac_of_peak": round(fb / f_ms / 1e6 / peak, 4)},
+        "backward": {"path": sms.PATH_NAMES[sms.sms_select_path(w.rows, w.cols, dt, True)], "ms": round(b_ms, 4),
+                     "alg_bytes": bb, "gbs": round(bb / b_ms / 1e6, 1), "frac_of_peak": round(bb / b_ms / 1e6 / peak, 4)},
+    }
+    dom = "backward" if b_ms * K >= f_ms * K else "forward"
+    traffic = _traffic_record(w.name, dom)
+    roof = {"kernel": dom, "bound": "hbm", "achieved": kernels[dom]["gbs"], "peak": peak, "unit": "GB/s",
+            "frac": round(kernels[dom]["gbs"] / peak, 4), "traffic": traffic, "peak_source": peak_kind}
+
+    value = step_bytes * world / (step_ms * 1e6)
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": DTYPE_NAME[x.dtype], "data": "synthetic (seeded, see workloads.py)",
+        "config": {"workload": w.name, "shape": [w.B, w.H, w.S, w.S] if w.rows_override is None else [w.rows, w.S],
+                   "rows": w.rows, "cols": w.cols, "mask": w.mask, "is_causal": w.is_causal,
+                   "step": "forward + backward (dy ~ N(0,1))", "scale": w.scale,
+                   "l2": ("flushed between steps (2x L2 write), step = kernel time" if flush
+                          else "inputs larger than L2, no flush"),
+                   "parallelism": f"replicas x{world} (independent rows per GPU)"},
+        "pct_of_peak": round(100 * value / world / peak, 2),
+        "rows_per_s": round(w.rows * world / (step_ms / 1e3), 1),
+        "kernels": kernels, "roofline": roof, "gpu_launches": int(n_launch),
+        "clocks": clk,
+    }
+    return res, (w, inp, y, dx)
+
+
+def run_e2e(args, w, inp, device, steps):
+    """Same metric through the public API with host buffers: per step, H2D of
+    x (+mask) and dy from pinned memory, forward + backward, D2H of y and dx."""
+    import scaled_masked_softmax_gb300 as sms
+
+    hx = inp["x"].cpu().pin_memory()
+    hm = inp["mask"].cpu().pin_memory() if inp["mask"] is not None else None
+    hdy = inp["dy"].cpu().pin_memory()
+    hy = torch.empty_like(hx).pin_memory()
+    hdx = torch.empty_like(hx).pin_memory()
+    dx_ = torch.empty_like(inp["x"])
+    dm = torch.empty_like(inp["mask"]) if hm is not None else None
+    ddy = torch.empty_like(inp["dy"])
+    dy_ = torch.empty_like(inp["x"])
+    ddx = torch.empty_like(inp["x"])
+    stream = torch.cuda.current_stream(device)
+    shape = (w.B, w.H, w.S, w.S) if w.rows_override is None else (w.rows, w.S)
+
+    def step():
+        dx_.copy_(hx, non_blocking=True)
+        if hm is not None:
+            dm.copy_(hm, non_blocking=True)
+        ddy.copy_(hdy, non_blocking=True)
+        sms.forward(dx_.view(shape), None if dm is None else dm, w.scale, w.is_causal, out=dy_.view(shape))
+        sms.backward(dy_.view(shape), ddy.view(shape), w.scale, w.is_causal, out=ddx.view(shape))
+        hy.copy_(dy_, non_blocking=True)
+        hdx.copy_(ddx, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(device)
+    ms = a.elapsed_time(b) / steps
+    h2d = hx.numel() * hx.element_size() + hdy.numel() * hdy.element_size() + \
+        (0 if hm is None else hm.numel() * hm.element_size())
+    d2h = hy.numel() * hy.element_size() + hdx.numel() * hdx.element_size()
+    alg = fwd_bytes(w, inp) + bwd_bytes(w)
+    return {"value": round(alg / (ms * 1e6), 1), "unit": "GB/s", "ms_per_step": round(ms, 3),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ------------------------------------------------------- oracle on the CPU ---
+
+def _oracle_sample(w, inp_cpu, n_rows, start):
+    import oracle
+
+    rows = np.arange(start, start + n_rows, dtype=np.int64) % w.rows
+    ti = torch.as_tensor(rows)
+    xr = inp_cpu["x"][ti]
+    y = oracle.forward(xr, w.cols, w.scale, w.is_causal, inp_cpu["mask"], inp_cpu["mask_stride_b"],
+                       inp_cpu["mask_stride_h"], inp_cpu["heads"], row_index=rows)
+    dyr = inp_cpu["dy"][ti]
+    oracle.backward(y, dyr, w.cols, w.scale)
+    return rows
+
+
+_PER_ROW = {}
+
+
+def _sample_bytes(w, rows_idx, inp_cpu):
+    """Algorithmic bytes of forward + backward over the sampled rows: the GPU
+    figure's per-row average (same accounting) times the rows processed."""
+    if w.name not in _PER_ROW:
+        _PER_ROW[w.name] = (fwd_bytes(w, inp_cpu) + bwd_bytes(w)) / w.rows
+    return int(_PER_ROW[w.name] * len(rows_idx))
+
+
+def cpu_inputs(w):
+    from scaled_masked_softmax_gb300 import workloads
+
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = workloads.make_inputs(w, device=dev, with_dy=True)
+    return {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+
+
+def run_cpu_baseline(w, inp_cpu, seconds):
+    """Oracle throughput on the host cores over a time-bounded sample of rows."""
+    import oracle
+
+    oracle.build()
+    cores = oracle.num_threads()
+    chunk = max(64, min(4096, int(2_000_000 // w.cols)))
+    t0 = time.perf_counter()
+    done_bytes, n_rows, start = 0, 0, 0
+    while True:
+        idx = _oracle_sample(w, inp_cpu, chunk, start)
+        done_bytes += _sample_bytes(w, idx, inp_cpu)
+        n_rows += chunk
+        start += chunk * 97  # spread the sample over the tensor
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": round(done_bytes / el / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n_rows} rows of {w.name} (fwd+bwd, fp64, {chunk}-row chunks spread over the tensor), "
+                      f"{el:.1f} s", "rows_per_s": round(n_rows / el, 1)}
+
+
+def run_reference(args, rank, world):
+    import oracle
+    from scaled_masked_softmax_gb300 import workloads
+
+    if rank != 0:
+        return None
+    w = workloads.WORKLOADS[args.workload]
+    inp_cpu = cpu_inputs(w)
+    oracle.build()
+    cores = oracle.num_threads()
+    # size each step so the K timed steps take about a minute at most
+    t = time.perf_counter()
+    _oracle_sample(w, inp_cpu, 64, 0)
+    per_row = (time.perf_counter() - t) / 64
+    budget = max(5.0, min(60.0, 4.0 * args.steps))
+    n = int(max(8, min(65536, budget / max(args.steps, 1) / max(per_row, 1e-7))))
+    for i in range(max(args.warmup, 1)):
+        _oracle_sample(w, inp_cpu, n, i * n)
+    t0 = time.perf_counter()
+    tot = 0
+    for i in range(args.steps):
+        idx = _oracle_sample(w, inp_cpu, n, (i + 7) * n * 13)
+        tot += _sample_bytes(w, idx, inp_cpu)
+    el = time.perf_counter() - t0
+    value = tot / el / 1e9
+    sample = f"{n} rows of {w.name} per step (fwd+bwd in fp64), {args.steps} steps"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * el / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, see workloads.py)",
+        "config": {"workload": w.name, "rows": w.rows, "cols": w.cols, "mask": w.mask, "is_causal": w.is_causal,
+                   "step": "forward + backward on a bounded row sample"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# -------------------------------------------------------------------- main ---
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--all", metavar="JSONL", default=None, help="also bench every workload into this file")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend, rank=rank, world_size=world)
+
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    if not torch.cuda.is_available():
+        print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
+        sys.exit(1)
+    device = torch.device("cuda", local)
+    import __graft_entry__
+
+    __graft_entry__.build()
+    res, (w, inp, _y, _dx) = run_ours(args, rank, world, device)
+    if rank == 0:
+        res["e2e"] = run_e2e(args, w, inp, device, args.e2e_steps)
+        if world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = run_cpu_baseline(w, {k: (v.cpu() if isinstance(v, torch.Tensor) else v)
+                                                       for k, v in inp.items()}, args.cpu_seconds)
+        else:
+            res["cpu_baseline"] = None
+    del inp, _y, _dx
+    torch.cuda.empty_cache()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if args.all and rank == 0 and world == 1:
+        from scaled_masked_softmax_gb300 import workloads
+
+        with open(args.all, "w") as f:
+            for name in workloads.WORKLOADS:
+                a2 = argparse.Namespace(**vars(args))
+                a2.workload = name
+                r, (w2, i2, y2, d2) = run_ours(a2, 0, 1, device)
+                r.pop("clocks", None)
+                f.write(json.dumps(r) + "\n")
+                f.flush()
+                del i2, y2, d2
+                torch.cuda.empty_cache()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

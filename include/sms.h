@@ -1,0 +1,154 @@
+/*
+ * sms.h - C ABI of libsms, the GB300 (sm_103a) fused ScaledMaskSoftmax library.
+ *
+ * The operation is defined on the page "用CUDA自定义融合Softmax算子并封装进PyTorch"
+ * (lmnt.cn/news/346102):
+ *   forward  (§1.2 formula, §2.1 max-subtracted form, §2.2 additive mask plus
+ *             causal flag, §3.1 kernel: causal applied after the mask add)
+ *       s_j = x_j * scale + mask_j ;  s_j = -inf if is_causal and j > q
+ *       y_j = exp(s_j - max_k s_k) / sum_k exp(s_k - max_k s_k)
+ *   backward (§3.3 Jacobian derivation)
+ *       dot = sum_j dy_j * y_j ;  dx_j = (dy_j - dot) * y_j * scale
+ * A row whose every score is -inf yields y = 0 (the second article,
+ * pnsm.cn/news/1983787, §4.2 table and §4.3 pitfall 1: never divide such a
+ * row; the all-zero choice is taken).
+ *
+ * Layout.  Every tensor is a dense row-major [rows, cols] view of the
+ * [B, H, S_q, S_k] score tensor with cols = S_k and rows = B*H*S_q (the page's
+ * §4.2 "rows = numel / size(-1)" view).  Row r has query position q = r mod cols
+ * (the page's §3.1 kernel: S_q = S_k), head h = (r / cols) mod heads and batch
+ * b = r / (cols * heads).  rows need not be a multiple of cols.
+ *
+ * Mask.  The additive mask has the dtype of x.  Row r reads the `cols`
+ * contiguous mask elements starting at
+ *       b * mask_stride_b + h * mask_stride_h + q * cols
+ * so [S,S] is (0, 0), [B,1,S,S] is (S*S, 0) and [B,H,S,S] is (H*S*S, S*S)
+ * (the second article's §2.1 input contract).  mask == NULL means no mask
+ * (the page's §2.2: an empty mask means none); then the strides, heads and
+ * mask_numel are ignored.  The mask is not scaled: only x is.
+ *
+ * Numerics.  Inputs are widened to fp32, every step runs in fp32, and the
+ * result is rounded once to the output dtype (round to nearest even) - the
+ * page's §6.3 advice.  Masked and causal positions are written as exact 0.
+ *
+ * Ownership and streams.  The caller owns every buffer; they are device
+ * pointers (cudaMalloc / PyTorch allocations) on the current device.  The
+ * library allocates nothing, never synchronises, and enqueues its kernels on
+ * `stream` (a cudaStream_t passed as void*, NULL = legacy default stream), so
+ * the caller must pass the stream its tensors are used on (the second
+ * article's §4.3 pitfall 3).  Calls are asynchronous: a SMS_OK return means the
+ * launch was accepted.
+ *
+ * Alignment.  x, y, mask, dy and dx must be 16-byte aligned (every CUDA / PyTorch
+ * allocation is); rows may start at any element.
+ *
+ * Errors.  Functions return an sms_status; nothing is thrown across the ABI and
+ * no CUDA error is left pending by a rejected call.  Arguments are validated on
+ * the host before any launch:
+ *   SMS_ERR_INVALID_ARG  NULL x/y (dy/dx), rows < 0, cols <= 0, heads <= 0,
+ *                        unknown dtype, non-finite scale, an unaligned pointer,
+ *                        negative mask strides, a mask extent beyond mask_numel,
+ *                        element counts beyond 2^60, or an output that overlaps
+ *                        an input without being the same buffer.
+ *   SMS_ERR_UNSUPPORTED  a forced path that cannot take the shape.
+ *   SMS_ERR_CUDA         the launch failed (cudaGetLastError after the launch).
+ * sms_last_error() gives a one-line description of the last failure on the
+ * calling host thread.
+ */
+#ifndef SMS_H
+#define SMS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { SMS_F32 = 0, SMS_F16 = 1, SMS_BF16 = 2 } sms_dtype;
+
+typedef enum {
+    SMS_OK = 0,
+    SMS_ERR_INVALID_ARG = 1,
+    SMS_ERR_UNSUPPORTED = 2,
+    SMS_ERR_CUDA = 3
+} sms_status;
+
+/* Kernel families; SMS_PATH_AUTO lets the dispatcher choose by row width. */
+typedef enum {
+    SMS_PATH_AUTO = 0,
+    SMS_PATH_WARP = 1,   /* rows held in registers by a warp (or part of one)          */
+    SMS_PATH_CTA = 2,    /* persistent CTA per row, rows staged by bulk (TMA) copies   */
+    SMS_PATH_ONLINE = 3  /* streaming two pass: online max/sum, then re-read and write */
+} sms_path;
+
+/*
+ * Forward.  y[r, j] = softmax_j(x[r, :] * scale + mask_row(r)) with the causal
+ * override, for r < rows, j < cols (see the top of this file).
+ *   x, y           [rows, cols] device buffers of `dtype`; y may equal x (in place)
+ *   mask           NULL or the additive mask (device, `dtype`), mask_numel elements
+ *   mask_stride_b  elements between batches of the mask (0 = broadcast)
+ *   mask_stride_h  elements between heads of the mask (0 = broadcast)
+ *   heads          H of the [B,H,S,S] view (>= 1); only used to locate mask rows
+ *   scale          multiplier of x (finite), typically 1/sqrt(d_k)
+ *   is_causal      nonzero: positions j > q are masked
+ *   stream         cudaStream_t
+ * rows == 0 is a valid no-op.
+ */
+int sms_forward(const void *x, const void *mask, int64_t mask_numel, int64_t mask_stride_b,
+                int64_t mask_stride_h, int64_t heads, void *y, int64_t rows, int64_t cols, float scale,
+                int is_causal, int dtype, void *stream);
+
+/*
+ * Backward.  dx[r, j] = (dy[r, j] - sum_k dy[r, k] * y[r, k]) * y[r, j] * scale.
+ *   y              forward output [rows, cols] (device, `dtype`)
+ *   dy             upstream gradient [rows, cols] (device, `dtype`)
+ *   dx             result [rows, cols] (device, `dtype`); may equal dy (in place)
+ *   is_causal_hint nonzero promises that y[r, j] == 0 for every j > q (true for a
+ *                  forward run with is_causal); the kernels then skip reading y
+ *                  and dy there and write dx = 0.  For finite dy the result is
+ *                  identical with and without the hint.
+ */
+int sms_backward(const void *y, const void *dy, void *dx, int64_t rows, int64_t cols, float scale,
+                 int is_causal_hint, int dtype, void *stream);
+
+/* Static description of a status code. */
+const char *sms_status_string(int status);
+
+/* One-line description of the last failure on this host thread ("" if none). */
+const char *sms_last_error(void);
+
+/*
+ * Force every later call in this process onto one kernel family (testing and
+ * benchmarking); SMS_PATH_AUTO restores the dispatcher.  Returns the previous
+ * setting, or -1 for an unknown path.  Process-wide, not thread-safe.
+ */
+int sms_set_forced_path(int path);
+
+/* The family the dispatcher would pick for this forward (or backward) shape. */
+int sms_select_path(int64_t rows, int64_t cols, int dtype, int is_backward);
+
+/* The family taken by the last successful call on this host thread. */
+int sms_last_path(void);
+
+/*
+ * Number of kernel launches made by successful calls since load, process-wide
+ * (each sms_forward / sms_backward enqueues exactly one kernel when rows > 0).
+ */
+int64_t sms_launch_count(void);
+
+/*
+ * Reads (and clears) the device-side error word of the current device after
+ * synchronising `stream`.  Nonzero means a kernel gave up on a bounded wait
+ * for its own bulk copies (1 = consumer wait, 2 = producer wait); its output
+ * is then incomplete.  Returns -1 if the read itself failed.
+ */
+int sms_device_error(void *stream);
+
+/* ABI version: 100 * major + minor. */
+int sms_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SMS_H */

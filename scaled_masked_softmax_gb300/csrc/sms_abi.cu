@@ -1,0 +1,316 @@
+// C ABI of libsms: host-side argument validation, kernel-family dispatch,
+// status reporting.  See include/sms.h for the contract of every entry point.
+#include "sms.h"
+#include "sms_internal.h"
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+namespace sms {
+
+// Error word written by kernels whose bounded waits expire (one per device;
+// its address is looked up once per device and passed to the kernels).
+__device__ int g_device_error = 0;
+
+namespace {
+
+thread_local char t_err[256] = "";
+thread_local int t_last_path = SMS_PATH_AUTO;
+std::atomic<int> g_forced{SMS_PATH_AUTO};
+std::atomic<int64_t> g_launches{0};
+
+constexpr int kMaxDevices = 64;
+std::once_flag g_dev_once[kMaxDevices];
+int g_dev_sms[kMaxDevices];
+int *g_dev_err[kMaxDevices];
+cudaError_t g_dev_status[kMaxDevices];
+
+int fail(int status, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+int fail(int status, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_err, sizeof(t_err), fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+// Per-device facts, looked up once with that device current.
+cudaError_t device_info(int &dev, int &sms, int *&err)
+{
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::call_once(g_dev_once[dev], [dev] {
+        int n = 0;
+        cudaError_t s = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        void *p = nullptr;
+        if (s == cudaSuccess) s = cudaGetSymbolAddress(&p, g_device_error);
+        g_dev_sms[dev] = n;
+        g_dev_err[dev] = static_cast<int *>(p);
+        g_dev_status[dev] = s;
+    });
+    sms = g_dev_sms[dev];
+    err = g_dev_err[dev];
+    return g_dev_status[dev];
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// [a, a+na) and [b, b+nb) share a byte (both non-empty).
+bool overlap(const void *a, int64_t na, const void *b, int64_t nb)
+{
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return pa < pb + (uintptr_t)nb && pb < pa + (uintptr_t)na;
+}
+
+// Largest mask element any row touches, plus one (see sms.h for the row rule).
+int64_t mask_extent(int64_t rows, int64_t cols, int64_t heads, int64_t sb, int64_t sh)
+{
+    auto off = [&](int64_t r) {
+        return (r / (cols * heads)) * sb + ((r / cols) % heads) * sh + (r % cols) * cols;
+    };
+    const int64_t last = rows - 1;
+    int64_t m = off(last);
+    const int64_t b = last / (cols * heads), h = (last / cols) % heads;
+    if (h > 0) m = std::max(m, off((b * heads + h) * cols - 1));
+    if (b > 0) m = std::max(m, off(b * heads * cols - 1));
+    return m + cols;
+}
+
+const char *cuda_msg(cudaError_t e) { return cudaGetErrorString(e); }
+
+int launch_status(cudaError_t e, const char *what)
+{
+    if (e == cudaSuccess) {
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+        return SMS_OK;
+    }
+    cudaGetLastError();  // leave no error pending from this launch
+    if (e == cudaErrorNotSupported) return fail(SMS_ERR_UNSUPPORTED, "%s: shape not supported by the path", what);
+    return fail(SMS_ERR_CUDA, "%s: launch failed: %s", what, cuda_msg(e));
+}
+
+constexpr int64_t kMaxCols = (int64_t)1 << 30;
+constexpr int64_t kMaxElems = (int64_t)1 << 60;
+
+int pick_path(int forced, int64_t cols, int dtype, bool aligned, bool bwd)
+{
+    if (forced != SMS_PATH_AUTO) return forced;
+    // Warp-resident rows up to 1024 elements; wider rows go to the staged
+    // CTA path while they fit its registers; beyond that, stream twice.
+    if (cols <= 1024 && warp_fits(cols, dtype, aligned)) return SMS_PATH_WARP;
+    if (bwd ? cta_fits_bwd(cols, dtype) : cta_fits(cols, dtype)) return SMS_PATH_CTA;
+    return SMS_PATH_ONLINE;
+}
+
+}  // namespace
+
+int sm_count()
+{
+    int dev = 0, n = 0;
+    int *err = nullptr;
+    if (device_info(dev, n, err) != cudaSuccess || n <= 0) return 148;
+    return n;
+}
+
+}  // namespace sms
+
+using namespace sms;
+
+extern "C" {
+
+int sms_version(void) { return 100; }
+
+const char *sms_status_string(int status)
+{
+    switch (status) {
+    case SMS_OK: return "ok";
+    case SMS_ERR_INVALID_ARG: return "invalid argument";
+    case SMS_ERR_UNSUPPORTED: return "unsupported by the selected path";
+    case SMS_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+    }
+}
+
+const char *sms_last_error(void) { return t_err; }
+
+int sms_set_forced_path(int path)
+{
+    if (path < SMS_PATH_AUTO || path > SMS_PATH_ONLINE) return -1;
+    return g_forced.exchange(path);
+}
+
+int sms_last_path(void) { return t_last_path; }
+
+int64_t sms_launch_count(void) { return g_launches.load(); }
+
+int sms_select_path(int64_t rows, int64_t cols, int dtype, int is_backward)
+{
+    (void)rows;
+    if (cols <= 0 || dtype < SMS_F32 || dtype > SMS_BF16) return -1;
+    const bool aligned = cols % vec_elems(dtype) == 0;
+    return pick_path(SMS_PATH_AUTO, cols, dtype, aligned, is_backward != 0);
+}
+
+int sms_forward(const void *x, const void *mask, int64_t mask_numel, int64_t mask_stride_b, int64_t mask_stride_h,
+                int64_t heads, void *y, int64_t rows, int64_t cols, float scale, int is_causal, int dtype,
+                void *stream)
+{
+    t_err[0] = '\0';
+    if (dtype < SMS_F32 || dtype > SMS_BF16) return fail(SMS_ERR_INVALID_ARG, "sms_forward: unknown dtype %d", dtype);
+    if (!x || !y) return fail(SMS_ERR_INVALID_ARG, "sms_forward: x and y must not be NULL");
+    if (rows < 0) return fail(SMS_ERR_INVALID_ARG, "sms_forward: rows < 0");
+    if (cols <= 0 || cols > kMaxCols) return fail(SMS_ERR_INVALID_ARG, "sms_forward: cols must be in [1, 2^30]");
+    if (rows > 0 && rows > kMaxElems / cols) return fail(SMS_ERR_INVALID_ARG, "sms_forward: rows*cols too large");
+    if (!std::isfinite(scale)) return fail(SMS_ERR_INVALID_ARG, "sms_forward: scale must be finite");
+    if (!aligned16(x) || !aligned16(y)) return fail(SMS_ERR_INVALID_ARG, "sms_forward: x and y must be 16-byte aligned");
+    const int eb = elem_bytes(dtype);
+    const int64_t total = rows * cols;
+    if (x != y && overlap(x, total * eb, y, total * eb))
+        return fail(SMS_ERR_INVALID_ARG, "sms_forward: y partially overlaps x");
+    if (mask) {
+        if (heads <= 0 || heads > ((int64_t)1 << 31)) return fail(SMS_ERR_INVALID_ARG, "sms_forward: heads must be in [1, 2^31]");
+        if (mask_stride_b < 0 || mask_stride_h < 0)
+            return fail(SMS_ERR_INVALID_ARG, "sms_forward: mask strides must be >= 0");
+        if (!aligned16(mask)) return fail(SMS_ERR_INVALID_ARG, "sms_forward: mask must be 16-byte aligned");
+        if (mask_numel < 0 || mask_numel > kMaxElems) return fail(SMS_ERR_INVALID_ARG, "sms_forward: bad mask_numel");
+        if (rows > 0) {
+            // guard the extent arithmetic against overflow before evaluating it
+            const double est = (double)(rows / (cols * heads) + 1) * (double)mask_stride_b +
+                               (double)heads * (double)mask_stride_h + (double)cols * (double)cols;
+            if (est > 4e18) return fail(SMS_ERR_INVALID_ARG, "sms_forward: mask strides too large");
+            const int64_t ext = mask_extent(rows, cols, heads, mask_stride_b, mask_stride_h);
+            if (ext > mask_numel)
+                return fail(SMS_ERR_INVALID_ARG, "sms_forward: rows reach mask element %lld but mask_numel is %lld",
+                            (long long)ext - 1, (long long)mask_numel);
+            if (overlap(mask, mask_numel * eb, y, total * eb))
+                return fail(SMS_ERR_INVALID_ARG, "sms_forward: y overlaps the mask");
+        }
+    } else if (heads <= 0) {
+        heads = 1;
+    }
+    if (rows == 0) {
+        t_last_path = SMS_PATH_AUTO;
+        return SMS_OK;
+    }
+
+    int dev = 0, nsm = 0;
+    int *err = nullptr;
+    cudaError_t e = device_info(dev, nsm, err);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SMS_ERR_CUDA, "sms_forward: device query failed: %s", cuda_msg(e));
+    }
+
+    const int vec = vec_elems(dtype);
+    const bool aligned = cols % vec == 0 && (!mask || (mask_stride_b % vec == 0 && mask_stride_h % vec == 0));
+    FwdArgs a;
+    a.x = x; a.mask = mask; a.y = y;
+    a.rows = rows; a.cols = cols; a.x_total = total;
+    a.mask_total = mask ? mask_numel : 0;
+    a.msb = mask ? mask_stride_b : 0; a.msh = mask ? mask_stride_h : 0; a.heads = heads;
+    a.scale = scale; a.causal = is_causal ? 1 : 0; a.err = err;
+
+    const int path = pick_path(g_forced.load(), cols, dtype, aligned, false);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (path) {
+    case SMS_PATH_WARP:
+        if (!warp_fits(cols, dtype, aligned)) return fail(SMS_ERR_UNSUPPORTED, "sms_forward: row too wide for the warp path");
+        e = launch_fwd_warp(a, dtype, aligned, st);
+        break;
+    case SMS_PATH_CTA:
+        if (!cta_fits(cols, dtype)) return fail(SMS_ERR_UNSUPPORTED, "sms_forward: row too wide for the CTA path");
+        e = launch_fwd_cta(a, dtype, st);
+        break;
+    default:
+        e = launch_fwd_online(a, dtype, st);
+        break;
+    }
+    const int rc = launch_status(e, "sms_forward");
+    if (rc == SMS_OK) t_last_path = path;
+    return rc;
+}
+
+int sms_backward(const void *y, const void *dy, void *dx, int64_t rows, int64_t cols, float scale,
+                 int is_causal_hint, int dtype, void *stream)
+{
+    t_err[0] = '\0';
+    if (dtype < SMS_F32 || dtype > SMS_BF16) return fail(SMS_ERR_INVALID_ARG, "sms_backward: unknown dtype %d", dtype);
+    if (!y || !dy || !dx) return fail(SMS_ERR_INVALID_ARG, "sms_backward: y, dy and dx must not be NULL");
+    if (rows < 0) return fail(SMS_ERR_INVALID_ARG, "sms_backward: rows < 0");
+    if (cols <= 0 || cols > kMaxCols) return fail(SMS_ERR_INVALID_ARG, "sms_backward: cols must be in [1, 2^30]");
+    if (rows > 0 && rows > kMaxElems / cols) return fail(SMS_ERR_INVALID_ARG, "sms_backward: rows*cols too large");
+    if (!std::isfinite(scale)) return fail(SMS_ERR_INVALID_ARG, "sms_backward: scale must be finite");
+    if (!aligned16(y) || !aligned16(dy) || !aligned16(dx))
+        return fail(SMS_ERR_INVALID_ARG, "sms_backward: y, dy and dx must be 16-byte aligned");
+    const int eb = elem_bytes(dtype);
+    const int64_t total = rows * cols;
+    if (overlap(dx, total * eb, y, total * eb)) return fail(SMS_ERR_INVALID_ARG, "sms_backward: dx overlaps y");
+    if (dx != dy && overlap(dx, total * eb, dy, total * eb))
+        return fail(SMS_ERR_INVALID_ARG, "sms_backward: dx partially overlaps dy");
+    if (rows == 0) {
+        t_last_path = SMS_PATH_AUTO;
+        return SMS_OK;
+    }
+
+    int dev = 0, nsm = 0;
+    int *err = nullptr;
+    cudaError_t e = device_info(dev, nsm, err);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SMS_ERR_CUDA, "sms_backward: device query failed: %s", cuda_msg(e));
+    }
+
+    const bool aligned = cols % vec_elems(dtype) == 0;
+    BwdArgs a;
+    a.y = y; a.dy = dy; a.dx = dx;
+    a.rows = rows; a.cols = cols; a.total = total;
+    a.scale = scale; a.causal = is_causal_hint ? 1 : 0; a.err = err;
+
+    const int path = pick_path(g_forced.load(), cols, dtype, aligned, true);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (path) {
+    case SMS_PATH_WARP:
+        if (!warp_fits(cols, dtype, aligned)) return fail(SMS_ERR_UNSUPPORTED, "sms_backward: row too wide for the warp path");
+        e = launch_bwd_warp(a, dtype, aligned, st);
+        break;
+    case SMS_PATH_CTA:
+        if (!cta_fits_bwd(cols, dtype)) return fail(SMS_ERR_UNSUPPORTED, "sms_backward: row too wide for the CTA path");
+        e = launch_bwd_cta(a, dtype, st);
+        break;
+    default:
+        e = launch_bwd_online(a, dtype, st);
+        break;
+    }
+    const int rc = launch_status(e, "sms_backward");
+    if (rc == SMS_OK) t_last_path = path;
+    return rc;
+}
+
+int sms_device_error(void *stream)
+{
+    int dev = 0, nsm = 0;
+    int *err = nullptr;
+    if (device_info(dev, nsm, err) != cudaSuccess || !err) {
+        cudaGetLastError();
+        return -1;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int v = 0;
+    const int zero = 0;
+    if (cudaMemcpyAsync(&v, err, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemcpyAsync(err, &zero, sizeof(int), cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    return v;
+}
+
+}  // extern "C"

@@ -1,0 +1,60 @@
+// Host-side interface between the C ABI (sms_abi.cu) and the kernel families.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sms {
+
+// dtype codes, equal to sms_dtype in include/sms.h
+enum { kF32 = 0, kF16 = 1, kBF16 = 2 };
+
+inline int vec_elems(int dtype) { return dtype == kF32 ? 4 : 8; }
+inline int elem_bytes(int dtype) { return dtype == kF32 ? 4 : 2; }
+
+struct FwdArgs {
+    const void *x;
+    const void *mask;      // nullptr: no mask
+    void *y;
+    int64_t rows, cols;
+    int64_t x_total;       // rows * cols
+    int64_t mask_total;    // elements in the mask buffer
+    int64_t msb, msh, heads;
+    float scale;
+    int causal;
+    int *err;              // device error word
+};
+
+struct BwdArgs {
+    const void *y;
+    const void *dy;
+    void *dx;
+    int64_t rows, cols;
+    int64_t total;         // rows * cols
+    float scale;
+    int causal;            // the causal hint: y == 0 beyond the diagonal
+    int *err;
+};
+
+// "aligned" means every row (and every mask row) starts on a 16-byte boundary:
+// cols and both mask strides are multiples of the 16-byte vector width.
+
+// warp-per-row (or a power-of-two part of a warp per row), rows in registers
+bool warp_fits(int64_t cols, int dtype, bool aligned);
+cudaError_t launch_fwd_warp(const FwdArgs &a, int dtype, bool aligned, cudaStream_t st);
+cudaError_t launch_bwd_warp(const BwdArgs &a, int dtype, bool aligned, cudaStream_t st);
+
+// persistent CTA per row, bulk-copy (TMA) staging ring, rows in registers
+bool cta_fits(int64_t cols, int dtype);      // forward
+bool cta_fits_bwd(int64_t cols, int dtype);  // backward (y and dy both held)
+cudaError_t launch_fwd_cta(const FwdArgs &a, int dtype, cudaStream_t st);
+cudaError_t launch_bwd_cta(const BwdArgs &a, int dtype, cudaStream_t st);
+
+// streaming two pass, any row length
+cudaError_t launch_fwd_online(const FwdArgs &a, int dtype, cudaStream_t st);
+cudaError_t launch_bwd_online(const BwdArgs &a, int dtype, cudaStream_t st);
+
+// multiprocessor count of the current device (cached per device)
+int sm_count();
+
+}  // namespace sms

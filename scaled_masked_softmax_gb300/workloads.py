@@ -32,7 +32,7 @@ class Workload:
     dtype: str                 # "f32" | "f16" | "bf16"
     sigma: float               # x ~ N(0, sigma^2)
     scale: float               # float32 value handed to the kernel
-    mask: str                  # "none" | "B1SS" (key padding) | "SS" (random broadcast)
+    mask: str                  # "none" | "B1SS" (key padding) | "SS" (random broadcast) | "BHSS" (full, tests)
     is_causal: bool
     backward: bool             # the workload also runs the backward
     seed: int
@@ -42,6 +42,7 @@ class Workload:
     spike_frac: float = 0.0    # fraction of rows that get one +spike_value score
     spike_value: float = 6.0e4
     rows_override: Optional[int] = None  # rows not equal to B*H*S (the width sweep)
+    mask_values: str = "zero"  # kept mask entries: "zero" or "normal" (N(0,1), tests only)
 
     @property
     def rows(self) -> int:
@@ -63,13 +64,17 @@ class Workload:
         """(mask_stride_b, mask_stride_h, heads) of the additive mask."""
         if self.mask == "B1SS":
             return self.S * self.S, 0, self.H
+        if self.mask == "BHSS":
+            return self.H * self.S * self.S, self.S * self.S, self.H
         return 0, 0, self.H
 
     def mask_shape(self):
         if self.mask == "B1SS":
             return (self.B, 1, self.S, self.S)
         if self.mask == "SS":
-            return (self.S, self.S)
+            return (min(self.S, self.rows), self.S)
+        if self.mask == "BHSS":
+            return (self.B, self.H, self.S, self.S)
         return None
 
 
@@ -152,10 +157,22 @@ def make_inputs(w: Workload, device="cpu", with_dy: Optional[bool] = None):
         keep = cols_idx[None, :] < L.to(dev)[:, None]  # [B, S]
         mrow = torch.where(keep, torch.tensor(0.0, device=dev), torch.tensor(w.pad_fill, device=dev))
         mask = mrow[:, None, None, :].expand(w.B, 1, S, S).to(dt).contiguous()
+    elif w.mask == "BHSS":
+        drop = torch.rand(w.B, w.H, S, S, generator=g_dev, device=dev) < w.drop_p
+        drop[..., 0] = False
+        vals = torch.randn(w.B, w.H, S, S, generator=g_dev, device=dev) if w.mask_values == "normal" else \
+            torch.zeros(w.B, w.H, S, S, device=dev)
+        mask = torch.where(drop, torch.tensor(w.pad_fill, device=dev), vals).to(dt)
     elif w.mask == "SS":
-        drop = torch.rand(S, S, generator=g_dev, device=dev) < w.drop_p
+        # only the first min(rows, S) query rows of an [S,S] mask are ever read
+        # (row r reads mask row r mod S), so only those are materialised
+        drop = torch.rand(min(S, rows), S, generator=g_dev, device=dev) < w.drop_p
         drop[:, 0] = False
         mask = torch.where(drop, torch.tensor(w.pad_fill, device=dev), torch.tensor(0.0, device=dev)).to(dt)
+        if w.mask_values == "normal":  # finite additive values as well as dropped entries
+            vals = torch.randn(min(S, rows), S, generator=g_dev, device=dev)
+            mask = torch.where(drop, torch.tensor(w.pad_fill, device=dev), vals).to(dt)
+            mask[:, 0] = 0
 
     dy = None
     if with_dy:

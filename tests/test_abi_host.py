@@ -1,0 +1,140 @@
+"""Host-side checks of the C ABI (no GPU needed, no compute calls).
+
+The library must load, export every function include/sms.h declares, and
+reject bad arguments on the host before any launch.  Pointer arguments here
+are fake addresses: every call is rejected by validation before anything is
+dereferenced or launched.
+"""
+import os
+import re
+
+import pytest
+import torch
+
+import scaled_masked_softmax_gb300 as sms
+from scaled_masked_softmax_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sms.h")
+INVALID, UNSUPPORTED = binding.SMS_ERR_INVALID_ARG, binding.SMS_ERR_UNSUPPORTED
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sms_\w+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = binding.lib()
+    names = _declared()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), f"libsms.so does not export {n}"
+    assert set(names) == set(binding.SIGNATURES), "binding signatures out of sync with include/sms.h"
+    assert sms.sms_version() == 100
+
+
+def _fwd(**kw):
+    a = dict(x=0x10000, mask=None, mask_numel=0, sb=0, sh=0, heads=1, y=0x20000, rows=4, cols=8, scale=1.0,
+             causal=0, dtype=0, stream=None)
+    a.update(kw)
+    return binding.lib().sms_forward(a["x"], a["mask"], a["mask_numel"], a["sb"], a["sh"], a["heads"], a["y"],
+                                     a["rows"], a["cols"], a["scale"], a["causal"], a["dtype"], a["stream"])
+
+
+def _bwd(**kw):
+    a = dict(y=0x10000, dy=0x20000, dx=0x30000, rows=4, cols=8, scale=1.0, causal=0, dtype=0, stream=None)
+    a.update(kw)
+    return binding.lib().sms_backward(a["y"], a["dy"], a["dx"], a["rows"], a["cols"], a["scale"], a["causal"],
+                                      a["dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("kw", [
+    dict(x=None), dict(y=None), dict(dtype=3), dict(dtype=-1), dict(rows=-1), dict(cols=0), dict(cols=-5),
+    dict(cols=(1 << 30) + 1), dict(rows=1 << 40, cols=1 << 30), dict(scale=float("inf")), dict(scale=float("nan")),
+    dict(x=0x10004), dict(y=0x20008), dict(y=0x10010),  # misaligned, partial overlap of y and x
+    dict(mask=0x40000, mask_numel=8 * 8 - 1, cols=8, rows=8),  # [S,S] mask one element short
+    dict(mask=0x40000, mask_numel=64, heads=0), dict(mask=0x40000, mask_numel=64, sb=-1),
+    dict(mask=0x40004, mask_numel=64),  # misaligned mask
+    dict(mask=0x40000, mask_numel=64, rows=16, cols=8, sb=64, heads=1),  # 2 batches, extent 128 > 64
+    dict(mask=0x1ffe0, mask_numel=64, rows=8, cols=8),  # y overlaps the mask
+])
+def test_forward_rejects_bad_arguments(kw):
+    assert _fwd(**kw) == INVALID
+    assert binding.sms_last_error() != ""
+
+
+@pytest.mark.parametrize("kw", [
+    dict(y=None), dict(dy=None), dict(dx=None), dict(dtype=7), dict(rows=-2), dict(cols=0),
+    dict(scale=float("nan")), dict(dx=0x30008), dict(dx=0x10010), dict(dx=0x20010)])
+def test_backward_rejects_bad_arguments(kw):
+    assert _bwd(**kw) == INVALID
+
+
+def test_rows_zero_is_a_noop_without_device():
+    assert _fwd(rows=0) == binding.SMS_OK
+    assert _bwd(rows=0) == binding.SMS_OK
+
+
+def test_in_place_aliasing_passes_validation():
+    # y == x and dx == dy are allowed; without a GPU the call then fails at the
+    # device query (SMS_ERR_CUDA), never at validation
+    if torch.cuda.is_available():
+        pytest.skip("host-only check")
+    assert _fwd(y=0x10000) == binding.SMS_ERR_CUDA
+    assert _bwd(dx=0x20000) == binding.SMS_ERR_CUDA
+
+
+def test_mask_extent_rule_for_partial_heads():
+    # rows = 1.5 heads of S=8 with a [B,H,S,S] mask: the extent is the last
+    # row's offset + cols, not B*H*S*S
+    if torch.cuda.is_available():
+        pytest.skip("host-only check")
+    S, Hh = 8, 2
+    rows = 12  # head 0 full, head 1 rows 0..3
+    need = 1 * S * S + 3 * S + S  # h=1, q=3
+    assert _fwd(mask=0x40000, mask_numel=need - 1, rows=rows, cols=S, heads=Hh, sb=Hh * S * S, sh=S * S) == INVALID
+    assert _fwd(mask=0x40000, mask_numel=need, rows=rows, cols=S, heads=Hh, sb=Hh * S * S, sh=S * S) == \
+        binding.SMS_ERR_CUDA
+
+
+def test_status_strings_and_forced_path():
+    for st in range(4):
+        assert sms.sms_status_string(st)
+    prev = sms.sms_set_forced_path(sms.SMS_PATH_CTA)
+    assert sms.sms_set_forced_path(prev) == sms.SMS_PATH_CTA
+    with pytest.raises(ValueError):
+        sms.sms_set_forced_path(9)
+
+
+def test_dispatcher_thresholds():
+    W, C, O = sms.SMS_PATH_WARP, sms.SMS_PATH_CTA, sms.SMS_PATH_ONLINE
+    for dt in (0, 1, 2):
+        assert sms.sms_select_path(1000, 64, dt) == W
+        assert sms.sms_select_path(1000, 1024, dt) == W
+        assert sms.sms_select_path(1000, 4096, dt) == C
+        assert sms.sms_select_path(1000, 16384, dt) == C
+        assert sms.sms_select_path(1000, 1 << 20, dt) == O
+        assert sms.sms_select_path(1000, 1 << 20, dt, True) == O
+    assert sms.sms_select_path(1, 0, 0) == -1
+
+
+@pytest.mark.parametrize("x_shape,m_shape,want", [
+    ((2, 3, 8, 8), (8, 8), (0, 0, 3)),
+    ((2, 3, 8, 8), (2, 1, 8, 8), (64, 0, 3)),
+    ((2, 3, 8, 8), (2, 3, 8, 8), (192, 64, 3)),
+    ((2, 3, 8, 8), (1, 3, 8, 8), (0, 64, 3)),
+    ((2, 3, 8, 8), (1, 1, 8, 8), (0, 0, 3)),
+    ((3, 8, 8), (3, 8, 8), (0, 64, 3)),
+    ((4, 2, 3, 8, 8), (4, 2, 1, 8, 8), (64, 0, 3)),
+])
+def test_mask_layout(x_shape, m_shape, want):
+    assert sms.mask_layout(x_shape, m_shape) == want
+
+
+@pytest.mark.parametrize("x_shape,m_shape", [((2, 3, 8, 8), (3, 1, 8, 8)), ((2, 3, 8, 8), (2, 2, 8, 8)),
+                                             ((2, 3, 8, 8), (8, 7)), ((4, 2, 3, 8, 8), (4, 1, 1, 8, 8))])
+def test_mask_layout_rejects(x_shape, m_shape):
+    with pytest.raises(ValueError):
+        sms.mask_layout(x_shape, m_shape)
