@@ -210,7 +210,10 @@ def run_ours(args, rank, world, device):
 
     for _ in range(max(args.warmup, 3)):
         fwd()
+        fp = sms.sms_last_path()
         bwd()
+        bp = sms.sms_last_path()
+    taken = (fp, bp)
     torch.cuda.synchronize(device)
 
     K = args.steps
@@ -255,10 +258,11 @@ def run_ours(args, rank, world, device):
 
     peak, peak_kind = _peaks()
     f_ms, b_ms = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
+    fwd_path, bwd_path = taken
     kernels = {
-        "forward": {"path": sms.PATH_NAMES[sms.sms_select_path(w.rows, w.cols, dt, False)], "ms": round(f_ms, 4),
+        "forward": {"path": sms.PATH_NAMES[fwd_path], "ms": round(f_ms, 4),
                     "alg_bytes": fb, "gbs": round(fb / f_ms / 1e6, 1), "frac_of_peak": round(fb / f_ms / 1e6 / peak, 4)},
-        "backward": {"path": sms.PATH_NAMES[sms.sms_select_path(w.rows, w.cols, dt, True)], "ms": round(b_ms, 4),
+        "backward": {"path": sms.PATH_NAMES[bwd_path], "ms": round(b_ms, 4),
                      "alg_bytes": bb, "gbs": round(bb / b_ms / 1e6, 1), "frac_of_peak": round(bb / b_ms / 1e6 / peak, 4)},
     }
     dom = "backward" if b_ms * K >= f_ms * K else "forward"
@@ -439,6 +443,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--all", metavar="JSONL", default=None, help="also bench every workload into this file")
+    ap.add_argument("--path", choices=["auto", "warp", "cta", "online"], default="auto",
+                    help="force one kernel family (tuning); the default lets the dispatcher choose")
+    ap.add_argument("--all-paths", action="store_true", help="with --all: every kernel family per workload")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -464,6 +471,10 @@ def main():
     import __graft_entry__
 
     __graft_entry__.build()
+    import scaled_masked_softmax_gb300 as sms
+
+    path_code = {"auto": 0, "warp": 1, "cta": 2, "online": 3}
+    sms.sms_set_forced_path(path_code[args.path])
     res, (w, inp, _y, _dx) = run_ours(args, rank, world, device)
     if rank == 0:
         res["e2e"] = run_e2e(args, w, inp, device, args.e2e_steps)
@@ -479,16 +490,26 @@ def main():
     if args.all and rank == 0 and world == 1:
         from scaled_masked_softmax_gb300 import workloads
 
+        paths = ["auto", "warp", "cta", "online"] if args.all_paths else [args.path]
         with open(args.all, "w") as f:
             for name in workloads.WORKLOADS:
-                a2 = argparse.Namespace(**vars(args))
-                a2.workload = name
-                r, (w2, i2, y2, d2) = run_ours(a2, 0, 1, device)
-                r.pop("clocks", None)
-                f.write(json.dumps(r) + "\n")
-                f.flush()
-                del i2, y2, d2
-                torch.cuda.empty_cache()
+                for pth in paths:
+                    a2 = argparse.Namespace(**vars(args))
+                    a2.workload = name
+                    sms.sms_set_forced_path(path_code[pth])
+                    try:
+                        r, (w2, i2, y2, d2) = run_ours(a2, 0, 1, device)
+                    except RuntimeError as e:  # the forced family cannot take this width
+                        f.write(json.dumps({"workload": name, "path": pth, "skipped": str(e)}) + "\n")
+                        torch.cuda.empty_cache()
+                        continue
+                    r.pop("clocks", None)
+                    r["forced_path"] = pth
+                    f.write(json.dumps(r) + "\n")
+                    f.flush()
+                    del i2, y2, d2
+                    torch.cuda.empty_cache()
+            sms.sms_set_forced_path(0)
     if world > 1:
         torch.distributed.destroy_process_group()
 

@@ -92,7 +92,7 @@ typedef enum {
  *   scale          multiplier of x (finite), typically 1/sqrt(d_k)
  *   is_causal      nonzero: positions j > q are masked
  *   stream         cudaStream_t
- * rows == 0 is a valid no-op.
+ * rows == 0 (with cols >= 1) is a valid no-op; the pointers may then be NULL.
  */
 int sms_forward(const void *x, const void *mask, int64_t mask_numel, int64_t mask_stride_b,
                 int64_t mask_stride_h, int64_t heads, void *y, int64_t rows, int64_t cols, float scale,
@@ -107,6 +107,7 @@ int sms_forward(const void *x, const void *mask, int64_t mask_numel, int64_t mas
  *                  forward run with is_causal); the kernels then skip reading y
  *                  and dy there and write dx = 0.  For finite dy the result is
  *                  identical with and without the hint.
+ * rows == 0 (with cols >= 1) is a valid no-op; the pointers may then be NULL.
  */
 int sms_backward(const void *y, const void *dy, void *dx, int64_t rows, int64_t cols, float scale,
                  int is_causal_hint, int dtype, void *stream);

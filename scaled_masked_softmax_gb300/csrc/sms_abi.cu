@@ -105,7 +105,7 @@ int pick_path(int forced, int64_t cols, int dtype, bool aligned, bool bwd)
     // Warp-resident rows up to 1024 elements; wider rows go to the staged
     // CTA path while they fit its registers; beyond that, stream twice.
     if (cols <= 1024 && warp_fits(cols, dtype, aligned)) return SMS_PATH_WARP;
-    if (bwd ? cta_fits_bwd(cols, dtype) : cta_fits(cols, dtype)) return SMS_PATH_CTA;
+    if (bwd ? cta_fits_bwd(cols, dtype, aligned) : cta_fits(cols, dtype, aligned)) return SMS_PATH_CTA;
     return SMS_PATH_ONLINE;
 }
 
@@ -164,8 +164,12 @@ int sms_forward(const void *x, const void *mask, int64_t mask_numel, int64_t mas
 {
     t_err[0] = '\0';
     if (dtype < SMS_F32 || dtype > SMS_BF16) return fail(SMS_ERR_INVALID_ARG, "sms_forward: unknown dtype %d", dtype);
-    if (!x || !y) return fail(SMS_ERR_INVALID_ARG, "sms_forward: x and y must not be NULL");
     if (rows < 0) return fail(SMS_ERR_INVALID_ARG, "sms_forward: rows < 0");
+    if (rows == 0 && cols > 0) {  // empty problem: nothing is read, pointers may be NULL
+        t_last_path = SMS_PATH_AUTO;
+        return SMS_OK;
+    }
+    if (!x || !y) return fail(SMS_ERR_INVALID_ARG, "sms_forward: x and y must not be NULL");
     if (cols <= 0 || cols > kMaxCols) return fail(SMS_ERR_INVALID_ARG, "sms_forward: cols must be in [1, 2^30]");
     if (rows > 0 && rows > kMaxElems / cols) return fail(SMS_ERR_INVALID_ARG, "sms_forward: rows*cols too large");
     if (!std::isfinite(scale)) return fail(SMS_ERR_INVALID_ARG, "sms_forward: scale must be finite");
@@ -216,6 +220,8 @@ int sms_forward(const void *x, const void *mask, int64_t mask_numel, int64_t mas
     a.mask_total = mask ? mask_numel : 0;
     a.msb = mask ? mask_stride_b : 0; a.msh = mask ? mask_stride_h : 0; a.heads = heads;
     a.scale = scale; a.causal = is_causal ? 1 : 0; a.err = err;
+    a.dcols = FastDiv((uint32_t)cols);
+    a.dheads = FastDiv((uint32_t)heads);
 
     const int path = pick_path(g_forced.load(), cols, dtype, aligned, false);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -225,8 +231,8 @@ int sms_forward(const void *x, const void *mask, int64_t mask_numel, int64_t mas
         e = launch_fwd_warp(a, dtype, aligned, st);
         break;
     case SMS_PATH_CTA:
-        if (!cta_fits(cols, dtype)) return fail(SMS_ERR_UNSUPPORTED, "sms_forward: row too wide for the CTA path");
-        e = launch_fwd_cta(a, dtype, st);
+        if (!cta_fits(cols, dtype, aligned)) return fail(SMS_ERR_UNSUPPORTED, "sms_forward: row too wide for the CTA path");
+        e = launch_fwd_cta(a, dtype, aligned, st);
         break;
     default:
         e = launch_fwd_online(a, dtype, st);
@@ -242,8 +248,12 @@ int sms_backward(const void *y, const void *dy, void *dx, int64_t rows, int64_t 
 {
     t_err[0] = '\0';
     if (dtype < SMS_F32 || dtype > SMS_BF16) return fail(SMS_ERR_INVALID_ARG, "sms_backward: unknown dtype %d", dtype);
-    if (!y || !dy || !dx) return fail(SMS_ERR_INVALID_ARG, "sms_backward: y, dy and dx must not be NULL");
     if (rows < 0) return fail(SMS_ERR_INVALID_ARG, "sms_backward: rows < 0");
+    if (rows == 0 && cols > 0) {  // empty problem: nothing is read, pointers may be NULL
+        t_last_path = SMS_PATH_AUTO;
+        return SMS_OK;
+    }
+    if (!y || !dy || !dx) return fail(SMS_ERR_INVALID_ARG, "sms_backward: y, dy and dx must not be NULL");
     if (cols <= 0 || cols > kMaxCols) return fail(SMS_ERR_INVALID_ARG, "sms_backward: cols must be in [1, 2^30]");
     if (rows > 0 && rows > kMaxElems / cols) return fail(SMS_ERR_INVALID_ARG, "sms_backward: rows*cols too large");
     if (!std::isfinite(scale)) return fail(SMS_ERR_INVALID_ARG, "sms_backward: scale must be finite");
@@ -272,6 +282,7 @@ int sms_backward(const void *y, const void *dy, void *dx, int64_t rows, int64_t 
     a.y = y; a.dy = dy; a.dx = dx;
     a.rows = rows; a.cols = cols; a.total = total;
     a.scale = scale; a.causal = is_causal_hint ? 1 : 0; a.err = err;
+    a.dcols = FastDiv((uint32_t)cols);
 
     const int path = pick_path(g_forced.load(), cols, dtype, aligned, true);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -281,8 +292,8 @@ int sms_backward(const void *y, const void *dy, void *dx, int64_t rows, int64_t 
         e = launch_bwd_warp(a, dtype, aligned, st);
         break;
     case SMS_PATH_CTA:
-        if (!cta_fits_bwd(cols, dtype)) return fail(SMS_ERR_UNSUPPORTED, "sms_backward: row too wide for the CTA path");
-        e = launch_bwd_cta(a, dtype, st);
+        if (!cta_fits_bwd(cols, dtype, aligned)) return fail(SMS_ERR_UNSUPPORTED, "sms_backward: row too wide for the CTA path");
+        e = launch_bwd_cta(a, dtype, aligned, st);
         break;
     default:
         e = launch_bwd_online(a, dtype, st);

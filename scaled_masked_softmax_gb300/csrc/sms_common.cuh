@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "sms_fastdiv.h"
+
 namespace sms {
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -210,6 +212,36 @@ __device__ __forceinline__ uint64_t policy_evict_normal()
 __device__ __forceinline__ void named_sync(int id, int threads)
 {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
+}
+
+// ------------------------------------------------------------ row index ---
+// Row r of the [rows, cols] view is query position q of head h of batch b:
+// r = (b * heads + h) * cols + q.
+__device__ __forceinline__ void split_row(int64_t r, int64_t cols, int64_t heads, const FastDiv &dc,
+                                          const FastDiv &dh, int64_t &q, int64_t &h, int64_t &b)
+{
+    if (r <= 0xffffffffll) {
+        const uint32_t rr = (uint32_t)r;
+        const uint32_t rc = dc.div(rr);
+        q = rr - rc * (uint32_t)cols;
+        const uint32_t bb = dh.div(rc);
+        h = rc - bb * (uint32_t)heads;
+        b = bb;
+    } else {
+        const int64_t rc = r / cols;
+        q = r - rc * cols;
+        b = rc / heads;
+        h = rc - b * heads;
+    }
+}
+
+__device__ __forceinline__ int64_t row_q(int64_t r, int64_t cols, const FastDiv &dc)
+{
+    if (r <= 0xffffffffll) {
+        const uint32_t rr = (uint32_t)r;
+        return rr - dc.div(rr) * (uint32_t)cols;
+    }
+    return r % cols;
 }
 
 // Records the first failure code in the library's device error word (its

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "sms_fastdiv.h"
+
 namespace sms {
 
 // dtype codes, equal to sms_dtype in include/sms.h
@@ -23,6 +25,7 @@ struct FwdArgs {
     float scale;
     int causal;
     int *err;              // device error word
+    FastDiv dcols, dheads; // division by cols and by heads
 };
 
 struct BwdArgs {
@@ -34,6 +37,7 @@ struct BwdArgs {
     float scale;
     int causal;            // the causal hint: y == 0 beyond the diagonal
     int *err;
+    FastDiv dcols;         // division by cols
 };
 
 // "aligned" means every row (and every mask row) starts on a 16-byte boundary:
@@ -45,10 +49,10 @@ cudaError_t launch_fwd_warp(const FwdArgs &a, int dtype, bool aligned, cudaStrea
 cudaError_t launch_bwd_warp(const BwdArgs &a, int dtype, bool aligned, cudaStream_t st);
 
 // persistent CTA per row, bulk-copy (TMA) staging ring, rows in registers
-bool cta_fits(int64_t cols, int dtype);      // forward
-bool cta_fits_bwd(int64_t cols, int dtype);  // backward (y and dy both held)
-cudaError_t launch_fwd_cta(const FwdArgs &a, int dtype, cudaStream_t st);
-cudaError_t launch_bwd_cta(const BwdArgs &a, int dtype, cudaStream_t st);
+bool cta_fits(int64_t cols, int dtype, bool aligned);      // forward
+bool cta_fits_bwd(int64_t cols, int dtype, bool aligned);  // backward (y and dy both held)
+cudaError_t launch_fwd_cta(const FwdArgs &a, int dtype, bool aligned, cudaStream_t st);
+cudaError_t launch_bwd_cta(const BwdArgs &a, int dtype, bool aligned, cudaStream_t st);
 
 // streaming two pass, any row length
 cudaError_t launch_fwd_online(const FwdArgs &a, int dtype, cudaStream_t st);

@@ -31,12 +31,11 @@ struct OnlineRow {
 };
 
 template <int VEC>
-__device__ __forceinline__ OnlineRow online_geom(int64_t r, int64_t cols, int causal)
+__device__ __forceinline__ OnlineRow online_geom(int64_t r, int64_t cols, int causal, int64_t q)
 {
     OnlineRow g;
     g.x0 = r * cols;
     g.xoff = (int)(g.x0 & (VEC - 1));
-    const int64_t q = r % cols;
     g.limit = causal ? (int)(q + 1) : (int)cols;
     g.nv_read = (g.xoff + g.limit + VEC - 1) / VEC;
     g.nv_row = (int)((g.xoff + cols + VEC - 1) / VEC);
@@ -97,14 +96,15 @@ __global__ void __launch_bounds__(kNT) fwd_online_kernel(const FwdArgs a)
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     int rp = 0;
     for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x, rp ^= 1) {
-        const OnlineRow g = online_geom<VEC>(r, a.cols, a.causal);
+        int64_t q, hh, bb;
+        split_row(r, a.cols, a.heads, a.dcols, a.dheads, q, hh, bb);
+        const OnlineRow g = online_geom<VEC>(r, a.cols, a.causal, q);
         const T *xs = reinterpret_cast<const T *>(a.x) + (g.x0 - g.xoff);
         const T *ms = nullptr;
         int64_t m0 = 0;
         bool mvec = false;
         if (a.mask) {
-            const int64_t hh = (r / a.cols) % a.heads, bb = r / (a.cols * a.heads);
-            m0 = bb * a.msb + hh * a.msh + (r % a.cols) * a.cols;
+            m0 = bb * a.msb + hh * a.msh + q * a.cols;
             ms = reinterpret_cast<const T *>(a.mask) + m0;
             mvec = ((m0 - g.xoff) & (VEC - 1)) == 0;
         }
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(kNT) bwd_online_kernel(const BwdArgs a)
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     int rp = 0;
     for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x, rp ^= 1) {
-        const OnlineRow g = online_geom<VEC>(r, a.cols, a.causal);
+        const OnlineRow g = online_geom<VEC>(r, a.cols, a.causal, row_q(r, a.cols, a.dcols));
         const T *ys = reinterpret_cast<const T *>(a.y) + (g.x0 - g.xoff);
         const T *gs = reinterpret_cast<const T *>(a.dy) + (g.x0 - g.xoff);
         float dot = 0.f;

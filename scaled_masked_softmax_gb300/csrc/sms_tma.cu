@@ -10,9 +10,12 @@
 //     cp.async.bulk (the TMA unit), running ahead of the consumers by up to
 //     the whole ring, so HBM reads for the next rows overlap the reductions
 //     and stores of the current one;
+//   * the producer also writes a 64-byte descriptor into every stage (row
+//     start, alignment, causal limit, mask span, ...): consumer threads do no
+//     index arithmetic of their own;
 //   * NT consumer threads pull each stage into registers (the row stays in
 //     registers, not shared memory) and release the stage at once;
-//   * reductions are warp shuffles plus one 16-entry shared exchange;
+//   * reductions are warp shuffles plus one shared exchange across warps;
 //   * exp is evaluated once per element, and causal positions j > q are never
 //     copied.
 // Rows of any start alignment are handled: stages hold 16-byte vectors
@@ -31,72 +34,53 @@
 namespace sms {
 namespace {
 
-constexpr int kNT = 512;                    // consumer threads (16 warps)
-constexpr int kNW = kNT / 32;
-constexpr int kThreads = kNT + 32;          // + one producer warp
-constexpr int kSV = kNT;                    // 16-byte vectors of x (or y) per stage
-constexpr int kStageBytes = 16 * (2 * kSV + 1);  // x/y area + mask/dy area (+1 vector of slack)
-constexpr int kMaxStages = 16;
-constexpr int kSmemTarget = 200 * 1024;
+constexpr int kMaxStages = 32;
 
-struct Hdr {
+// Written by the producer at the head of every stage.
+struct __align__(16) ChunkDesc {
+    int64_t x0;      // flat element index of the row start
+    int64_t m0;      // mask row start (elements)
+    int64_t mv_lo;   // first mask vector (tensor index) held by the stage
+    int64_t cm_hi;   // one past the last mask vector held by the stage
+    int32_t cx_hi;   // one past the last row vector (row-relative) held by the stage
+    int32_t xoff;    // x0 mod VEC
+    int32_t limit;   // elements read: q+1 under causal, else cols
+    int32_t nv_read; // vectors holding elements < limit
+    int32_t nv_row;  // vectors holding row elements
+    int32_t nchunks; // stages the row occupies
+    int32_t pad0, pad1;
+};
+static_assert(sizeof(ChunkDesc) == 64, "descriptor is one 64-byte slot");
+
+template <int NT> struct Geo {
+    static constexpr int NW = NT / 32;
+    static constexpr int THREADS = NT + 32;                 // + one producer warp
+    static constexpr int SV = NT;                           // 16-byte vectors of x (or y) per stage
+    static constexpr int A_OFF = 64;                        // after the descriptor
+    static constexpr int B_OFF = 64 + 16 * SV;              // mask (or dy) area, SV + 1 vectors
+    static constexpr int STAGE = 64 + 16 * (2 * SV + 1);
+};
+
+template <int NT> struct Hdr {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
-    float red_max[kNW];
-    float red_sum[2][kNW];  // double buffered by row parity (one barrier per row in backward)
-    int abort;       // any thread gave up (producer or consumer)
-    int cons_abort;  // a consumer gave up (read only after a consumer barrier)
+    float red_max[Geo<NT>::NW];
+    float red_sum[2][Geo<NT>::NW];  // double buffered by row parity (one barrier per row in backward)
+    int abort;                      // any thread gave up (producer or consumer)
+    int cons_abort;                 // a consumer gave up (read only after a consumer barrier)
 };
-constexpr int kHdrBytes = (int)((sizeof(Hdr) + 127) / 128 * 128);
+template <int NT> __host__ __device__ constexpr int hdr_bytes() { return (int)((sizeof(Hdr<NT>) + 127) / 128 * 128); }
 
-// Geometry of one row, computed identically by producer and consumers.
-struct Row {
-    int64_t x0;     // flat element index of the row start
-    int64_t gbase;  // tensor vector index of the aligned row start
-    int xoff;       // x0 mod VEC
-    int limit;      // elements read (q+1 under causal, else cols)
-    int nv_read;    // vectors holding elements < limit
-    int nv_row;     // vectors holding row elements
-    int nchunks;    // stages used by the row
-    int64_t m0;     // mask row start (forward)
-};
-
-template <int VEC>
-__device__ __forceinline__ Row row_geom(int64_t r, int64_t cols, int causal)
+template <typename T, int NT, int SLOTS, bool BWD>
+__global__ void __launch_bounds__(Geo<NT>::THREADS, 1)
+    cta_kernel(const FwdArgs fa, const BwdArgs ba, int nstage)
 {
-    Row g;
-    g.x0 = r * cols;
-    g.xoff = (int)(g.x0 & (VEC - 1));
-    g.gbase = (g.x0 - g.xoff) / VEC;
-    const int64_t q = r % cols;
-    g.limit = causal ? (int)(q + 1) : (int)cols;
-    g.nv_read = (g.xoff + g.limit + VEC - 1) / VEC;
-    g.nv_row = (int)((g.xoff + cols + VEC - 1) / VEC);
-    g.nchunks = (g.nv_read + kSV - 1) / kSV;
-    g.m0 = 0;
-    return g;
-}
-
-// Mask vectors of chunk c: [mv_lo, cm_hi) are in the stage (tensor vector indices).
-template <int VEC>
-__device__ __forceinline__ void mask_span(const Row &g, int c, int64_t mask_total, int64_t &mv_lo, int64_t &cm_hi)
-{
-    const int vlo = c * kSV;
-    const int vhi = min(g.nv_read, vlo + kSV);
-    const int64_t jlo = max(0, vlo * VEC - g.xoff);
-    const int64_t jhi = min((int64_t)g.limit, (int64_t)vhi * VEC - g.xoff);
-    mv_lo = (g.m0 + jlo) / VEC;
-    const int64_t mv_hi = (g.m0 + jhi + VEC - 1) / VEC;
-    cm_hi = min(mv_hi, mask_total / VEC);
-}
-
-template <typename T, int SLOTS, bool BWD>
-__global__ void __launch_bounds__(kThreads, 1) cta_kernel(const FwdArgs fa, const BwdArgs ba, int nstage)
-{
+    using G = Geo<NT>;
     constexpr int VEC = Dt<T>::VEC;
+    constexpr int SV = G::SV;
     extern __shared__ __align__(128) unsigned char smem[];
-    Hdr &h = *reinterpret_cast<Hdr *>(smem);
-    unsigned char *stages = smem + kHdrBytes;
+    Hdr<NT> &h = *reinterpret_cast<Hdr<NT> *>(smem);
+    unsigned char *stages = smem + hdr_bytes<NT>();
 
     const int64_t rows = BWD ? ba.rows : fa.rows;
     const int64_t cols = BWD ? ba.cols : fa.cols;
@@ -110,7 +94,7 @@ __global__ void __launch_bounds__(kThreads, 1) cta_kernel(const FwdArgs fa, cons
     if (threadIdx.x == 0) {
         for (int s = 0; s < nstage; ++s) {
             mbar_init(&h.full[s], 1);
-            mbar_init(&h.empty[s], kNW);
+            mbar_init(&h.empty[s], G::NW);
         }
         h.abort = 0;
         h.cons_abort = 0;
@@ -120,9 +104,9 @@ __global__ void __launch_bounds__(kThreads, 1) cta_kernel(const FwdArgs fa, cons
 
     volatile int *abort_flag = &h.abort;
 
-    if (threadIdx.x >= kNT) {
+    if (threadIdx.x >= NT) {
         // ------------------------------------------------------- producer ---
-        if (threadIdx.x != kNT) return;
+        if (threadIdx.x != NT) return;
         const uint64_t polA = policy_evict_first();
         const uint64_t polB = BWD ? polA : policy_evict_normal();
         uint32_t issued = 0, parity = 0;  // per stage: ever issued / parity of its last issue
@@ -130,39 +114,57 @@ __global__ void __launch_bounds__(kThreads, 1) cta_kernel(const FwdArgs fa, cons
         uint32_t ph = 0;
         bool ok = true;
         for (int64_t r = blockIdx.x; r < rows && ok; r += gridDim.x) {
-            Row g = row_geom<VEC>(r, cols, causal);
-            if (!BWD && srcB) {
-                const int64_t hh = (r / cols) % fa.heads, bb = r / (cols * fa.heads);
-                g.m0 = bb * fa.msb + hh * fa.msh + (r % cols) * cols;
+            int64_t q = 0, hh = 0, bb = 0;
+            if (BWD) {
+                if (causal) q = row_q(r, cols, ba.dcols);
+            } else if (causal || srcB) {
+                split_row(r, cols, fa.heads, fa.dcols, fa.dheads, q, hh, bb);
             }
-            for (int c = 0; c < g.nchunks; ++c) {
+            ChunkDesc d;
+            d.x0 = r * cols;
+            d.xoff = (int)(d.x0 & (VEC - 1));
+            const int64_t gbase = (d.x0 - d.xoff) / VEC;
+            d.limit = causal ? (int)(q + 1) : (int)cols;
+            d.nv_read = (d.xoff + d.limit + VEC - 1) / VEC;
+            d.nv_row = (int)((d.xoff + cols + VEC - 1) / VEC);
+            d.nchunks = (d.nv_read + SV - 1) / SV;
+            d.m0 = (!BWD && srcB) ? bb * fa.msb + hh * fa.msh + q * cols : 0;
+            d.pad0 = d.pad1 = 0;
+            for (int c = 0; c < d.nchunks; ++c) {
                 if (!mbar_wait_bounded(&h.empty[stage], ph ^ 1u, abort_flag)) {
                     *abort_flag = 1;
                     report_error(err, 2);
                     ok = false;
                     break;
                 }
-                const int vlo = c * kSV;
-                const int vhi = min(g.nv_read, vlo + kSV);
-                const int64_t cx_hi = min((int64_t)vhi, full_vecs - g.gbase);
-                const uint32_t bytesA = cx_hi > vlo ? (uint32_t)(cx_hi - vlo) * 16u : 0u;
+                const int vlo = c * SV;
+                const int vhi = min(d.nv_read, vlo + SV);
+                d.cx_hi = (int)min((int64_t)vhi, full_vecs - gbase);
+                const uint32_t bytesA = d.cx_hi > vlo ? (uint32_t)(d.cx_hi - vlo) * 16u : 0u;
                 uint32_t bytesB = 0;
                 int64_t b_src = 0;
+                d.mv_lo = 0;
+                d.cm_hi = 0;
                 if (BWD) {
                     bytesB = bytesA;
-                    b_src = g.gbase + vlo;
+                    b_src = gbase + vlo;
                 } else if (srcB) {
-                    int64_t mv_lo, cm_hi;
-                    mask_span<VEC>(g, c, fa.mask_total, mv_lo, cm_hi);
-                    bytesB = cm_hi > mv_lo ? (uint32_t)(cm_hi - mv_lo) * 16u : 0u;
-                    b_src = mv_lo;
+                    const int64_t jlo = max(0, vlo * VEC - d.xoff);
+                    const int64_t jhi = min((int64_t)d.limit, (int64_t)vhi * VEC - d.xoff);
+                    d.mv_lo = (d.m0 + jlo) / VEC;
+                    d.cm_hi = min((d.m0 + jhi + VEC - 1) / VEC, fa.mask_total / VEC);
+                    bytesB = d.cm_hi > d.mv_lo ? (uint32_t)(d.cm_hi - d.mv_lo) * 16u : 0u;
+                    b_src = d.mv_lo;
                 }
-                unsigned char *st = stages + (size_t)stage * kStageBytes;
+                unsigned char *st = stages + (size_t)stage * G::STAGE;
+                *reinterpret_cast<ChunkDesc *>(st) = d;  // visible to consumers through the barrier
                 mbar_arrive_expect_tx(&h.full[stage], bytesA + bytesB);
                 if (bytesA)
-                    bulk_g2s(st, reinterpret_cast<const uint4 *>(srcA) + g.gbase + vlo, bytesA, &h.full[stage], polA);
+                    bulk_g2s(st + G::A_OFF, reinterpret_cast<const uint4 *>(srcA) + gbase + vlo, bytesA,
+                             &h.full[stage], polA);
                 if (bytesB)
-                    bulk_g2s(st + 16 * kSV, reinterpret_cast<const uint4 *>(srcB) + b_src, bytesB, &h.full[stage], polB);
+                    bulk_g2s(st + G::B_OFF, reinterpret_cast<const uint4 *>(srcB) + b_src, bytesB, &h.full[stage],
+                             polB);
                 issued |= 1u << stage;
                 parity = (parity & ~(1u << stage)) | (ph << stage);
                 if (++stage == nstage) { stage = 0; ph ^= 1u; }
@@ -187,25 +189,16 @@ __global__ void __launch_bounds__(kThreads, 1) cta_kernel(const FwdArgs fa, cons
     int stage = 0;
     uint32_t ph = 0;
     int rp = 0;  // row parity: selects the reduction buffer
+    const int64_t my_rows = rows > blockIdx.x ? (rows - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
 
-    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x, rp ^= 1) {
-        Row g = row_geom<VEC>(r, cols, causal);
-        const T *mrow = nullptr;
-        bool mvec = false;
-        if (!BWD && srcB) {
-            const int64_t hh = (r / cols) % fa.heads, bb = r / (cols * fa.heads);
-            g.m0 = bb * fa.msb + hh * fa.msh + (r % cols) * cols;
-            mrow = reinterpret_cast<const T *>(srcB) + g.m0;
-            mvec = ((g.m0 - g.xoff) & (VEC - 1)) == 0;
-        }
-        const T *arow = reinterpret_cast<const T *>(srcA) + (g.x0 - g.xoff);  // aligned
-        const T *brow = BWD ? reinterpret_cast<const T *>(srcB) + (g.x0 - g.xoff) : nullptr;
-
+    for (int64_t it = 0; it < my_rows; ++it, rp ^= 1) {
         // forward: scores s as fp32; backward: y and dy kept as the raw 16-byte
         // vectors (half the registers for fp16/bf16), widened again for dx
         float va[BWD ? 1 : SLOTS][VEC];
         uint4 ra[BWD ? SLOTS : 1], rb[BWD ? SLOTS : 1];
         float acc = BWD ? 0.f : neg_inf();  // backward: dot; forward: running max
+        int64_t x0 = 0;
+        int xoff = 0, limit = 0, nv_row = 0, nchunks = 1;
 
 #pragma unroll
         for (int k = 0; k < SLOTS; ++k) {
@@ -216,23 +209,37 @@ __global__ void __launch_bounds__(kThreads, 1) cta_kernel(const FwdArgs fa, cons
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) va[k][e] = neg_inf();
             }
-            if (k < g.nchunks) {
-                if (!mbar_wait_bounded(&h.full[stage], ph, abort_flag)) {
+            if (k < nchunks) {
+                // warp-uniform outcome: a warp whose wait failed skips the stage
+                // (its descriptor may be stale) and the CTA leaves at the barrier
+                const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&h.full[stage], ph, abort_flag));
+                if (!ok && lane == 0) {
                     *abort_flag = 1;
                     h.cons_abort = 1;
                     report_error(err, 1);
                 }
-                const unsigned char *st = stages + (size_t)stage * kStageBytes;
-                const int vi = k * kSV + t;
-                const int j0 = vi * VEC - g.xoff;
-                if (vi < g.nv_read) {
-                    const int64_t gv = g.gbase + vi;
+                const unsigned char *st = stages + (size_t)stage * G::STAGE;
+                const ChunkDesc &d = *reinterpret_cast<const ChunkDesc *>(st);
+                if (k == 0 && ok) {
+                    x0 = d.x0;
+                    xoff = d.xoff;
+                    limit = d.limit;
+                    nv_row = d.nv_row;
+                    nchunks = min(max(d.nchunks, 1), SLOTS);
+                }
+                const int vi = k * SV + t;
+                const int j0 = vi * VEC - xoff;
+                if (ok && vi < d.nv_read) {
+                    const T *arow = reinterpret_cast<const T *>(srcA) + (x0 - xoff);
+                    const int64_t gv = (x0 - xoff) / VEC + vi;
                     float a[VEC], b[VEC];
+                    const bool staged = vi < d.cx_hi;  // else: last partial vector of the tensor
                     if (BWD) {
-                        if (gv < full_vecs) {
-                            ra[k] = reinterpret_cast<const uint4 *>(st)[t];
-                            rb[k] = reinterpret_cast<const uint4 *>(st + 16 * kSV)[t];
-                        } else {  // last partial vector of the tensor: not in the stage
+                        const T *brow = reinterpret_cast<const T *>(srcB) + (x0 - xoff);
+                        if (staged) {
+                            ra[k] = reinterpret_cast<const uint4 *>(st + G::A_OFF)[t];
+                            rb[k] = reinterpret_cast<const uint4 *>(st + G::B_OFF)[t];
+                        } else {
 #pragma unroll
                             for (int e = 0; e < VEC; ++e) {
                                 const bool in = gv * VEC + e < total;
@@ -247,31 +254,32 @@ __global__ void __launch_bounds__(kThreads, 1) cta_kernel(const FwdArgs fa, cons
 #pragma unroll
                         for (int e = 0; e < VEC; ++e) {
                             const int j = j0 + e;
-                            if (j >= 0 && j < g.limit) acc = fmaf(a[e], b[e], acc);
+                            if (j >= 0 && j < limit) acc = fmaf(a[e], b[e], acc);
                         }
                     } else {
-                        if (gv < full_vecs) {
-                            unpack<T>(reinterpret_cast<const uint4 *>(st)[t], a);
-                        } else {  // last partial vector of the tensor: not in the stage
+                        if (staged) {
+                            unpack<T>(reinterpret_cast<const uint4 *>(st + G::A_OFF)[t], a);
+                        } else {
 #pragma unroll
                             for (int e = 0; e < VEC; ++e)
                                 a[e] = gv * VEC + e < total ? to_f32<T>(arow[vi * VEC + e]) : 0.f;
                         }
 #pragma unroll
                         for (int e = 0; e < VEC; ++e) b[e] = 0.f;
-                        if (mrow) {
-                            int64_t mv_lo, cm_hi;
-                            mask_span<VEC>(g, k, fa.mask_total, mv_lo, cm_hi);
-                            const T *msm = reinterpret_cast<const T *>(st + 16 * kSV);
-                            const int64_t mvi = (g.m0 - g.xoff) / VEC + vi;  // valid when mvec
+                        if (srcB) {
+                            const int64_t m0 = d.m0, mv_lo = d.mv_lo, cm_hi = d.cm_hi;
+                            const T *msm = reinterpret_cast<const T *>(st + G::B_OFF);
+                            const int64_t mvi = (m0 - xoff) / VEC + vi;
+                            const bool mvec = ((m0 - xoff) & (VEC - 1)) == 0;
                             if (mvec && mvi >= mv_lo && mvi < cm_hi) {
                                 unpack<T>(reinterpret_cast<const uint4 *>(msm)[mvi - mv_lo], b);
                             } else {
+                                const T *mrow = reinterpret_cast<const T *>(srcB) + m0;
 #pragma unroll
                                 for (int e = 0; e < VEC; ++e) {
                                     const int j = j0 + e;
-                                    if (j >= 0 && j < g.limit) {
-                                        const int64_t f = g.m0 + j;
+                                    if (j >= 0 && j < limit) {
+                                        const int64_t f = m0 + j;
                                         b[e] = f < cm_hi * VEC ? to_f32<T>(msm[f - mv_lo * VEC]) : to_f32<T>(mrow[j]);
                                     }
                                 }
@@ -280,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) cta_kernel(const FwdArgs fa, cons
 #pragma unroll
                         for (int e = 0; e < VEC; ++e) {
                             const int j = j0 + e;
-                            va[k][e] = (j >= 0 && j < g.limit) ? fmaf(a[e], fa.scale, b[e]) : neg_inf();
+                            va[k][e] = (j >= 0 && j < limit) ? fmaf(a[e], fa.scale, b[e]) : neg_inf();
                             acc = fmaxf(acc, va[k][e]);
                         }
                     }
@@ -294,24 +302,24 @@ __global__ void __launch_bounds__(kThreads, 1) cta_kernel(const FwdArgs fa, cons
         if (BWD) {
             acc = group_sum<32>(acc);
             if (lane == 0) h.red_sum[rp][warp] = acc;
-            named_sync(1, kNT);
+            named_sync(1, NT);
             if (h.cons_abort) break;  // uniform: every consumer reads the same value here
             float dot = 0.f;
 #pragma unroll
-            for (int w = 0; w < kNW; ++w) dot += h.red_sum[rp][w];
-            T *orow = reinterpret_cast<T *>(ba.dx) + (g.x0 - g.xoff);
+            for (int w = 0; w < G::NW; ++w) dot += h.red_sum[rp][w];
+            T *orow = reinterpret_cast<T *>(ba.dx) + (x0 - xoff);
 #pragma unroll
             for (int k = 0; k < SLOTS; ++k) {
-                const int vi = k * kSV + t;
-                const int j0 = vi * VEC - g.xoff;
-                if (vi >= g.nv_row) continue;
+                const int vi = k * SV + t;
+                const int j0 = vi * VEC - xoff;
+                if (vi >= nv_row) continue;
                 float yv[VEC], gv[VEC], o[VEC];
                 unpack<T>(ra[k], yv);
                 unpack<T>(rb[k], gv);
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) {
                     const int j = j0 + e;
-                    const bool valid = j >= 0 && j < g.limit;  // y == 0 (masked) gives exactly +0
+                    const bool valid = j >= 0 && j < limit;  // y == 0 (masked) gives exactly +0
                     o[e] = (!valid || yv[e] == 0.f) ? 0.f : (gv[e] - dot) * yv[e] * ba.scale;
                 }
                 if (j0 >= 0 && j0 + VEC <= cols) {
@@ -327,11 +335,11 @@ __global__ void __launch_bounds__(kThreads, 1) cta_kernel(const FwdArgs fa, cons
         } else {
             acc = group_max<32>(acc);
             if (lane == 0) h.red_max[warp] = acc;
-            named_sync(1, kNT);
+            named_sync(1, NT);
             if (h.cons_abort) break;  // uniform: every consumer reads the same value here
             float mx = neg_inf();
 #pragma unroll
-            for (int w = 0; w < kNW; ++w) mx = fmaxf(mx, h.red_max[w]);
+            for (int w = 0; w < G::NW; ++w) mx = fmaxf(mx, h.red_max[w]);
             const float mref = (mx == neg_inf()) ? 0.f : mx;
             float sum = 0.f;
 #pragma unroll
@@ -344,17 +352,17 @@ __global__ void __launch_bounds__(kThreads, 1) cta_kernel(const FwdArgs fa, cons
                 }
             sum = group_sum<32>(sum);
             if (lane == 0) h.red_sum[rp][warp] = sum;
-            named_sync(1, kNT);
+            named_sync(1, NT);
             float tot = 0.f;
 #pragma unroll
-            for (int w = 0; w < kNW; ++w) tot += h.red_sum[rp][w];
+            for (int w = 0; w < G::NW; ++w) tot += h.red_sum[rp][w];
             const float inv = tot > 0.f ? __frcp_rn(tot) : 0.f;
-            T *orow = reinterpret_cast<T *>(fa.y) + (g.x0 - g.xoff);
+            T *orow = reinterpret_cast<T *>(fa.y) + (x0 - xoff);
 #pragma unroll
             for (int k = 0; k < SLOTS; ++k) {
-                const int vi = k * kSV + t;
-                const int j0 = vi * VEC - g.xoff;
-                if (vi >= g.nv_row) continue;
+                const int vi = k * SV + t;
+                const int j0 = vi * VEC - xoff;
+                if (vi >= nv_row) continue;
                 float o[VEC];
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) o[e] = va[k][e] * inv;
@@ -372,84 +380,113 @@ __global__ void __launch_bounds__(kThreads, 1) cta_kernel(const FwdArgs fa, cons
     }
 }
 
-int stages_for_budget() { return (kSmemTarget - kHdrBytes) / kStageBytes; }
+// Shared memory per CTA: 1 CTA/SM for NT=512 (~200 KB), 2 CTAs/SM for NT=256.
+template <int NT> constexpr int smem_target() { return NT >= 512 ? 200 * 1024 : 100 * 1024; }
+template <int NT> constexpr int n_stages()
+{
+    return (smem_target<NT>() - hdr_bytes<NT>()) / Geo<NT>::STAGE < kMaxStages
+               ? (smem_target<NT>() - hdr_bytes<NT>()) / Geo<NT>::STAGE
+               : kMaxStages;
+}
 
-template <typename T, int SLOTS, bool BWD>
+template <typename T, int NT, int SLOTS, bool BWD>
 cudaError_t launch_one(const FwdArgs &fa, const BwdArgs &ba, cudaStream_t st)
 {
-    const int nstage = stages_for_budget() < kMaxStages ? stages_for_budget() : kMaxStages;
-    const int smem = kHdrBytes + nstage * kStageBytes;
-    auto kern = cta_kernel<T, SLOTS, BWD>;
+    constexpr int nstage = n_stages<NT>();
+    constexpr int smem = hdr_bytes<NT>() + nstage * Geo<NT>::STAGE;
+    auto kern = cta_kernel<T, NT, SLOTS, BWD>;
     static std::once_flag once[64];
+    static cudaError_t attr_status[64];
+    static int per_sm[64];
     int dev = 0;
-    cudaGetDevice(&dev);
-    cudaError_t attr = cudaSuccess;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
     std::call_once(once[dev & 63], [&] {
-        attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t s = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        int n = 1;
+        if (s == cudaSuccess) s = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Geo<NT>::THREADS, smem);
+        attr_status[dev & 63] = s;
+        per_sm[dev & 63] = n > 0 ? n : 1;
     });
-    if (attr != cudaSuccess) return attr;
+    if (attr_status[dev & 63] != cudaSuccess) return attr_status[dev & 63];
     const int64_t rows = BWD ? ba.rows : fa.rows;
-    int64_t grid = (int64_t)sm_count();
+    int64_t grid = (int64_t)sm_count() * per_sm[dev & 63];
     if (grid > rows) grid = rows;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(Geo<NT>::THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     return cudaLaunchKernelEx(&cfg, kern, fa, ba, nstage);
 }
 
-// Register slots (16-byte vectors per consumer thread) needed for a row.
-inline int64_t slots_needed(int64_t cols, int dtype)
+// 16-byte vectors a row spans (one more when rows may start mid-vector).
+inline int64_t row_vectors(int64_t cols, int dtype, bool aligned)
 {
     const int vec = vec_elems(dtype);
-    const int64_t vecs = (cols + vec - 1) / vec + 1;  // +1: a row may start mid-vector
-    return (vecs + kNT - 1) / kNT;
+    return (cols + vec - 1) / vec + (aligned ? 0 : 1);
 }
 
-template <typename T, bool BWD>
-cudaError_t launch_t(const FwdArgs &fa, const BwdArgs &ba, int64_t cols, int dtype, cudaStream_t st)
+// Consumer threads: 256 while a row spans at most 4 vectors per thread of a
+// 256-thread CTA, else 512.  Register slots = vectors per consumer thread.
+inline int pick_nt(int64_t vecs) { return vecs <= 4 * 256 ? 256 : 512; }
+
+template <typename T, bool BWD, int NT>
+cudaError_t launch_nt(const FwdArgs &fa, const BwdArgs &ba, int64_t vecs, cudaStream_t st)
 {
-    const int64_t s = slots_needed(cols, dtype);
-    if (s <= 1) return launch_one<T, 1, BWD>(fa, ba, st);
-    if (s <= 2) return launch_one<T, 2, BWD>(fa, ba, st);
-    if (s <= 4) return launch_one<T, 4, BWD>(fa, ba, st);
-    if (s <= 8) return launch_one<T, 8, BWD>(fa, ba, st);
-    if constexpr (!BWD && Dt<T>::VEC == 4) {
-        if (s <= 16) return launch_one<T, 16, BWD>(fa, ba, st);
+    const int64_t s = (vecs + NT - 1) / NT;
+    if (s <= 1) return launch_one<T, NT, 1, BWD>(fa, ba, st);
+    if (s <= 2) return launch_one<T, NT, 2, BWD>(fa, ba, st);
+    if (s <= 4) return launch_one<T, NT, 4, BWD>(fa, ba, st);
+    if constexpr (NT == 512) {
+        if (s <= 8) return launch_one<T, NT, 8, BWD>(fa, ba, st);
+        if constexpr (!BWD && Dt<T>::VEC == 4) {
+            if (s <= 16) return launch_one<T, NT, 16, BWD>(fa, ba, st);
+        }
     }
     return cudaErrorNotSupported;
 }
 
+template <typename T, bool BWD>
+cudaError_t launch_t(const FwdArgs &fa, const BwdArgs &ba, int64_t cols, int dtype, bool aligned, cudaStream_t st)
+{
+    const int64_t vecs = row_vectors(cols, dtype, aligned);
+    if (pick_nt(vecs) == 256) return launch_nt<T, BWD, 256>(fa, ba, vecs, st);
+    return launch_nt<T, BWD, 512>(fa, ba, vecs, st);
+}
+
 template <bool BWD>
-cudaError_t dispatch(const FwdArgs &fa, const BwdArgs &ba, int64_t cols, int dtype, cudaStream_t st)
+cudaError_t dispatch(const FwdArgs &fa, const BwdArgs &ba, int64_t cols, int dtype, bool aligned, cudaStream_t st)
 {
     switch (dtype) {
-    case kF32: return launch_t<float, BWD>(fa, ba, cols, dtype, st);
-    case kF16: return launch_t<__half, BWD>(fa, ba, cols, dtype, st);
-    case kBF16: return launch_t<__nv_bfloat16, BWD>(fa, ba, cols, dtype, st);
+    case kF32: return launch_t<float, BWD>(fa, ba, cols, dtype, aligned, st);
+    case kF16: return launch_t<__half, BWD>(fa, ba, cols, dtype, aligned, st);
+    case kBF16: return launch_t<__nv_bfloat16, BWD>(fa, ba, cols, dtype, aligned, st);
     default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-// Forward keeps fp32 scores: 16 slots (64 values) for fp32 rows, 8 for 16-bit
-// rows (64 values); backward keeps raw vectors: 8 slots.
-bool cta_fits(int64_t cols, int dtype) { return slots_needed(cols, dtype) <= (vec_elems(dtype) == 4 ? 16 : 8); }
-
-bool cta_fits_bwd(int64_t cols, int dtype) { return slots_needed(cols, dtype) <= 8; }
-
-cudaError_t launch_fwd_cta(const FwdArgs &a, int dtype, cudaStream_t st)
+// Forward keeps fp32 scores: up to 16 slots (64 values) for fp32 rows, 8 for
+// 16-bit rows (64 values); backward keeps raw vectors: 8 slots.
+bool cta_fits(int64_t cols, int dtype, bool aligned)
 {
-    BwdArgs none = {};
-    return dispatch<false>(a, none, a.cols, dtype, st);
+    return row_vectors(cols, dtype, aligned) <= 512 * (vec_elems(dtype) == 4 ? 16 : 8);
 }
 
-cudaError_t launch_bwd_cta(const BwdArgs &a, int dtype, cudaStream_t st)
+bool cta_fits_bwd(int64_t cols, int dtype, bool aligned) { return row_vectors(cols, dtype, aligned) <= 512 * 8; }
+
+cudaError_t launch_fwd_cta(const FwdArgs &a, int dtype, bool aligned, cudaStream_t st)
+{
+    BwdArgs none = {};
+    return dispatch<false>(a, none, a.cols, dtype, aligned, st);
+}
+
+cudaError_t launch_bwd_cta(const BwdArgs &a, int dtype, bool aligned, cudaStream_t st)
 {
     FwdArgs none = {};
-    return dispatch<true>(none, a, a.cols, dtype, st);
+    return dispatch<true>(none, a, a.cols, dtype, aligned, st);
 }
 
 }  // namespace sms

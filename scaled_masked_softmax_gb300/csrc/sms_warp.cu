@@ -32,7 +32,8 @@ __global__ void __launch_bounds__(kThreads) fwd_warp_kernel(const FwdArgs a)
     const bool live = row < a.rows;
     const int64_t r = live ? row : a.rows - 1;  // dead lanes still join the shuffles
     const int64_t cols = a.cols;
-    const int64_t q = r % cols;
+    int64_t q = 0, h = 0, b = 0;
+    if (a.causal || a.mask) split_row(r, cols, a.heads, a.dcols, a.dheads, q, h, b);
     const int limit = a.causal ? (int)(q + 1) : (int)cols;  // elements that are read
     const int64_t x0 = r * cols;
     const int xoff = ALIGNED ? 0 : (int)(x0 & (VEC - 1));
@@ -42,8 +43,6 @@ __global__ void __launch_bounds__(kThreads) fwd_warp_kernel(const FwdArgs a)
     int64_t m0 = 0;
     bool mvec = ALIGNED;
     if (a.mask) {
-        const int64_t h = (r / cols) % a.heads;
-        const int64_t b = r / (cols * a.heads);
         m0 = b * a.msb + h * a.msh + q * cols;
         ms = reinterpret_cast<const T *>(a.mask) + m0;
         if (!ALIGNED) mvec = ((m0 - xoff) & (VEC - 1)) == 0;
@@ -136,8 +135,7 @@ __global__ void __launch_bounds__(kThreads) bwd_warp_kernel(const BwdArgs a)
     const bool live = row < a.rows;
     const int64_t r = live ? row : a.rows - 1;
     const int64_t cols = a.cols;
-    const int64_t q = r % cols;
-    const int limit = a.causal ? (int)(q + 1) : (int)cols;
+    const int limit = a.causal ? (int)(row_q(r, cols, a.dcols) + 1) : (int)cols;
     const int64_t x0 = r * cols;
     const int xoff = ALIGNED ? 0 : (int)(x0 & (VEC - 1));
     const T *ys = reinterpret_cast<const T *>(a.y) + (x0 - xoff);

@@ -75,6 +75,9 @@ def test_backward_rejects_bad_arguments(kw):
 def test_rows_zero_is_a_noop_without_device():
     assert _fwd(rows=0) == binding.SMS_OK
     assert _bwd(rows=0) == binding.SMS_OK
+    assert _fwd(rows=0, x=None, y=None) == binding.SMS_OK  # empty tensors have NULL data pointers
+    assert _bwd(rows=0, y=None, dy=None, dx=None) == binding.SMS_OK
+    assert _fwd(rows=0, cols=0) == INVALID
 
 
 def test_in_place_aliasing_passes_validation():
