@@ -290,32 +290,39 @@ def run_ours(args, rank, world, device):
 
 
 def run_e2e(args, w, inp, device, steps):
-    """Same metric through the public API with host buffers: per step, H2D of
-    x (+mask) and dy from pinned memory, forward + backward, D2H of y and dx."""
+    """Same metric through the C ABI with host buffers: per step, H2D of x
+    (+mask) and dy from pinned memory, forward + backward, D2H of y and dx."""
     import scaled_masked_softmax_gb300 as sms
 
+    L = sms.binding.lib()
     hx = inp["x"].cpu().pin_memory()
     hm = inp["mask"].cpu().pin_memory() if inp["mask"] is not None else None
     hdy = inp["dy"].cpu().pin_memory()
     hy = torch.empty_like(hx).pin_memory()
     hdx = torch.empty_like(hx).pin_memory()
-    dx_ = torch.empty_like(inp["x"])
-    dm = torch.empty_like(inp["mask"]) if hm is not None else None
-    ddy = torch.empty_like(inp["dy"])
-    dy_ = torch.empty_like(inp["x"])
-    ddx = torch.empty_like(inp["x"])
+    d_x = torch.empty_like(inp["x"])
+    d_m = torch.empty_like(inp["mask"]) if hm is not None else None
+    d_dy = torch.empty_like(inp["dy"])
+    d_y = torch.empty_like(inp["x"])
+    d_dx = torch.empty_like(inp["x"])
     stream = torch.cuda.current_stream(device)
-    shape = (w.B, w.H, w.S, w.S) if w.rows_override is None else (w.rows, w.S)
+    st = stream.cuda_stream
+    dt = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}[hx.dtype]
 
     def step():
-        dx_.copy_(hx, non_blocking=True)
+        d_x.copy_(hx, non_blocking=True)
         if hm is not None:
-            dm.copy_(hm, non_blocking=True)
-        ddy.copy_(hdy, non_blocking=True)
-        sms.forward(dx_.view(shape), None if dm is None else dm, w.scale, w.is_causal, out=dy_.view(shape))
-        sms.backward(dy_.view(shape), ddy.view(shape), w.scale, w.is_causal, out=ddx.view(shape))
-        hy.copy_(dy_, non_blocking=True)
-        hdx.copy_(ddx, non_blocking=True)
+            d_m.copy_(hm, non_blocking=True)
+        d_dy.copy_(hdy, non_blocking=True)
+        rc = L.sms_forward(d_x.data_ptr(), None if d_m is None else d_m.data_ptr(), 0 if d_m is None else d_m.numel(),
+                           inp["mask_stride_b"], inp["mask_stride_h"], inp["heads"], d_y.data_ptr(), w.rows, w.cols,
+                           w.scale, int(w.is_causal), dt, st)
+        rc = rc or L.sms_backward(d_y.data_ptr(), d_dy.data_ptr(), d_dx.data_ptr(), w.rows, w.cols, w.scale,
+                                  int(w.is_causal), dt, st)
+        if rc:
+            raise RuntimeError(sms.sms_last_error())
+        hy.copy_(d_y, non_blocking=True)
+        hdx.copy_(d_dx, non_blocking=True)
 
     for _ in range(2):
         step()
@@ -332,7 +339,8 @@ def run_e2e(args, w, inp, device, steps):
     d2h = hy.numel() * hy.element_size() + hdx.numel() * hdx.element_size()
     alg = fwd_bytes(w, inp) + bwd_bytes(w)
     return {"value": round(alg / (ms * 1e6), 1), "unit": "GB/s", "ms_per_step": round(ms, 3),
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "path": "C ABI (sms_forward + sms_backward) on pinned host buffers copied in and out every step"}
 
 
 # ------------------------------------------------------- oracle on the CPU ---
