@@ -104,7 +104,7 @@ int pick_path(int forced, int64_t cols, int dtype, bool aligned, bool bwd)
     if (forced != SMS_PATH_AUTO) return forced;
     // Warp-resident rows up to 1024 elements; wider rows go to the staged
     // CTA path while they fit its registers; beyond that, stream twice.
-    if (cols <= 1024 && warp_fits(cols, dtype, aligned)) return SMS_PATH_WARP;
+    if (cols <= 1024 && warp_fits(cols, dtype, aligned, bwd)) return SMS_PATH_WARP;
     if (bwd ? cta_fits_bwd(cols, dtype, aligned) : cta_fits(cols, dtype, aligned)) return SMS_PATH_CTA;
     return SMS_PATH_ONLINE;
 }
@@ -227,7 +227,7 @@ int sms_forward(const void *x, const void *mask, int64_t mask_numel, int64_t mas
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (path) {
     case SMS_PATH_WARP:
-        if (!warp_fits(cols, dtype, aligned)) return fail(SMS_ERR_UNSUPPORTED, "sms_forward: row too wide for the warp path");
+        if (!warp_fits(cols, dtype, aligned, false)) return fail(SMS_ERR_UNSUPPORTED, "sms_forward: row too wide for the warp path");
         e = launch_fwd_warp(a, dtype, aligned, st);
         break;
     case SMS_PATH_CTA:
@@ -288,7 +288,7 @@ int sms_backward(const void *y, const void *dy, void *dx, int64_t rows, int64_t 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (path) {
     case SMS_PATH_WARP:
-        if (!warp_fits(cols, dtype, aligned)) return fail(SMS_ERR_UNSUPPORTED, "sms_backward: row too wide for the warp path");
+        if (!warp_fits(cols, dtype, aligned, true)) return fail(SMS_ERR_UNSUPPORTED, "sms_backward: row too wide for the warp path");
         e = launch_bwd_warp(a, dtype, aligned, st);
         break;
     case SMS_PATH_CTA:

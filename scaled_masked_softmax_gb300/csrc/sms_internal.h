@@ -44,7 +44,7 @@ struct BwdArgs {
 // cols and both mask strides are multiples of the 16-byte vector width.
 
 // warp-per-row (or a power-of-two part of a warp per row), rows in registers
-bool warp_fits(int64_t cols, int dtype, bool aligned);
+bool warp_fits(int64_t cols, int dtype, bool aligned, bool bwd);
 cudaError_t launch_fwd_warp(const FwdArgs &a, int dtype, bool aligned, cudaStream_t st);
 cudaError_t launch_bwd_warp(const BwdArgs &a, int dtype, bool aligned, cudaStream_t st);
 

@@ -40,15 +40,17 @@ constexpr int kMaxStages = 32;
 struct __align__(16) ChunkDesc {
     int64_t x0;      // flat element index of the row start
     int64_t m0;      // mask row start (elements)
-    int64_t mv_lo;   // first mask vector (tensor index) held by the stage
-    int64_t cm_hi;   // one past the last mask vector held by the stage
+    int32_t mrel;    // stage index of mask element j is j + mrel
+    int32_t mcnt;    // mask elements held by the stage
+    int32_t mvec;    // mask row aligned like the x row: 16-byte stage reads
+    int32_t pad0;
     int32_t cx_hi;   // one past the last row vector (row-relative) held by the stage
     int32_t xoff;    // x0 mod VEC
     int32_t limit;   // elements read: q+1 under causal, else cols
     int32_t nv_read; // vectors holding elements < limit
     int32_t nv_row;  // vectors holding row elements
     int32_t nchunks; // stages the row occupies
-    int32_t pad0, pad1;
+    int32_t pad1, pad2;
 };
 static_assert(sizeof(ChunkDesc) == 64, "descriptor is one 64-byte slot");
 
@@ -64,15 +66,18 @@ template <int NT> struct Geo {
 template <int NT> struct Hdr {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
-    float red_max[Geo<NT>::NW];
-    float red_sum[2][Geo<NT>::NW];  // double buffered by row parity (one barrier per row in backward)
+    float red_max[2][Geo<NT>::NW];  // double buffered by row parity: one barrier per row
+    float red_sum[2][Geo<NT>::NW];
     int abort;                      // any thread gave up (producer or consumer)
     int cons_abort;                 // a consumer gave up (read only after a consumer barrier)
 };
 template <int NT> __host__ __device__ constexpr int hdr_bytes() { return (int)((sizeof(Hdr<NT>) + 127) / 128 * 128); }
 
+// CTAs resident per SM: 512 / NT (shared memory is split the same way)
+template <int NT> __host__ __device__ constexpr int ctas_per_sm() { return NT >= 512 ? 1 : 512 / NT; }
+
 template <typename T, int NT, int SLOTS, bool BWD>
-__global__ void __launch_bounds__(Geo<NT>::THREADS, 1)
+__global__ void __launch_bounds__(Geo<NT>::THREADS, ctas_per_sm<NT>())
     cta_kernel(const FwdArgs fa, const BwdArgs ba, int nstage)
 {
     using G = Geo<NT>;
@@ -129,7 +134,8 @@ __global__ void __launch_bounds__(Geo<NT>::THREADS, 1)
             d.nv_row = (int)((d.xoff + cols + VEC - 1) / VEC);
             d.nchunks = (d.nv_read + SV - 1) / SV;
             d.m0 = (!BWD && srcB) ? bb * fa.msb + hh * fa.msh + q * cols : 0;
-            d.pad0 = d.pad1 = 0;
+            d.mvec = ((d.m0 - d.xoff) & (VEC - 1)) == 0;
+            d.pad0 = d.pad1 = d.pad2 = 0;
             for (int c = 0; c < d.nchunks; ++c) {
                 if (!mbar_wait_bounded(&h.empty[stage], ph ^ 1u, abort_flag)) {
                     *abort_flag = 1;
@@ -143,18 +149,20 @@ __global__ void __launch_bounds__(Geo<NT>::THREADS, 1)
                 const uint32_t bytesA = d.cx_hi > vlo ? (uint32_t)(d.cx_hi - vlo) * 16u : 0u;
                 uint32_t bytesB = 0;
                 int64_t b_src = 0;
-                d.mv_lo = 0;
-                d.cm_hi = 0;
+                d.mrel = 0;
+                d.mcnt = 0;
                 if (BWD) {
                     bytesB = bytesA;
                     b_src = gbase + vlo;
                 } else if (srcB) {
                     const int64_t jlo = max(0, vlo * VEC - d.xoff);
                     const int64_t jhi = min((int64_t)d.limit, (int64_t)vhi * VEC - d.xoff);
-                    d.mv_lo = (d.m0 + jlo) / VEC;
-                    d.cm_hi = min((d.m0 + jhi + VEC - 1) / VEC, fa.mask_total / VEC);
-                    bytesB = d.cm_hi > d.mv_lo ? (uint32_t)(d.cm_hi - d.mv_lo) * 16u : 0u;
-                    b_src = d.mv_lo;
+                    const int64_t mv_lo = (d.m0 + jlo) / VEC;
+                    const int64_t cm_hi = min((d.m0 + jhi + VEC - 1) / VEC, fa.mask_total / VEC);
+                    d.mrel = (int)(d.m0 - mv_lo * VEC);
+                    d.mcnt = cm_hi > mv_lo ? (int)(cm_hi - mv_lo) * VEC : 0;
+                    bytesB = cm_hi > mv_lo ? (uint32_t)(cm_hi - mv_lo) * 16u : 0u;
+                    b_src = mv_lo;
                 }
                 unsigned char *st = stages + (size_t)stage * G::STAGE;
                 *reinterpret_cast<ChunkDesc *>(st) = d;  // visible to consumers through the barrier
@@ -267,20 +275,18 @@ __global__ void __launch_bounds__(Geo<NT>::THREADS, 1)
 #pragma unroll
                         for (int e = 0; e < VEC; ++e) b[e] = 0.f;
                         if (srcB) {
-                            const int64_t m0 = d.m0, mv_lo = d.mv_lo, cm_hi = d.cm_hi;
                             const T *msm = reinterpret_cast<const T *>(st + G::B_OFF);
-                            const int64_t mvi = (m0 - xoff) / VEC + vi;
-                            const bool mvec = ((m0 - xoff) & (VEC - 1)) == 0;
-                            if (mvec && mvi >= mv_lo && mvi < cm_hi) {
-                                unpack<T>(reinterpret_cast<const uint4 *>(msm)[mvi - mv_lo], b);
+                            const int jj = j0 + d.mrel;  // stage index of element j0
+                            if (d.mvec && jj >= 0 && jj + VEC <= d.mcnt) {
+                                unpack<T>(*reinterpret_cast<const uint4 *>(msm + jj), b);
                             } else {
-                                const T *mrow = reinterpret_cast<const T *>(srcB) + m0;
+                                const T *mrow = reinterpret_cast<const T *>(srcB) + d.m0;
 #pragma unroll
                                 for (int e = 0; e < VEC; ++e) {
                                     const int j = j0 + e;
                                     if (j >= 0 && j < limit) {
-                                        const int64_t f = m0 + j;
-                                        b[e] = f < cm_hi * VEC ? to_f32<T>(msm[f - mv_lo * VEC]) : to_f32<T>(mrow[j]);
+                                        const int idx = j + d.mrel;
+                                        b[e] = idx < d.mcnt ? to_f32<T>(msm[idx]) : to_f32<T>(mrow[j]);
                                     }
                                 }
                             }
@@ -302,7 +308,7 @@ __global__ void __launch_bounds__(Geo<NT>::THREADS, 1)
         if (BWD) {
             acc = group_sum<32>(acc);
             if (lane == 0) h.red_sum[rp][warp] = acc;
-            named_sync(1, NT);
+            named_sync(1, NT);  // one barrier per row
             if (h.cons_abort) break;  // uniform: every consumer reads the same value here
             float dot = 0.f;
 #pragma unroll
@@ -333,30 +339,40 @@ __global__ void __launch_bounds__(Geo<NT>::THREADS, 1)
                 }
             }
         } else {
-            acc = group_max<32>(acc);
-            if (lane == 0) h.red_max[warp] = acc;
-            named_sync(1, NT);
-            if (h.cons_abort) break;  // uniform: every consumer reads the same value here
-            float mx = neg_inf();
-#pragma unroll
-            for (int w = 0; w < G::NW; ++w) mx = fmaxf(mx, h.red_max[w]);
-            const float mref = (mx == neg_inf()) ? 0.f : mx;
-            float sum = 0.f;
+            // one barrier per row: each thread exponentiates against its own
+            // max, warps merge (max, sum) pairs, the CTA merges the warps' pairs
+            const float mt = acc;
+            const float mtr = (mt == neg_inf()) ? 0.f : mt;
+            float lt = 0.f;
 #pragma unroll
             for (int k = 0; k < SLOTS; ++k)
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) {
-                    const float v = ex2((va[k][e] - mref) * kLog2e);
+                    const float v = ex2((va[k][e] - mtr) * kLog2e);
                     va[k][e] = v;
-                    sum += v;
+                    lt += v;
                 }
-            sum = group_sum<32>(sum);
-            if (lane == 0) h.red_sum[rp][warp] = sum;
+            const float mw = group_max<32>(mt);
+            const float mwr = (mw == neg_inf()) ? 0.f : mw;
+            const float lw = group_sum<32>(mt == neg_inf() ? 0.f : lt * ex2((mt - mwr) * kLog2e));
+            if (lane == 0) {
+                h.red_max[rp][warp] = mw;
+                h.red_sum[rp][warp] = lw;
+            }
             named_sync(1, NT);
+            if (h.cons_abort) break;  // uniform: every consumer reads the same value here
+            float M = neg_inf();
+#pragma unroll
+            for (int w = 0; w < G::NW; ++w) M = fmaxf(M, h.red_max[rp][w]);
+            const float Mr = (M == neg_inf()) ? 0.f : M;
             float tot = 0.f;
 #pragma unroll
-            for (int w = 0; w < G::NW; ++w) tot += h.red_sum[rp][w];
+            for (int w = 0; w < G::NW; ++w) {
+                const float m2 = h.red_max[rp][w];
+                tot += (m2 == neg_inf()) ? 0.f : h.red_sum[rp][w] * ex2((m2 - Mr) * kLog2e);
+            }
             const float inv = tot > 0.f ? __frcp_rn(tot) : 0.f;
+            const float f = (mt == neg_inf()) ? 0.f : ex2((mt - Mr) * kLog2e) * inv;  // this thread's factor
             T *orow = reinterpret_cast<T *>(fa.y) + (x0 - xoff);
 #pragma unroll
             for (int k = 0; k < SLOTS; ++k) {
@@ -365,7 +381,7 @@ __global__ void __launch_bounds__(Geo<NT>::THREADS, 1)
                 if (vi >= nv_row) continue;
                 float o[VEC];
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) o[e] = va[k][e] * inv;
+                for (int e = 0; e < VEC; ++e) o[e] = va[k][e] * f;
                 if (j0 >= 0 && j0 + VEC <= cols) {
                     st_stream(orow + vi * VEC, pack<T>(o));
                 } else {
@@ -380,8 +396,8 @@ __global__ void __launch_bounds__(Geo<NT>::THREADS, 1)
     }
 }
 
-// Shared memory per CTA: 1 CTA/SM for NT=512 (~200 KB), 2 CTAs/SM for NT=256.
-template <int NT> constexpr int smem_target() { return NT >= 512 ? 200 * 1024 : 100 * 1024; }
+// ~200 KB of shared memory per SM, split over the resident CTAs.
+template <int NT> constexpr int smem_target() { return 200 * 1024 / ctas_per_sm<NT>(); }
 template <int NT> constexpr int n_stages()
 {
     return (smem_target<NT>() - hdr_bytes<NT>()) / Geo<NT>::STAGE < kMaxStages
@@ -427,9 +443,14 @@ inline int64_t row_vectors(int64_t cols, int dtype, bool aligned)
     return (cols + vec - 1) / vec + (aligned ? 0 : 1);
 }
 
-// Consumer threads: 256 while a row spans at most 4 vectors per thread of a
-// 256-thread CTA, else 512.  Register slots = vectors per consumer thread.
-inline int pick_nt(int64_t vecs) { return vecs <= 4 * 256 ? 256 : 512; }
+// Consumer threads: the smallest of 128 / 256 / 512 that keeps a row within
+// `slots` register slots (16-byte vectors per thread); smaller CTAs run more
+// rows per SM at once (4 / 2 / 1 CTAs per SM).  The 16-bit forward holds 8
+// fp32 scores per slot, so it aims at 4 slots.
+inline int pick_nt(int64_t vecs, int slots)
+{
+    return vecs <= slots * 128 ? 128 : (vecs <= slots * 256 ? 256 : 512);
+}
 
 template <typename T, bool BWD, int NT>
 cudaError_t launch_nt(const FwdArgs &fa, const BwdArgs &ba, int64_t vecs, cudaStream_t st)
@@ -438,11 +459,9 @@ cudaError_t launch_nt(const FwdArgs &fa, const BwdArgs &ba, int64_t vecs, cudaSt
     if (s <= 1) return launch_one<T, NT, 1, BWD>(fa, ba, st);
     if (s <= 2) return launch_one<T, NT, 2, BWD>(fa, ba, st);
     if (s <= 4) return launch_one<T, NT, 4, BWD>(fa, ba, st);
-    if constexpr (NT == 512) {
-        if (s <= 8) return launch_one<T, NT, 8, BWD>(fa, ba, st);
-        if constexpr (!BWD && Dt<T>::VEC == 4) {
-            if (s <= 16) return launch_one<T, NT, 16, BWD>(fa, ba, st);
-        }
+    if (s <= 8) return launch_one<T, NT, 8, BWD>(fa, ba, st);
+    if constexpr (NT == 512 && !BWD && Dt<T>::VEC == 4) {
+        if (s <= 16) return launch_one<T, NT, 16, BWD>(fa, ba, st);
     }
     return cudaErrorNotSupported;
 }
@@ -451,7 +470,9 @@ template <typename T, bool BWD>
 cudaError_t launch_t(const FwdArgs &fa, const BwdArgs &ba, int64_t cols, int dtype, bool aligned, cudaStream_t st)
 {
     const int64_t vecs = row_vectors(cols, dtype, aligned);
-    if (pick_nt(vecs) == 256) return launch_nt<T, BWD, 256>(fa, ba, vecs, st);
+    const int nt = pick_nt(vecs, (!BWD && Dt<T>::VEC == 8) ? 4 : 8);
+    if (nt == 128) return launch_nt<T, BWD, 128>(fa, ba, vecs, st);
+    if (nt == 256) return launch_nt<T, BWD, 256>(fa, ba, vecs, st);
     return launch_nt<T, BWD, 512>(fa, ba, vecs, st);
 }
 

@@ -21,187 +21,246 @@ namespace {
 
 constexpr int kThreads = 256;  // 8 warps per CTA
 
-template <typename T, int G, int NV, bool ALIGNED>
-__global__ void __launch_bounds__(kThreads) fwd_warp_kernel(const FwdArgs a)
+// One lane group (G lanes) handles RPG consecutive rows at once: every raw
+// 16-byte load of all RPG rows is issued before any arithmetic, so each lane
+// keeps RPG*NV vectors in flight; the RPG reductions then run as independent
+// shuffle chains.
+template <typename T, int G, int NV, int RPG, bool ALIGNED>
+__global__ void __launch_bounds__(kThreads, 2) fwd_warp_kernel(const FwdArgs a)
 {
     constexpr int VEC = Dt<T>::VEC;
-    constexpr int RPW = 32 / G;  // rows per warp
+    constexpr int GPW = 32 / G;  // groups per warp
     const int lane = threadIdx.x & 31;
     const int gl = lane & (G - 1);
-    const int64_t row = ((int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * RPW + lane / G;
-    const bool live = row < a.rows;
-    const int64_t r = live ? row : a.rows - 1;  // dead lanes still join the shuffles
+    const int64_t row0 = (((int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * GPW + lane / G) * RPG;
     const int64_t cols = a.cols;
-    int64_t q = 0, h = 0, b = 0;
-    if (a.causal || a.mask) split_row(r, cols, a.heads, a.dcols, a.dheads, q, h, b);
-    const int limit = a.causal ? (int)(q + 1) : (int)cols;  // elements that are read
-    const int64_t x0 = r * cols;
-    const int xoff = ALIGNED ? 0 : (int)(x0 & (VEC - 1));
-    const T *xs = reinterpret_cast<const T *>(a.x) + (x0 - xoff);
 
-    const T *ms = nullptr;
-    int64_t m0 = 0;
-    bool mvec = ALIGNED;
-    if (a.mask) {
-        m0 = b * a.msb + h * a.msh + q * cols;
-        ms = reinterpret_cast<const T *>(a.mask) + m0;
-        if (!ALIGNED) mvec = ((m0 - xoff) & (VEC - 1)) == 0;
+    int64_t x0[RPG];
+    int xoff[RPG], limit[RPG];
+    const T *ms[RPG];
+    bool mvec[RPG], live[RPG];
+    uint4 xr[RPG][NV], mr[RPG][NV];
+
+#pragma unroll
+    for (int i = 0; i < RPG; ++i) {
+        live[i] = row0 + i < a.rows;
+        const int64_t r = live[i] ? row0 + i : a.rows - 1;  // dead rows still join the shuffles
+        int64_t q = 0, h = 0, b = 0;
+        if (a.causal || a.mask) split_row(r, cols, a.heads, a.dcols, a.dheads, q, h, b);
+        limit[i] = a.causal ? (int)(q + 1) : (int)cols;
+        x0[i] = r * cols;
+        xoff[i] = ALIGNED ? 0 : (int)(x0[i] & (VEC - 1));
+        ms[i] = nullptr;
+        mvec[i] = ALIGNED;
+        if (a.mask) {
+            const int64_t m0 = b * a.msb + h * a.msh + q * cols;
+            ms[i] = reinterpret_cast<const T *>(a.mask) + m0;
+            if (!ALIGNED) mvec[i] = ((m0 - xoff[i]) & (VEC - 1)) == 0 && m0 - xoff[i] + (int64_t)G * NV * VEC <= a.mask_total;
+        }
+    }
+    // issue every full-vector load first
+#pragma unroll
+    for (int i = 0; i < RPG; ++i) {
+        const T *xs = reinterpret_cast<const T *>(a.x) + (x0[i] - xoff[i]);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int vi = k * G + gl;
+            const int j0 = vi * VEC - xoff[i];
+            xr[i][k] = make_uint4(0, 0, 0, 0);
+            mr[i][k] = make_uint4(0, 0, 0, 0);
+            if (j0 < limit[i]) {
+                if (ALIGNED || x0[i] - xoff[i] + (int64_t)(vi + 1) * VEC <= a.x_total) xr[i][k] = ld_stream(xs + vi * VEC);
+                if (ms[i] && mvec[i]) mr[i][k] = ld_keep(ms[i] + j0);
+            }
+        }
     }
 
-    float s[NV][VEC];
-    float mx = neg_inf();
+    float s[RPG][NV][VEC];
+    float mx[RPG];
 #pragma unroll
-    for (int k = 0; k < NV; ++k) {
-        const int vi = k * G + gl;
-        const int j0 = vi * VEC - xoff;
-        float xv[VEC], mv[VEC];
+    for (int i = 0; i < RPG; ++i) {
+        mx[i] = neg_inf();
+        const T *xs = reinterpret_cast<const T *>(a.x) + (x0[i] - xoff[i]);
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) { xv[e] = 0.f; mv[e] = 0.f; }
-        const bool any = j0 < limit;
-        if (any) {
-            const int64_t g = x0 - xoff + (int64_t)vi * VEC;
-            if (ALIGNED || g + VEC <= a.x_total) {
-                unpack<T>(ld_stream(xs + vi * VEC), xv);
-            } else {
+        for (int k = 0; k < NV; ++k) {
+            const int vi = k * G + gl;
+            const int j0 = vi * VEC - xoff[i];
+            float xv[VEC], mv[VEC];
+            unpack<T>(xr[i][k], xv);
+            unpack<T>(mr[i][k], mv);
+            if (!ALIGNED && j0 < limit[i]) {
+                const int64_t g = x0[i] - xoff[i] + (int64_t)vi * VEC;
+                if (g + VEC > a.x_total) {  // last partial vector of the tensor
 #pragma unroll
-                for (int e = 0; e < VEC; ++e)
-                    if (g + e < a.x_total) xv[e] = to_f32<T>(xs[vi * VEC + e]);
-            }
-            if (ms) {
-                if (mvec && (ALIGNED || m0 + j0 + VEC <= a.mask_total)) {
-                    unpack<T>(ld_keep(ms + j0), mv);
-                } else {
+                    for (int e = 0; e < VEC; ++e) xv[e] = g + e < a.x_total ? to_f32<T>(xs[vi * VEC + e]) : 0.f;
+                }
+                if (ms[i] && !mvec[i]) {  // mask row not aligned like the x row: element loads
 #pragma unroll
                     for (int e = 0; e < VEC; ++e) {
                         const int j = j0 + e;
-                        if (j >= 0 && j < limit) mv[e] = to_f32<T>(ms[j]);
+                        mv[e] = (j >= 0 && j < limit[i]) ? to_f32<T>(ms[i][j]) : 0.f;
                     }
                 }
             }
-        }
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-            const int j = j0 + e;
-            const bool valid = any && j >= 0 && j < limit;
-            s[k][e] = valid ? fmaf(xv[e], a.scale, mv[e]) : neg_inf();
-            mx = fmaxf(mx, s[k][e]);
-        }
-    }
-
-    mx = group_max<G>(mx);
-    const float mref = (mx == neg_inf()) ? 0.f : mx;  // fully masked row: every term becomes 0
-    float sum = 0.f;
-#pragma unroll
-    for (int k = 0; k < NV; ++k)
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-            const float t = ex2((s[k][e] - mref) * kLog2e);
-            s[k][e] = t;
-            sum += t;
-        }
-    sum = group_sum<G>(sum);
-    const float inv = sum > 0.f ? __frcp_rn(sum) : 0.f;
-    if (!live) return;
-
-    T *ys = reinterpret_cast<T *>(a.y) + (x0 - xoff);
-#pragma unroll
-    for (int k = 0; k < NV; ++k) {
-        const int vi = k * G + gl;
-        const int j0 = vi * VEC - xoff;
-        if (j0 >= cols) continue;
-        float o[VEC];
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) o[e] = s[k][e] * inv;
-        if (ALIGNED || (j0 >= 0 && j0 + VEC <= cols)) {
-            st_stream(ys + vi * VEC, pack<T>(o));
-        } else {
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
                 const int j = j0 + e;
-                if (j >= 0 && j < cols) ys[vi * VEC + e] = from_f32<T>(o[e]);
+                const bool valid = j >= 0 && j < limit[i];
+                s[i][k][e] = valid ? fmaf(xv[e], a.scale, mv[e]) : neg_inf();
+                mx[i] = fmaxf(mx[i], s[i][k][e]);
             }
         }
     }
-}
-
-template <typename T, int G, int NV, bool ALIGNED>
-__global__ void __launch_bounds__(kThreads) bwd_warp_kernel(const BwdArgs a)
-{
-    constexpr int VEC = Dt<T>::VEC;
-    constexpr int RPW = 32 / G;
-    const int lane = threadIdx.x & 31;
-    const int gl = lane & (G - 1);
-    const int64_t row = ((int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * RPW + lane / G;
-    const bool live = row < a.rows;
-    const int64_t r = live ? row : a.rows - 1;
-    const int64_t cols = a.cols;
-    const int limit = a.causal ? (int)(row_q(r, cols, a.dcols) + 1) : (int)cols;
-    const int64_t x0 = r * cols;
-    const int xoff = ALIGNED ? 0 : (int)(x0 & (VEC - 1));
-    const T *ys = reinterpret_cast<const T *>(a.y) + (x0 - xoff);
-    const T *gs = reinterpret_cast<const T *>(a.dy) + (x0 - xoff);
-
-    float yv[NV][VEC], gv[NV][VEC];
-    float dot = 0.f;
+    float sum[RPG];
 #pragma unroll
-    for (int k = 0; k < NV; ++k) {
-        const int vi = k * G + gl;
-        const int j0 = vi * VEC - xoff;
+    for (int i = 0; i < RPG; ++i) {
+        mx[i] = group_max<G>(mx[i]);
+        const float mref = (mx[i] == neg_inf()) ? 0.f : mx[i];  // fully masked row: every term becomes 0
+        sum[i] = 0.f;
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) { yv[k][e] = 0.f; gv[k][e] = 0.f; }
-        if (j0 < limit) {
-            const int64_t g = x0 - xoff + (int64_t)vi * VEC;
-            float tv[VEC], tg[VEC];
-            if (ALIGNED || g + VEC <= a.total) {
-                unpack<T>(ld_stream(ys + vi * VEC), tv);
-                unpack<T>(ld_stream(gs + vi * VEC), tg);
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                const float t = ex2((s[i][k][e] - mref) * kLog2e);
+                s[i][k][e] = t;
+                sum[i] += t;
+            }
+    }
+#pragma unroll
+    for (int i = 0; i < RPG; ++i) {
+        sum[i] = group_sum<G>(sum[i]);
+        const float inv = sum[i] > 0.f ? __frcp_rn(sum[i]) : 0.f;
+        if (!live[i]) continue;
+        T *ys = reinterpret_cast<T *>(a.y) + (x0[i] - xoff[i]);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int vi = k * G + gl;
+            const int j0 = vi * VEC - xoff[i];
+            if (j0 >= cols) continue;
+            float o[VEC];
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) o[e] = s[i][k][e] * inv;
+            if (ALIGNED || (j0 >= 0 && j0 + VEC <= cols)) {
+                st_stream(ys + vi * VEC, pack<T>(o));
             } else {
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) {
-                    const bool in = g + e < a.total;
-                    tv[e] = in ? to_f32<T>(ys[vi * VEC + e]) : 0.f;
-                    tg[e] = in ? to_f32<T>(gs[vi * VEC + e]) : 0.f;
+                    const int j = j0 + e;
+                    if (j >= 0 && j < cols) ys[vi * VEC + e] = from_f32<T>(o[e]);
                 }
-            }
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const int j = j0 + e;
-                const bool valid = j >= 0 && j < limit;
-                yv[k][e] = valid ? tv[e] : 0.f;
-                gv[k][e] = valid ? tg[e] : 0.f;
-                dot = fmaf(yv[k][e], gv[k][e], dot);
-            }
-        }
-    }
-    dot = group_sum<G>(dot);
-    if (!live) return;
-
-    T *dxs = reinterpret_cast<T *>(a.dx) + (x0 - xoff);
-#pragma unroll
-    for (int k = 0; k < NV; ++k) {
-        const int vi = k * G + gl;
-        const int j0 = vi * VEC - xoff;
-        if (j0 >= cols) continue;
-        float o[VEC];
-#pragma unroll
-        for (int e = 0; e < VEC; ++e)  // y == 0 (masked) gives exactly +0
-            o[e] = (yv[k][e] == 0.f) ? 0.f : (gv[k][e] - dot) * yv[k][e] * a.scale;
-        if (ALIGNED || (j0 >= 0 && j0 + VEC <= cols)) {
-            st_stream(dxs + vi * VEC, pack<T>(o));
-        } else {
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const int j = j0 + e;
-                if (j >= 0 && j < cols) dxs[vi * VEC + e] = from_f32<T>(o[e]);
             }
         }
     }
 }
 
-template <typename T, int G, int NV, bool ALIGNED, bool BWD, typename Args>
+template <typename T, int G, int NV, int RPG, bool ALIGNED>
+__global__ void __launch_bounds__(kThreads, 2) bwd_warp_kernel(const BwdArgs a)
+{
+    constexpr int VEC = Dt<T>::VEC;
+    constexpr int GPW = 32 / G;
+    const int lane = threadIdx.x & 31;
+    const int gl = lane & (G - 1);
+    const int64_t row0 = (((int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * GPW + lane / G) * RPG;
+    const int64_t cols = a.cols;
+
+    int64_t x0[RPG];
+    int xoff[RPG], limit[RPG];
+    bool live[RPG];
+    uint4 yr[RPG][NV], gr[RPG][NV];
+#pragma unroll
+    for (int i = 0; i < RPG; ++i) {
+        live[i] = row0 + i < a.rows;
+        const int64_t r = live[i] ? row0 + i : a.rows - 1;
+        limit[i] = a.causal ? (int)(row_q(r, cols, a.dcols) + 1) : (int)cols;
+        x0[i] = r * cols;
+        xoff[i] = ALIGNED ? 0 : (int)(x0[i] & (VEC - 1));
+    }
+#pragma unroll
+    for (int i = 0; i < RPG; ++i) {
+        const T *ys = reinterpret_cast<const T *>(a.y) + (x0[i] - xoff[i]);
+        const T *gs = reinterpret_cast<const T *>(a.dy) + (x0[i] - xoff[i]);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int vi = k * G + gl;
+            const int j0 = vi * VEC - xoff[i];
+            yr[i][k] = make_uint4(0, 0, 0, 0);
+            gr[i][k] = make_uint4(0, 0, 0, 0);
+            if (j0 < limit[i] && (ALIGNED || x0[i] - xoff[i] + (int64_t)(vi + 1) * VEC <= a.total)) {
+                yr[i][k] = ld_stream(ys + vi * VEC);
+                gr[i][k] = ld_stream(gs + vi * VEC);
+            }
+        }
+    }
+    float dot[RPG];
+#pragma unroll
+    for (int i = 0; i < RPG; ++i) {
+        dot[i] = 0.f;
+        const T *ys = reinterpret_cast<const T *>(a.y) + (x0[i] - xoff[i]);
+        const T *gs = reinterpret_cast<const T *>(a.dy) + (x0[i] - xoff[i]);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int vi = k * G + gl;
+            const int j0 = vi * VEC - xoff[i];
+            if (!ALIGNED && j0 < limit[i]) {
+                const int64_t g = x0[i] - xoff[i] + (int64_t)vi * VEC;
+                if (g + VEC > a.total) {  // last partial vector of the tensor
+                    float tv[VEC], tg[VEC];
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) {
+                        const bool in = g + e < a.total;
+                        tv[e] = in ? to_f32<T>(ys[vi * VEC + e]) : 0.f;
+                        tg[e] = in ? to_f32<T>(gs[vi * VEC + e]) : 0.f;
+                    }
+                    yr[i][k] = pack<T>(tv);
+                    gr[i][k] = pack<T>(tg);
+                }
+            }
+            float yv[VEC], gv[VEC];
+            unpack<T>(yr[i][k], yv);
+            unpack<T>(gr[i][k], gv);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                const int j = j0 + e;
+                if (j >= 0 && j < limit[i]) dot[i] = fmaf(yv[e], gv[e], dot[i]);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < RPG; ++i) {
+        dot[i] = group_sum<G>(dot[i]);
+        if (!live[i]) continue;
+        T *dxs = reinterpret_cast<T *>(a.dx) + (x0[i] - xoff[i]);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int vi = k * G + gl;
+            const int j0 = vi * VEC - xoff[i];
+            if (j0 >= cols) continue;
+            float yv[VEC], gv[VEC], o[VEC];
+            unpack<T>(yr[i][k], yv);
+            unpack<T>(gr[i][k], gv);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                const int j = j0 + e;
+                const bool valid = j >= 0 && j < limit[i];  // y == 0 (masked) gives exactly +0
+                o[e] = (!valid || yv[e] == 0.f) ? 0.f : (gv[e] - dot[i]) * yv[e] * a.scale;
+            }
+            if (ALIGNED || (j0 >= 0 && j0 + VEC <= cols)) {
+                st_stream(dxs + vi * VEC, pack<T>(o));
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const int j = j0 + e;
+                    if (j >= 0 && j < cols) dxs[vi * VEC + e] = from_f32<T>(o[e]);
+                }
+            }
+        }
+    }
+}
+
+template <typename T, int G, int NV, int RPG, bool ALIGNED, bool BWD, typename Args>
 cudaError_t launch_one(const Args &a, cudaStream_t st)
 {
-    constexpr int rows_per_cta = (kThreads / 32) * (32 / G);
+    constexpr int rows_per_cta = (kThreads / 32) * (32 / G) * RPG;
     const int64_t blocks = (a.rows + rows_per_cta - 1) / rows_per_cta;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg = {};
@@ -209,23 +268,31 @@ cudaError_t launch_one(const Args &a, cudaStream_t st)
     cfg.blockDim = dim3(kThreads);
     cfg.stream = st;
     if constexpr (BWD)
-        return cudaLaunchKernelEx(&cfg, bwd_warp_kernel<T, G, NV, ALIGNED>, a);
+        return cudaLaunchKernelEx(&cfg, bwd_warp_kernel<T, G, NV, RPG, ALIGNED>, a);
     else
-        return cudaLaunchKernelEx(&cfg, fwd_warp_kernel<T, G, NV, ALIGNED>, a);
+        return cudaLaunchKernelEx(&cfg, fwd_warp_kernel<T, G, NV, RPG, ALIGNED>, a);
 }
 
-// Lane-group / vectors-per-lane shapes, smallest first.  Capacity = G*NV
-// vectors; a lane holds at most 64 fp32 values.
+// (lanes per row, vectors per lane per row, rows per lane group), smallest
+// capacity first.  Capacity = G*NV vectors; each lane keeps RPG*NV vectors
+// per input stream in flight: 8 for fp32 rows, 4 for 16-bit rows (32 fp32
+// values either way), except the 16-bit forward's widest shapes (6-8).
 template <typename T, bool ALIGNED, bool BWD, typename Args>
 cudaError_t launch_t(const Args &a, cudaStream_t st)
 {
     constexpr int VEC = Dt<T>::VEC;
     const int64_t need = (a.cols + VEC - 1) / VEC + (ALIGNED ? 0 : 1);
-#define SMS_TRY(G, NV) \
-    if (need <= (G) * (NV)) return launch_one<T, G, NV, ALIGNED, BWD>(a, st);
-    SMS_TRY(4, 1) SMS_TRY(8, 1) SMS_TRY(16, 1) SMS_TRY(32, 1) SMS_TRY(32, 2) SMS_TRY(32, 3) SMS_TRY(32, 4)
-    SMS_TRY(32, 6) SMS_TRY(32, 8)
-    if constexpr (VEC == 4) { SMS_TRY(32, 12) SMS_TRY(32, 16) }
+    // rows that may start mid-vector carry more bookkeeping: half the rows per group
+#define SMS_TRY(G, NV, RPG) \
+    if (need <= (G) * (NV)) return launch_one<T, G, NV, (ALIGNED || (RPG) == 1 ? (RPG) : (RPG) / 2), ALIGNED, BWD>(a, st);
+    if constexpr (VEC == 4) {
+        SMS_TRY(4, 1, 8) SMS_TRY(8, 1, 8) SMS_TRY(16, 1, 8) SMS_TRY(32, 1, 8) SMS_TRY(32, 2, 4) SMS_TRY(32, 3, 2)
+        SMS_TRY(32, 4, 2) SMS_TRY(32, 6, 1) SMS_TRY(32, 8, 1)
+    } else {
+        SMS_TRY(4, 1, 4) SMS_TRY(8, 1, 4) SMS_TRY(16, 1, 4) SMS_TRY(32, 1, 4) SMS_TRY(32, 2, 2) SMS_TRY(32, 3, 1)
+        SMS_TRY(32, 4, 1)
+        if constexpr (!BWD) { SMS_TRY(32, 6, 1) SMS_TRY(32, 8, 1) }
+    }
 #undef SMS_TRY
     return cudaErrorNotSupported;
 }
@@ -247,11 +314,11 @@ cudaError_t dispatch(const Args &a, int dtype, bool aligned, cudaStream_t st)
 
 }  // namespace
 
-bool warp_fits(int64_t cols, int dtype, bool aligned)
+bool warp_fits(int64_t cols, int dtype, bool aligned, bool bwd)
 {
     const int vec = vec_elems(dtype);
     const int64_t need = (cols + vec - 1) / vec + (aligned ? 0 : 1);
-    const int64_t cap = vec == 4 ? 32 * 16 : 32 * 8;
+    const int64_t cap = vec == 4 ? 32 * 8 : (bwd ? 32 * 4 : 32 * 8);
     return need <= cap;
 }
 
