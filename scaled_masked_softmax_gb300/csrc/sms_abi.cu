@@ -102,9 +102,10 @@ constexpr int64_t kMaxElems = (int64_t)1 << 60;
 int pick_path(int forced, int64_t cols, int dtype, bool aligned, bool bwd)
 {
     if (forced != SMS_PATH_AUTO) return forced;
-    // Warp-resident rows up to 1024 elements; wider rows go to the staged
-    // CTA path while they fit its registers; beyond that, stream twice.
-    if (cols <= 1024 && warp_fits(cols, dtype, aligned, bwd)) return SMS_PATH_WARP;
+    // Register-resident lane groups while a row fits them (8192 elements);
+    // wider rows go to the staged CTA path while they fit its registers;
+    // beyond that, stream twice.
+    if (warp_fits(cols, dtype, aligned, bwd)) return SMS_PATH_WARP;
     if (bwd ? cta_fits_bwd(cols, dtype, aligned) : cta_fits(cols, dtype, aligned)) return SMS_PATH_CTA;
     return SMS_PATH_ONLINE;
 }

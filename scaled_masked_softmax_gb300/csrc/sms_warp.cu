@@ -21,18 +21,20 @@ namespace {
 
 constexpr int kThreads = 256;  // 8 warps per CTA
 
-// One lane group (G lanes) handles RPG consecutive rows at once: every raw
-// 16-byte load of all RPG rows is issued before any arithmetic, so each lane
-// keeps RPG*NV vectors in flight; the RPG reductions then run as independent
-// shuffle chains.
+// One lane group (G lanes: part of a warp, a warp, or W = G/32 warps) handles
+// RPG consecutive rows at once: every raw 16-byte load of all RPG rows is
+// issued before any arithmetic, so each lane keeps RPG*NV vectors in flight.
+// Groups of one warp or less reduce with shuffles alone; multi-warp groups
+// merge per-warp (max, sum) pairs through shared memory with one barrier.
 template <typename T, int G, int NV, int RPG, bool ALIGNED>
 __global__ void __launch_bounds__(kThreads, 2) fwd_warp_kernel(const FwdArgs a)
 {
     constexpr int VEC = Dt<T>::VEC;
-    constexpr int GPW = 32 / G;  // groups per warp
-    const int lane = threadIdx.x & 31;
-    const int gl = lane & (G - 1);
-    const int64_t row0 = (((int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * GPW + lane / G) * RPG;
+    constexpr int GPC = kThreads / G;         // groups per CTA
+    constexpr int W = G > 32 ? G / 32 : 1;    // warps per group
+    const int gl = threadIdx.x % G;           // lane within the group
+    const int gi = threadIdx.x / G;           // group within the CTA
+    const int64_t row0 = ((int64_t)blockIdx.x * GPC + gi) * RPG;
     const int64_t cols = a.cols;
 
     int64_t x0[RPG];
@@ -111,25 +113,73 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_warp_kernel(const FwdArgs a)
             }
         }
     }
-    float sum[RPG];
+    float fac[RPG];  // y = e * fac, e the exponentials kept in s
+    if constexpr (G <= 32) {
+        float sum[RPG];
 #pragma unroll
-    for (int i = 0; i < RPG; ++i) {
-        mx[i] = group_max<G>(mx[i]);
-        const float mref = (mx[i] == neg_inf()) ? 0.f : mx[i];  // fully masked row: every term becomes 0
-        sum[i] = 0.f;
+        for (int i = 0; i < RPG; ++i) {
+            mx[i] = group_max<G>(mx[i]);
+            const float mref = (mx[i] == neg_inf()) ? 0.f : mx[i];  // fully masked row: every term becomes 0
+            sum[i] = 0.f;
 #pragma unroll
-        for (int k = 0; k < NV; ++k)
+            for (int k = 0; k < NV; ++k)
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const float t = ex2((s[i][k][e] - mref) * kLog2e);
-                s[i][k][e] = t;
-                sum[i] += t;
+                for (int e = 0; e < VEC; ++e) {
+                    const float t = ex2((s[i][k][e] - mref) * kLog2e);
+                    s[i][k][e] = t;
+                    sum[i] += t;
+                }
+        }
+#pragma unroll
+        for (int i = 0; i < RPG; ++i) {
+            sum[i] = group_sum<G>(sum[i]);
+            fac[i] = sum[i] > 0.f ? __frcp_rn(sum[i]) : 0.f;
+        }
+    } else {
+        // each lane exponentiates against its own max; warps merge (max, sum)
+        // pairs, the group's warps merge theirs through shared memory
+        __shared__ float red_m[GPC][RPG][W], red_l[GPC][RPG][W];
+        const int wg = gl >> 5, lane = threadIdx.x & 31;
+        float lt[RPG];
+#pragma unroll
+        for (int i = 0; i < RPG; ++i) {
+            const float mtr = (mx[i] == neg_inf()) ? 0.f : mx[i];
+            lt[i] = 0.f;
+#pragma unroll
+            for (int k = 0; k < NV; ++k)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const float t = ex2((s[i][k][e] - mtr) * kLog2e);
+                    s[i][k][e] = t;
+                    lt[i] += t;
+                }
+            const float mw = group_max<32>(mx[i]);
+            const float mwr = (mw == neg_inf()) ? 0.f : mw;
+            const float lw = group_sum<32>(mx[i] == neg_inf() ? 0.f : lt[i] * ex2((mx[i] - mwr) * kLog2e));
+            if (lane == 0) {
+                red_m[gi][i][wg] = mw;
+                red_l[gi][i][wg] = lw;
             }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < RPG; ++i) {
+            float M = neg_inf();
+#pragma unroll
+            for (int w = 0; w < W; ++w) M = fmaxf(M, red_m[gi][i][w]);
+            const float Mr = (M == neg_inf()) ? 0.f : M;
+            float tot = 0.f;
+#pragma unroll
+            for (int w = 0; w < W; ++w) {
+                const float m2 = red_m[gi][i][w];
+                tot += (m2 == neg_inf()) ? 0.f : red_l[gi][i][w] * ex2((m2 - Mr) * kLog2e);
+            }
+            const float inv = tot > 0.f ? __frcp_rn(tot) : 0.f;
+            fac[i] = (mx[i] == neg_inf()) ? 0.f : ex2((mx[i] - Mr) * kLog2e) * inv;
+        }
     }
 #pragma unroll
     for (int i = 0; i < RPG; ++i) {
-        sum[i] = group_sum<G>(sum[i]);
-        const float inv = sum[i] > 0.f ? __frcp_rn(sum[i]) : 0.f;
         if (!live[i]) continue;
         T *ys = reinterpret_cast<T *>(a.y) + (x0[i] - xoff[i]);
 #pragma unroll
@@ -139,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_warp_kernel(const FwdArgs a)
             if (j0 >= cols) continue;
             float o[VEC];
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) o[e] = s[i][k][e] * inv;
+            for (int e = 0; e < VEC; ++e) o[e] = s[i][k][e] * fac[i];
             if (ALIGNED || (j0 >= 0 && j0 + VEC <= cols)) {
                 st_stream(ys + vi * VEC, pack<T>(o));
             } else {
@@ -157,10 +207,11 @@ template <typename T, int G, int NV, int RPG, bool ALIGNED>
 __global__ void __launch_bounds__(kThreads, 2) bwd_warp_kernel(const BwdArgs a)
 {
     constexpr int VEC = Dt<T>::VEC;
-    constexpr int GPW = 32 / G;
-    const int lane = threadIdx.x & 31;
-    const int gl = lane & (G - 1);
-    const int64_t row0 = (((int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * GPW + lane / G) * RPG;
+    constexpr int GPC = kThreads / G;
+    constexpr int W = G > 32 ? G / 32 : 1;
+    const int gl = threadIdx.x % G;
+    const int gi = threadIdx.x / G;
+    const int64_t row0 = ((int64_t)blockIdx.x * GPC + gi) * RPG;
     const int64_t cols = a.cols;
 
     int64_t x0[RPG];
@@ -225,9 +276,27 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_warp_kernel(const BwdArgs a)
             }
         }
     }
+    if constexpr (G <= 32) {
+#pragma unroll
+        for (int i = 0; i < RPG; ++i) dot[i] = group_sum<G>(dot[i]);
+    } else {
+        __shared__ float red[GPC][RPG][W];
+        const int wg = gl >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+        for (int i = 0; i < RPG; ++i) {
+            const float d = group_sum<32>(dot[i]);
+            if (lane == 0) red[gi][i][wg] = d;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < RPG; ++i) {
+            dot[i] = 0.f;
+#pragma unroll
+            for (int w = 0; w < W; ++w) dot[i] += red[gi][i][w];
+        }
+    }
 #pragma unroll
     for (int i = 0; i < RPG; ++i) {
-        dot[i] = group_sum<G>(dot[i]);
         if (!live[i]) continue;
         T *dxs = reinterpret_cast<T *>(a.dx) + (x0[i] - xoff[i]);
 #pragma unroll
@@ -260,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_warp_kernel(const BwdArgs a)
 template <typename T, int G, int NV, int RPG, bool ALIGNED, bool BWD, typename Args>
 cudaError_t launch_one(const Args &a, cudaStream_t st)
 {
-    constexpr int rows_per_cta = (kThreads / 32) * (32 / G) * RPG;
+    constexpr int rows_per_cta = (kThreads / G) * RPG;
     const int64_t blocks = (a.rows + rows_per_cta - 1) / rows_per_cta;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg = {};
@@ -275,8 +344,8 @@ cudaError_t launch_one(const Args &a, cudaStream_t st)
 
 // (lanes per row, vectors per lane per row, rows per lane group), smallest
 // capacity first.  Capacity = G*NV vectors; each lane keeps RPG*NV vectors
-// per input stream in flight: 8 for fp32 rows, 4 for 16-bit rows (32 fp32
-// values either way), except the 16-bit forward's widest shapes (6-8).
+// per input stream in flight: up to 8 for fp32 rows and 4 for 16-bit rows
+// (32 fp32 values either way).
 template <typename T, bool ALIGNED, bool BWD, typename Args>
 cudaError_t launch_t(const Args &a, cudaStream_t st)
 {
@@ -287,11 +356,11 @@ cudaError_t launch_t(const Args &a, cudaStream_t st)
     if (need <= (G) * (NV)) return launch_one<T, G, NV, (ALIGNED || (RPG) == 1 ? (RPG) : (RPG) / 2), ALIGNED, BWD>(a, st);
     if constexpr (VEC == 4) {
         SMS_TRY(4, 1, 8) SMS_TRY(8, 1, 8) SMS_TRY(16, 1, 8) SMS_TRY(32, 1, 8) SMS_TRY(32, 2, 4) SMS_TRY(32, 3, 2)
-        SMS_TRY(32, 4, 2) SMS_TRY(32, 6, 1) SMS_TRY(32, 8, 1)
+        SMS_TRY(32, 4, 2) SMS_TRY(32, 6, 1) SMS_TRY(32, 8, 1) SMS_TRY(64, 8, 1) SMS_TRY(128, 8, 1)
+        SMS_TRY(256, 6, 1) SMS_TRY(256, 8, 1)
     } else {
         SMS_TRY(4, 1, 4) SMS_TRY(8, 1, 4) SMS_TRY(16, 1, 4) SMS_TRY(32, 1, 4) SMS_TRY(32, 2, 2) SMS_TRY(32, 3, 1)
-        SMS_TRY(32, 4, 1)
-        if constexpr (!BWD) { SMS_TRY(32, 6, 1) SMS_TRY(32, 8, 1) }
+        SMS_TRY(32, 4, 1) SMS_TRY(64, 4, 1) SMS_TRY(128, 4, 1) SMS_TRY(256, 3, 1) SMS_TRY(256, 4, 1)
     }
 #undef SMS_TRY
     return cudaErrorNotSupported;
@@ -318,7 +387,8 @@ bool warp_fits(int64_t cols, int dtype, bool aligned, bool bwd)
 {
     const int vec = vec_elems(dtype);
     const int64_t need = (cols + vec - 1) / vec + (aligned ? 0 : 1);
-    const int64_t cap = vec == 4 ? 32 * 8 : (bwd ? 32 * 4 : 32 * 8);
+    (void)bwd;
+    const int64_t cap = vec == 4 ? 256 * 8 : 256 * 4;  // widest shapes: 256 lanes x 8 (fp32) / 4 (16-bit) vectors
     return need <= cap;
 }
 

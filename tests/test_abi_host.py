@@ -116,7 +116,8 @@ def test_dispatcher_thresholds():
     for dt in (0, 1, 2):
         assert sms.sms_select_path(1000, 64, dt) == W
         assert sms.sms_select_path(1000, 1024, dt) == W
-        assert sms.sms_select_path(1000, 4096, dt) == C
+        assert sms.sms_select_path(1000, 4096, dt) == W
+        assert sms.sms_select_path(1000, 8192, dt) == W
         assert sms.sms_select_path(1000, 16384, dt) == C
         assert sms.sms_select_path(1000, 1 << 20, dt) == O
         assert sms.sms_select_path(1000, 1 << 20, dt, True) == O
