@@ -21,7 +21,7 @@ LIB = os.path.join(PKG, "libsms.so")
 SOURCES = ["sms_abi.cu", "sms_warp.cu", "sms_tile_fwd.cu", "sms_tile_bwd.cu", "sms_online.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
-              "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
+              "--expt-relaxed-constexpr", "-I", INCLUDE]
 
 
 def _nvcc() -> str:
@@ -31,29 +31,31 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libsms")
 
 
-def _inputs():
-    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+def _inputs(csrc=CSRC):
+    files = [os.path.join(csrc, f) for f in os.listdir(csrc)]
     files.append(os.path.join(INCLUDE, "sms.h"))
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib=LIB, csrc=CSRC) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
-    return all(os.path.getmtime(f) <= t for f in _inputs())
+    t = os.path.getmtime(lib)
+    return all(os.path.getmtime(f) <= t for f in _inputs(csrc))
 
 
-def build_library(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    if not force and up_to_date():
-        return LIB
+def build_library(force: bool = False, verbose: bool = False, extra_flags=None, csrc: str = CSRC, out: str = LIB,
+                  build_dir: str = BUILD) -> str:
+    """Compile the sources in ``csrc`` into the shared library ``out``."""
+    if not force and up_to_date(out, csrc):
+        return out
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
-    flags = NVCC_FLAGS + (list(extra_flags) if extra_flags else [])
+    os.makedirs(build_dir, exist_ok=True)
+    flags = NVCC_FLAGS + ["-I", csrc] + (list(extra_flags) if extra_flags else [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-        cmd = [nvcc] + ARCH + flags + ["-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
+        cmd = [nvcc] + ARCH + flags + ["-c", os.path.join(csrc, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stderr}")
@@ -63,13 +65,13 @@ def build_library(force: bool = False, verbose: bool = False, extra_flags=None) 
 
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + ".tmp"
+    tmp = out + ".tmp"
     cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcudart_static", "-lrt", "-ldl", "-lpthread"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
-        raise RuntimeError(f"link of libsms.so failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+        raise RuntimeError(f"link of {os.path.basename(out)} failed:\n{r.stderr}")
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":
