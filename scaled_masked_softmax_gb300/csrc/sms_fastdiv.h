@@ -25,7 +25,7 @@ struct FastDiv {
     uint32_t s1;   // min(l, 1)
     uint32_t s2;   // max(l - 1, 0)
 
-    FastDiv() : d(1), m(1), s1(0), s2(0) {}
+    SMS_HD FastDiv() : d(1), m(1), s1(0), s2(0) {}
     explicit FastDiv(uint32_t div)
     {
         d = div ? div : 1;

@@ -21,6 +21,31 @@ namespace {
 
 constexpr int kThreads = 256;  // 8 warps per CTA
 
+// Positions of the RPG consecutive rows row0 .. row0+RPG-1 of a lane group:
+// the first is split with the invariant-divisor division, the others follow
+// by stepping one row (q+1, wrapping into the next head and batch).  Rows at
+// or beyond `rows` get limit 0: they read and write nothing.
+template <int RPG>
+__device__ __forceinline__ void group_rows(int64_t row0, int64_t rows, int64_t cols, int64_t heads, bool causal,
+                                           bool need_pos, const FastDiv &dc, const FastDiv &dh, int64_t msb,
+                                           int64_t msh, int (&limit)[RPG], int64_t (&m0)[RPG])
+{
+    int64_t q = 0, h = 0, b = 0;
+    if (need_pos && row0 < rows) split_row(row0, cols, heads, dc, dh, q, h, b);
+#pragma unroll
+    for (int i = 0; i < RPG; ++i) {
+        if (i > 0 && need_pos) {
+            if (++q == cols) {
+                q = 0;
+                if (++h == heads) { h = 0; ++b; }
+            }
+        }
+        const bool live = row0 + i < rows;
+        limit[i] = live ? (causal ? (int)(q + 1) : (int)cols) : 0;
+        m0[i] = b * msb + h * msh + q * cols;
+    }
+}
+
 // One lane group (G lanes: part of a warp, a warp, or W = G/32 warps) handles
 // RPG consecutive rows at once: every raw 16-byte load of all RPG rows is
 // issued before any arithmetic, so each lane keeps RPG*NV vectors in flight.
@@ -37,33 +62,26 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_warp_kernel(const FwdArgs a)
     const int64_t row0 = ((int64_t)blockIdx.x * GPC + gi) * RPG;
     const int64_t cols = a.cols;
 
-    int64_t x0[RPG];
-    int xoff[RPG], limit[RPG];
-    const T *ms[RPG];
-    bool mvec[RPG], live[RPG];
+    int limit[RPG];
+    int64_t m0[RPG];
+    group_rows<RPG>(row0, a.rows, cols, a.heads, a.causal, a.causal || a.mask, a.dcols, a.dheads, a.msb, a.msh, limit,
+                    m0);
+    int xoff[RPG];
+    bool mvec[RPG];
     uint4 xr[RPG][NV], mr[RPG][NV];
-
 #pragma unroll
     for (int i = 0; i < RPG; ++i) {
-        live[i] = row0 + i < a.rows;
-        const int64_t r = live[i] ? row0 + i : a.rows - 1;  // dead rows still join the shuffles
-        int64_t q = 0, h = 0, b = 0;
-        if (a.causal || a.mask) split_row(r, cols, a.heads, a.dcols, a.dheads, q, h, b);
-        limit[i] = a.causal ? (int)(q + 1) : (int)cols;
-        x0[i] = r * cols;
-        xoff[i] = ALIGNED ? 0 : (int)(x0[i] & (VEC - 1));
-        ms[i] = nullptr;
-        mvec[i] = ALIGNED;
-        if (a.mask) {
-            const int64_t m0 = b * a.msb + h * a.msh + q * cols;
-            ms[i] = reinterpret_cast<const T *>(a.mask) + m0;
-            if (!ALIGNED) mvec[i] = ((m0 - xoff[i]) & (VEC - 1)) == 0 && m0 - xoff[i] + (int64_t)G * NV * VEC <= a.mask_total;
-        }
+        const int64_t x0 = (row0 + i) * cols;
+        xoff[i] = ALIGNED ? 0 : (int)(x0 & (VEC - 1));
+        mvec[i] = ALIGNED || (((m0[i] - xoff[i]) & (VEC - 1)) == 0 &&
+                              m0[i] - xoff[i] + (int64_t)G * NV * VEC <= a.mask_total);
     }
     // issue every full-vector load first
 #pragma unroll
     for (int i = 0; i < RPG; ++i) {
-        const T *xs = reinterpret_cast<const T *>(a.x) + (x0[i] - xoff[i]);
+        const int64_t xb = (row0 + i) * cols - xoff[i];  // aligned start of the row's vectors
+        const T *xs = reinterpret_cast<const T *>(a.x) + xb;
+        const T *ms = reinterpret_cast<const T *>(a.mask) + m0[i];
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const int vi = k * G + gl;
@@ -71,8 +89,8 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_warp_kernel(const FwdArgs a)
             xr[i][k] = make_uint4(0, 0, 0, 0);
             mr[i][k] = make_uint4(0, 0, 0, 0);
             if (j0 < limit[i]) {
-                if (ALIGNED || x0[i] - xoff[i] + (int64_t)(vi + 1) * VEC <= a.x_total) xr[i][k] = ld_stream(xs + vi * VEC);
-                if (ms[i] && mvec[i]) mr[i][k] = ld_keep(ms[i] + j0);
+                if (ALIGNED || xb + (int64_t)(vi + 1) * VEC <= a.x_total) xr[i][k] = ld_stream(xs + vi * VEC);
+                if (a.mask && mvec[i]) mr[i][k] = ld_keep(ms + j0);
             }
         }
     }
@@ -82,7 +100,9 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_warp_kernel(const FwdArgs a)
 #pragma unroll
     for (int i = 0; i < RPG; ++i) {
         mx[i] = neg_inf();
-        const T *xs = reinterpret_cast<const T *>(a.x) + (x0[i] - xoff[i]);
+        const int64_t xb = (row0 + i) * cols - xoff[i];
+        const T *xs = reinterpret_cast<const T *>(a.x) + xb;
+        const T *ms = reinterpret_cast<const T *>(a.mask) + m0[i];
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const int vi = k * G + gl;
@@ -91,41 +111,50 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_warp_kernel(const FwdArgs a)
             unpack<T>(xr[i][k], xv);
             unpack<T>(mr[i][k], mv);
             if (!ALIGNED && j0 < limit[i]) {
-                const int64_t g = x0[i] - xoff[i] + (int64_t)vi * VEC;
-                if (g + VEC > a.x_total) {  // last partial vector of the tensor
+                if (xb + (int64_t)(vi + 1) * VEC > a.x_total) {  // last partial vector of the tensor
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) xv[e] = g + e < a.x_total ? to_f32<T>(xs[vi * VEC + e]) : 0.f;
+                    for (int e = 0; e < VEC; ++e) xv[e] = xb + vi * VEC + e < a.x_total ? to_f32<T>(xs[vi * VEC + e]) : 0.f;
                 }
-                if (ms[i] && !mvec[i]) {  // mask row not aligned like the x row: element loads
+                if (a.mask && !mvec[i]) {  // mask row not aligned like the x row: element loads
 #pragma unroll
                     for (int e = 0; e < VEC; ++e) {
                         const int j = j0 + e;
-                        mv[e] = (j >= 0 && j < limit[i]) ? to_f32<T>(ms[i][j]) : 0.f;
+                        mv[e] = (j >= 0 && j < limit[i]) ? to_f32<T>(ms[j]) : 0.f;
                     }
                 }
             }
+            if (j0 >= 0 && j0 + VEC <= limit[i]) {  // interior vector: every element is read
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const int j = j0 + e;
-                const bool valid = j >= 0 && j < limit[i];
-                s[i][k][e] = valid ? fmaf(xv[e], a.scale, mv[e]) : neg_inf();
-                mx[i] = fmaxf(mx[i], s[i][k][e]);
+                for (int e = 0; e < VEC; ++e) {
+                    s[i][k][e] = fmaf(xv[e], a.scale, mv[e]);
+                    mx[i] = fmaxf(mx[i], s[i][k][e]);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const int j = j0 + e;
+                    s[i][k][e] = (j >= 0 && j < limit[i]) ? fmaf(xv[e], a.scale, mv[e]) : neg_inf();
+                    mx[i] = fmaxf(mx[i], s[i][k][e]);
+                }
             }
         }
     }
+
+    // exp(s - m) = 2^(s*log2e - m*log2e): one FMA per element; the rounding
+    // of m*log2e is common to the whole row and cancels in the normalisation
     float fac[RPG];  // y = e * fac, e the exponentials kept in s
     if constexpr (G <= 32) {
         float sum[RPG];
 #pragma unroll
         for (int i = 0; i < RPG; ++i) {
             mx[i] = group_max<G>(mx[i]);
-            const float mref = (mx[i] == neg_inf()) ? 0.f : mx[i];  // fully masked row: every term becomes 0
+            const float c = (mx[i] == neg_inf()) ? 0.f : -mx[i] * kLog2e;  // fully masked row: every term 0
             sum[i] = 0.f;
 #pragma unroll
             for (int k = 0; k < NV; ++k)
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) {
-                    const float t = ex2((s[i][k][e] - mref) * kLog2e);
+                    const float t = ex2(fmaf(s[i][k][e], kLog2e, c));
                     s[i][k][e] = t;
                     sum[i] += t;
                 }
@@ -140,22 +169,21 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_warp_kernel(const FwdArgs a)
         // pairs, the group's warps merge theirs through shared memory
         __shared__ float red_m[GPC][RPG][W], red_l[GPC][RPG][W];
         const int wg = gl >> 5, lane = threadIdx.x & 31;
-        float lt[RPG];
 #pragma unroll
         for (int i = 0; i < RPG; ++i) {
-            const float mtr = (mx[i] == neg_inf()) ? 0.f : mx[i];
-            lt[i] = 0.f;
+            const float c = (mx[i] == neg_inf()) ? 0.f : -mx[i] * kLog2e;
+            float lt = 0.f;
 #pragma unroll
             for (int k = 0; k < NV; ++k)
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) {
-                    const float t = ex2((s[i][k][e] - mtr) * kLog2e);
+                    const float t = ex2(fmaf(s[i][k][e], kLog2e, c));
                     s[i][k][e] = t;
-                    lt[i] += t;
+                    lt += t;
                 }
             const float mw = group_max<32>(mx[i]);
             const float mwr = (mw == neg_inf()) ? 0.f : mw;
-            const float lw = group_sum<32>(mx[i] == neg_inf() ? 0.f : lt[i] * ex2((mx[i] - mwr) * kLog2e));
+            const float lw = group_sum<32>(mx[i] == neg_inf() ? 0.f : lt * ex2((mx[i] - mwr) * kLog2e));
             if (lane == 0) {
                 red_m[gi][i][wg] = mw;
                 red_l[gi][i][wg] = lw;
@@ -180,8 +208,8 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_warp_kernel(const FwdArgs a)
     }
 #pragma unroll
     for (int i = 0; i < RPG; ++i) {
-        if (!live[i]) continue;
-        T *ys = reinterpret_cast<T *>(a.y) + (x0[i] - xoff[i]);
+        if (row0 + i >= a.rows) continue;
+        T *ys = reinterpret_cast<T *>(a.y) + ((row0 + i) * cols - xoff[i]);
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const int vi = k * G + gl;
@@ -214,29 +242,25 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_warp_kernel(const BwdArgs a)
     const int64_t row0 = ((int64_t)blockIdx.x * GPC + gi) * RPG;
     const int64_t cols = a.cols;
 
-    int64_t x0[RPG];
-    int xoff[RPG], limit[RPG];
-    bool live[RPG];
+    int limit[RPG];
+    int64_t unused_m0[RPG];
+    group_rows<RPG>(row0, a.rows, cols, 1, a.causal, a.causal, a.dcols, FastDiv(), 0, 0, limit, unused_m0);
+    int xoff[RPG];
     uint4 yr[RPG][NV], gr[RPG][NV];
 #pragma unroll
-    for (int i = 0; i < RPG; ++i) {
-        live[i] = row0 + i < a.rows;
-        const int64_t r = live[i] ? row0 + i : a.rows - 1;
-        limit[i] = a.causal ? (int)(row_q(r, cols, a.dcols) + 1) : (int)cols;
-        x0[i] = r * cols;
-        xoff[i] = ALIGNED ? 0 : (int)(x0[i] & (VEC - 1));
-    }
+    for (int i = 0; i < RPG; ++i) xoff[i] = ALIGNED ? 0 : (int)(((row0 + i) * cols) & (VEC - 1));
 #pragma unroll
     for (int i = 0; i < RPG; ++i) {
-        const T *ys = reinterpret_cast<const T *>(a.y) + (x0[i] - xoff[i]);
-        const T *gs = reinterpret_cast<const T *>(a.dy) + (x0[i] - xoff[i]);
+        const int64_t xb = (row0 + i) * cols - xoff[i];
+        const T *ys = reinterpret_cast<const T *>(a.y) + xb;
+        const T *gs = reinterpret_cast<const T *>(a.dy) + xb;
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const int vi = k * G + gl;
             const int j0 = vi * VEC - xoff[i];
             yr[i][k] = make_uint4(0, 0, 0, 0);
             gr[i][k] = make_uint4(0, 0, 0, 0);
-            if (j0 < limit[i] && (ALIGNED || x0[i] - xoff[i] + (int64_t)(vi + 1) * VEC <= a.total)) {
+            if (j0 < limit[i] && (ALIGNED || xb + (int64_t)(vi + 1) * VEC <= a.total)) {
                 yr[i][k] = ld_stream(ys + vi * VEC);
                 gr[i][k] = ld_stream(gs + vi * VEC);
             }
@@ -246,33 +270,36 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_warp_kernel(const BwdArgs a)
 #pragma unroll
     for (int i = 0; i < RPG; ++i) {
         dot[i] = 0.f;
-        const T *ys = reinterpret_cast<const T *>(a.y) + (x0[i] - xoff[i]);
-        const T *gs = reinterpret_cast<const T *>(a.dy) + (x0[i] - xoff[i]);
+        const int64_t xb = (row0 + i) * cols - xoff[i];
+        const T *ys = reinterpret_cast<const T *>(a.y) + xb;
+        const T *gs = reinterpret_cast<const T *>(a.dy) + xb;
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const int vi = k * G + gl;
             const int j0 = vi * VEC - xoff[i];
-            if (!ALIGNED && j0 < limit[i]) {
-                const int64_t g = x0[i] - xoff[i] + (int64_t)vi * VEC;
-                if (g + VEC > a.total) {  // last partial vector of the tensor
-                    float tv[VEC], tg[VEC];
+            if (!ALIGNED && j0 < limit[i] && xb + (int64_t)(vi + 1) * VEC > a.total) {  // last partial vector
+                float tv[VEC], tg[VEC];
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) {
-                        const bool in = g + e < a.total;
-                        tv[e] = in ? to_f32<T>(ys[vi * VEC + e]) : 0.f;
-                        tg[e] = in ? to_f32<T>(gs[vi * VEC + e]) : 0.f;
-                    }
-                    yr[i][k] = pack<T>(tv);
-                    gr[i][k] = pack<T>(tg);
+                for (int e = 0; e < VEC; ++e) {
+                    const bool in = xb + vi * VEC + e < a.total;
+                    tv[e] = in ? to_f32<T>(ys[vi * VEC + e]) : 0.f;
+                    tg[e] = in ? to_f32<T>(gs[vi * VEC + e]) : 0.f;
                 }
+                yr[i][k] = pack<T>(tv);
+                gr[i][k] = pack<T>(tg);
             }
             float yv[VEC], gv[VEC];
             unpack<T>(yr[i][k], yv);
             unpack<T>(gr[i][k], gv);
+            if (j0 >= 0 && j0 + VEC <= limit[i]) {  // interior vector
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const int j = j0 + e;
-                if (j >= 0 && j < limit[i]) dot[i] = fmaf(yv[e], gv[e], dot[i]);
+                for (int e = 0; e < VEC; ++e) dot[i] = fmaf(yv[e], gv[e], dot[i]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const int j = j0 + e;
+                    if (j >= 0 && j < limit[i]) dot[i] = fmaf(yv[e], gv[e], dot[i]);
+                }
             }
         }
     }
@@ -297,8 +324,8 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_warp_kernel(const BwdArgs a)
     }
 #pragma unroll
     for (int i = 0; i < RPG; ++i) {
-        if (!live[i]) continue;
-        T *dxs = reinterpret_cast<T *>(a.dx) + (x0[i] - xoff[i]);
+        if (row0 + i >= a.rows) continue;
+        T *dxs = reinterpret_cast<T *>(a.dx) + ((row0 + i) * cols - xoff[i]);
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const int vi = k * G + gl;
@@ -343,9 +370,11 @@ cudaError_t launch_one(const Args &a, cudaStream_t st)
 }
 
 // (lanes per row, vectors per lane per row, rows per lane group), smallest
-// capacity first.  Capacity = G*NV vectors; each lane keeps RPG*NV vectors
-// per input stream in flight: up to 8 for fp32 rows and 4 for 16-bit rows
-// (32 fp32 values either way).
+// capacity first.  Capacity = G*NV vectors.  Each lane keeps RPG*NV vectors
+// per input stream in flight: 4 for every backward and 16-bit forward shape
+// (both streams come from HBM there), up to 8 for the fp32 forward (its mask
+// stream is served by L2).  More vectors per lane stop fitting the 128
+// registers that keep two CTAs per SM, and loads then serialise.
 template <typename T, bool ALIGNED, bool BWD, typename Args>
 cudaError_t launch_t(const Args &a, cudaStream_t st)
 {
@@ -354,13 +383,12 @@ cudaError_t launch_t(const Args &a, cudaStream_t st)
     // rows that may start mid-vector carry more bookkeeping: half the rows per group
 #define SMS_TRY(G, NV, RPG) \
     if (need <= (G) * (NV)) return launch_one<T, G, NV, (ALIGNED || (RPG) == 1 ? (RPG) : (RPG) / 2), ALIGNED, BWD>(a, st);
-    if constexpr (VEC == 4) {
-        SMS_TRY(4, 1, 8) SMS_TRY(8, 1, 8) SMS_TRY(16, 1, 8) SMS_TRY(32, 1, 8) SMS_TRY(32, 2, 4) SMS_TRY(32, 3, 2)
-        SMS_TRY(32, 4, 2) SMS_TRY(32, 6, 1) SMS_TRY(32, 8, 1) SMS_TRY(64, 8, 1) SMS_TRY(128, 8, 1)
-        SMS_TRY(256, 6, 1) SMS_TRY(256, 8, 1)
+    if constexpr (VEC == 4 && !BWD) {
+        SMS_TRY(4, 1, 8) SMS_TRY(8, 1, 8) SMS_TRY(16, 1, 8) SMS_TRY(32, 1, 8) SMS_TRY(32, 2, 4) SMS_TRY(32, 4, 2)
+        SMS_TRY(32, 8, 1) SMS_TRY(128, 4, 1) SMS_TRY(256, 4, 1) SMS_TRY(256, 6, 1) SMS_TRY(256, 8, 1)
     } else {
-        SMS_TRY(4, 1, 4) SMS_TRY(8, 1, 4) SMS_TRY(16, 1, 4) SMS_TRY(32, 1, 4) SMS_TRY(32, 2, 2) SMS_TRY(32, 3, 1)
-        SMS_TRY(32, 4, 1) SMS_TRY(64, 4, 1) SMS_TRY(128, 4, 1) SMS_TRY(256, 3, 1) SMS_TRY(256, 4, 1)
+        SMS_TRY(4, 1, 4) SMS_TRY(8, 1, 4) SMS_TRY(16, 1, 4) SMS_TRY(32, 1, 4) SMS_TRY(32, 2, 2) SMS_TRY(32, 4, 1)
+        SMS_TRY(64, 4, 1) SMS_TRY(128, 4, 1) SMS_TRY(256, 4, 1)
     }
 #undef SMS_TRY
     return cudaErrorNotSupported;
@@ -387,8 +415,7 @@ bool warp_fits(int64_t cols, int dtype, bool aligned, bool bwd)
 {
     const int vec = vec_elems(dtype);
     const int64_t need = (cols + vec - 1) / vec + (aligned ? 0 : 1);
-    (void)bwd;
-    const int64_t cap = vec == 4 ? 256 * 8 : 256 * 4;  // widest shapes: 256 lanes x 8 (fp32) / 4 (16-bit) vectors
+    const int64_t cap = (vec == 4 && !bwd) ? 256 * 8 : 256 * 4;  // widest shapes (see launch_t)
     return need <= cap;
 }
 
