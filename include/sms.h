@@ -60,6 +60,14 @@
 
 #include <stdint.h>
 
+/* Only the entry points below are exported; everything else in the library
+ * is hidden, so two copies of libsms in one process share no state. */
+#if defined(__GNUC__)
+#define SMS_API __attribute__((visibility("default")))
+#else
+#define SMS_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -94,7 +102,7 @@ typedef enum {
  *   stream         cudaStream_t
  * rows == 0 (with cols >= 1) is a valid no-op; the pointers may then be NULL.
  */
-int sms_forward(const void *x, const void *mask, int64_t mask_numel, int64_t mask_stride_b,
+SMS_API int sms_forward(const void *x, const void *mask, int64_t mask_numel, int64_t mask_stride_b,
                 int64_t mask_stride_h, int64_t heads, void *y, int64_t rows, int64_t cols, float scale,
                 int is_causal, int dtype, void *stream);
 
@@ -109,33 +117,33 @@ int sms_forward(const void *x, const void *mask, int64_t mask_numel, int64_t mas
  *                  identical with and without the hint.
  * rows == 0 (with cols >= 1) is a valid no-op; the pointers may then be NULL.
  */
-int sms_backward(const void *y, const void *dy, void *dx, int64_t rows, int64_t cols, float scale,
+SMS_API int sms_backward(const void *y, const void *dy, void *dx, int64_t rows, int64_t cols, float scale,
                  int is_causal_hint, int dtype, void *stream);
 
 /* Static description of a status code. */
-const char *sms_status_string(int status);
+SMS_API const char *sms_status_string(int status);
 
 /* One-line description of the last failure on this host thread ("" if none). */
-const char *sms_last_error(void);
+SMS_API const char *sms_last_error(void);
 
 /*
  * Force every later call in this process onto one kernel family (testing and
  * benchmarking); SMS_PATH_AUTO restores the dispatcher.  Returns the previous
  * setting, or -1 for an unknown path.  Process-wide, not thread-safe.
  */
-int sms_set_forced_path(int path);
+SMS_API int sms_set_forced_path(int path);
 
 /* The family the dispatcher would pick for this forward (or backward) shape. */
-int sms_select_path(int64_t rows, int64_t cols, int dtype, int is_backward);
+SMS_API int sms_select_path(int64_t rows, int64_t cols, int dtype, int is_backward);
 
 /* The family taken by the last successful call on this host thread. */
-int sms_last_path(void);
+SMS_API int sms_last_path(void);
 
 /*
  * Number of kernel launches made by successful calls since load, process-wide
  * (each sms_forward / sms_backward enqueues exactly one kernel when rows > 0).
  */
-int64_t sms_launch_count(void);
+SMS_API int64_t sms_launch_count(void);
 
 /*
  * Reads (and clears) the device-side error word of the current device after
@@ -143,10 +151,10 @@ int64_t sms_launch_count(void);
  * for its own bulk copies (1 = consumer wait, 2 = producer wait); its output
  * is then incomplete.  Returns -1 if the read itself failed.
  */
-int sms_device_error(void *stream);
+SMS_API int sms_device_error(void *stream);
 
 /* ABI version: 100 * major + minor. */
-int sms_version(void);
+SMS_API int sms_version(void);
 
 #ifdef __cplusplus
 }

@@ -21,7 +21,7 @@ LIB = os.path.join(PKG, "libsms.so")
 SOURCES = ["sms_abi.cu", "sms_warp.cu", "sms_tile_fwd.cu", "sms_tile_bwd.cu", "sms_online.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
-              "--expt-relaxed-constexpr", "-I", INCLUDE]
+              "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr", "-I", INCLUDE]
 
 
 def _nvcc() -> str:

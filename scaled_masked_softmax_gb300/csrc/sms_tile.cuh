@@ -30,13 +30,14 @@
 // the producer waits (bounded) for every copy it issued before exiting.
 #pragma once
 
-#include <mutex>
+#include <atomic>
 
 #include "sms_common.cuh"
 #include "sms_internal.h"
 
 namespace sms {
 namespace tile {
+namespace {  // internal linkage: no launch state is shared with another copy of the library
 
 constexpr int kMaxK = 16;                  // ring stages per group (upper bound)
 constexpr int kSmemBudget = 200 * 1024;    // one CTA per SM
@@ -459,15 +460,15 @@ cudaError_t launch_tile(const FwdArgs &fa, const BwdArgs &ba, cudaStream_t st)
 {
     constexpr int smem = smem_bytes<WG, R, SLOTS, CH>();
     auto kern = tile_kernel<T, WG, R, SLOTS, CH, BWD>;
-    static std::once_flag once[64];
-    static cudaError_t attr_status[64];
+    static std::atomic<int> attr_done[64];  // per device: the shared-memory limit has been raised
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    std::call_once(once[dev & 63], [&] {
-        attr_status[dev & 63] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    });
-    if (attr_status[dev & 63] != cudaSuccess) return attr_status[dev & 63];
+    if (!attr_done[dev & 63].load(std::memory_order_acquire)) {  // idempotent: a race only repeats the call
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr_done[dev & 63].store(1, std::memory_order_release);
+    }
     const int64_t rows = BWD ? ba.rows : fa.rows;
     int64_t grid = (int64_t)sm_count();
     if (grid > rows) grid = rows;
@@ -528,5 +529,6 @@ cudaError_t dispatch(const FwdArgs &fa, const BwdArgs &ba, int64_t cols, int dty
     }
 }
 
+}  // namespace
 }  // namespace tile
 }  // namespace sms

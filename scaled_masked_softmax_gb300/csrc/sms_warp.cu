@@ -385,10 +385,12 @@ cudaError_t launch_t(const Args &a, cudaStream_t st)
     if (need <= (G) * (NV)) return launch_one<T, G, NV, (ALIGNED || (RPG) == 1 ? (RPG) : (RPG) / 2), ALIGNED, BWD>(a, st);
     if constexpr (VEC == 4 && !BWD) {
         SMS_TRY(4, 1, 8) SMS_TRY(8, 1, 8) SMS_TRY(16, 1, 8) SMS_TRY(32, 1, 8) SMS_TRY(32, 2, 4) SMS_TRY(32, 4, 2)
-        SMS_TRY(32, 8, 1) SMS_TRY(128, 4, 1) SMS_TRY(256, 4, 1) SMS_TRY(256, 6, 1) SMS_TRY(256, 8, 1)
+        SMS_TRY(32, 8, 1) SMS_TRY(128, 4, 1) SMS_TRY(128, 5, 1) SMS_TRY(256, 4, 1) SMS_TRY(256, 5, 1)
+        SMS_TRY(256, 6, 1) SMS_TRY(256, 8, 1)
     } else {
         SMS_TRY(4, 1, 4) SMS_TRY(8, 1, 4) SMS_TRY(16, 1, 4) SMS_TRY(32, 1, 4) SMS_TRY(32, 2, 2) SMS_TRY(32, 4, 1)
-        SMS_TRY(64, 4, 1) SMS_TRY(128, 4, 1) SMS_TRY(256, 4, 1)
+        SMS_TRY(64, 4, 1) SMS_TRY(64, 5, 1) SMS_TRY(128, 4, 1) SMS_TRY(128, 5, 1) SMS_TRY(256, 4, 1)
+        SMS_TRY(256, 5, 1)
     }
 #undef SMS_TRY
     return cudaErrorNotSupported;
@@ -415,7 +417,7 @@ bool warp_fits(int64_t cols, int dtype, bool aligned, bool bwd)
 {
     const int vec = vec_elems(dtype);
     const int64_t need = (cols + vec - 1) / vec + (aligned ? 0 : 1);
-    const int64_t cap = (vec == 4 && !bwd) ? 256 * 8 : 256 * 4;  // widest shapes (see launch_t)
+    const int64_t cap = (vec == 4 && !bwd) ? 256 * 8 : 256 * 5;  // widest shapes (see launch_t)
     return need <= cap;
 }
 
