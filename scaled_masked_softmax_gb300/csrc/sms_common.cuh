@@ -87,6 +87,39 @@ template <> __device__ __forceinline__ uint4 pack<__nv_bfloat16>(const float *f)
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Elements S .. S+VEC-1 of the 2*VEC elements held by two consecutive 16-byte
+// vectors (lo, hi): realigns a row that starts mid-vector relative to another.
+template <int VEC, int S> __device__ __forceinline__ uint4 window_fixed(const uint4 &lo, const uint4 &hi)
+{
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    uint32_t o[4];
+    if constexpr (VEC == 4) {  // 32-bit elements: a shift of S words
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = w[(i + S) & 7];
+    } else {  // 16-bit elements: S/2 words, then half a word when S is odd
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t a = w[(i + S / 2) & 7], b = w[(i + S / 2 + 1) & 7];
+            o[i] = (S & 1) ? __funnelshift_r(a, b, 16) : a;
+        }
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+template <int VEC> __device__ __forceinline__ uint4 window(const uint4 &lo, const uint4 &hi, int s)
+{
+    switch (s) {
+    case 0: return lo;
+    case 1: return window_fixed<VEC, 1>(lo, hi);
+    case 2: return window_fixed<VEC, 2>(lo, hi);
+    case 3: return window_fixed<VEC, 3>(lo, hi);
+    case 4: return window_fixed<VEC, 4 % VEC>(lo, hi);
+    case 5: return window_fixed<VEC, 5 % VEC>(lo, hi);
+    case 6: return window_fixed<VEC, 6 % VEC>(lo, hi);
+    default: return window_fixed<VEC, 7 % VEC>(lo, hi);
+    }
+}
+
 // ------------------------------------------------------ global memory I/O ---
 // Scores and gradients are read exactly once: stream them past L1 and mark
 // them first to leave L2.  The broadcast mask is re-read by every head of a

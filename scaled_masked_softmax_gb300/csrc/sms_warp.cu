@@ -66,31 +66,46 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_warp_kernel(const FwdArgs a)
     int64_t m0[RPG];
     group_rows<RPG>(row0, a.rows, cols, a.heads, a.causal, a.causal || a.mask, a.dcols, a.dheads, a.msb, a.msh, limit,
                     m0);
-    int xoff[RPG];
-    bool mvec[RPG];
+    // The mask row of row i starts D = m0 - xoff elements into the x-aligned
+    // vector grid: its elements for x vector vi sit at A + vi*VEC + sh ..,
+    // A = D - sh aligned, sh = D mod VEC.  sh == 0: one 16-byte load per
+    // vector; otherwise two neighbouring aligned loads and a register shift.
+    int xoff[RPG], msh[RPG];
+    int64_t mA[RPG];
     uint4 xr[RPG][NV], mr[RPG][NV];
+    uint4 mr2[ALIGNED ? 1 : RPG][ALIGNED ? 1 : NV];
 #pragma unroll
     for (int i = 0; i < RPG; ++i) {
         const int64_t x0 = (row0 + i) * cols;
         xoff[i] = ALIGNED ? 0 : (int)(x0 & (VEC - 1));
-        mvec[i] = ALIGNED || (((m0[i] - xoff[i]) & (VEC - 1)) == 0 &&
-                              m0[i] - xoff[i] + (int64_t)G * NV * VEC <= a.mask_total);
+        const int64_t D = m0[i] - xoff[i];
+        msh[i] = ALIGNED ? 0 : (int)(D & (VEC - 1));
+        mA[i] = D - msh[i];
     }
     // issue every full-vector load first
 #pragma unroll
     for (int i = 0; i < RPG; ++i) {
         const int64_t xb = (row0 + i) * cols - xoff[i];  // aligned start of the row's vectors
         const T *xs = reinterpret_cast<const T *>(a.x) + xb;
-        const T *ms = reinterpret_cast<const T *>(a.mask) + m0[i];
+        const T *mk = reinterpret_cast<const T *>(a.mask);
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const int vi = k * G + gl;
             const int j0 = vi * VEC - xoff[i];
             xr[i][k] = make_uint4(0, 0, 0, 0);
             mr[i][k] = make_uint4(0, 0, 0, 0);
+            if constexpr (!ALIGNED) mr2[i][k] = make_uint4(0, 0, 0, 0);
             if (j0 < limit[i]) {
                 if (ALIGNED || xb + (int64_t)(vi + 1) * VEC <= a.x_total) xr[i][k] = ld_stream(xs + vi * VEC);
-                if (a.mask && mvec[i]) mr[i][k] = ld_keep(ms + j0);
+                if (a.mask) {
+                    const int64_t mb = mA[i] + (int64_t)vi * VEC;  // first aligned mask vector
+                    if (ALIGNED) {
+                        mr[i][k] = ld_keep(mk + mb);
+                    } else if (mb >= 0 && mb + (msh[i] ? 2 : 1) * VEC <= a.mask_total) {
+                        mr[i][k] = ld_keep(mk + mb);
+                        if (msh[i]) mr2[i][k] = ld_keep(mk + mb + VEC);
+                    }
+                }
             }
         }
     }
@@ -109,17 +124,28 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_warp_kernel(const FwdArgs a)
             const int j0 = vi * VEC - xoff[i];
             float xv[VEC], mv[VEC];
             unpack<T>(xr[i][k], xv);
-            unpack<T>(mr[i][k], mv);
-            if (!ALIGNED && j0 < limit[i]) {
-                if (xb + (int64_t)(vi + 1) * VEC > a.x_total) {  // last partial vector of the tensor
+            if constexpr (ALIGNED) {
+                unpack<T>(mr[i][k], mv);
+            } else {
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) xv[e] = xb + vi * VEC + e < a.x_total ? to_f32<T>(xs[vi * VEC + e]) : 0.f;
-                }
-                if (a.mask && !mvec[i]) {  // mask row not aligned like the x row: element loads
+                for (int e = 0; e < VEC; ++e) mv[e] = 0.f;
+                if (j0 < limit[i]) {
+                    if (xb + (int64_t)(vi + 1) * VEC > a.x_total) {  // last partial vector of the tensor
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) {
-                        const int j = j0 + e;
-                        mv[e] = (j >= 0 && j < limit[i]) ? to_f32<T>(ms[j]) : 0.f;
+                        for (int e = 0; e < VEC; ++e)
+                            xv[e] = xb + vi * VEC + e < a.x_total ? to_f32<T>(xs[vi * VEC + e]) : 0.f;
+                    }
+                    if (a.mask) {
+                        const int64_t mb = mA[i] + (int64_t)vi * VEC;
+                        if (mb >= 0 && mb + (msh[i] ? 2 : 1) * VEC <= a.mask_total) {
+                            unpack<T>(window<VEC>(mr[i][k], mr2[i][k], msh[i]), mv);
+                        } else {  // mask vectors at the ends of the mask buffer: element loads
+#pragma unroll
+                            for (int e = 0; e < VEC; ++e) {
+                                const int j = j0 + e;
+                                mv[e] = (j >= 0 && j < limit[i]) ? to_f32<T>(ms[j]) : 0.f;
+                            }
+                        }
                     }
                 }
             }
@@ -371,10 +397,11 @@ cudaError_t launch_one(const Args &a, cudaStream_t st)
 
 // (lanes per row, vectors per lane per row, rows per lane group), smallest
 // capacity first.  Capacity = G*NV vectors.  Each lane keeps RPG*NV vectors
-// per input stream in flight: 4 for every backward and 16-bit forward shape
-// (both streams come from HBM there), up to 8 for the fp32 forward (its mask
-// stream is served by L2).  More vectors per lane stop fitting the 128
-// registers that keep two CTAs per SM, and loads then serialise.
+// per input stream in flight: 4 (5 for rows just past a power of two) for
+// every backward and 16-bit forward shape, up to 8 for the fp32 forward (its
+// mask stream is served by L2).  More vectors per lane stop fitting the 128
+// registers that keep two CTAs per SM, and loads then serialise.  Short rows
+// use few lanes with several vectors each: fewer shuffle rounds per row.
 template <typename T, bool ALIGNED, bool BWD, typename Args>
 cudaError_t launch_t(const Args &a, cudaStream_t st)
 {
@@ -384,11 +411,11 @@ cudaError_t launch_t(const Args &a, cudaStream_t st)
 #define SMS_TRY(G, NV, RPG) \
     if (need <= (G) * (NV)) return launch_one<T, G, NV, (ALIGNED || (RPG) == 1 ? (RPG) : (RPG) / 2), ALIGNED, BWD>(a, st);
     if constexpr (VEC == 4 && !BWD) {
-        SMS_TRY(4, 1, 8) SMS_TRY(8, 1, 8) SMS_TRY(16, 1, 8) SMS_TRY(32, 1, 8) SMS_TRY(32, 2, 4) SMS_TRY(32, 4, 2)
+        SMS_TRY(4, 1, 8) SMS_TRY(4, 2, 4) SMS_TRY(8, 2, 4) SMS_TRY(8, 4, 2) SMS_TRY(16, 4, 2) SMS_TRY(32, 4, 2)
         SMS_TRY(32, 8, 1) SMS_TRY(128, 4, 1) SMS_TRY(128, 5, 1) SMS_TRY(256, 4, 1) SMS_TRY(256, 5, 1)
         SMS_TRY(256, 6, 1) SMS_TRY(256, 8, 1)
     } else {
-        SMS_TRY(4, 1, 4) SMS_TRY(8, 1, 4) SMS_TRY(16, 1, 4) SMS_TRY(32, 1, 4) SMS_TRY(32, 2, 2) SMS_TRY(32, 4, 1)
+        SMS_TRY(4, 1, 4) SMS_TRY(4, 2, 2) SMS_TRY(4, 4, 1) SMS_TRY(8, 4, 1) SMS_TRY(16, 4, 1) SMS_TRY(32, 4, 1)
         SMS_TRY(64, 4, 1) SMS_TRY(64, 5, 1) SMS_TRY(128, 4, 1) SMS_TRY(128, 5, 1) SMS_TRY(256, 4, 1)
         SMS_TRY(256, 5, 1)
     }
