@@ -99,9 +99,14 @@ def test_backward_widths(S, dt, path):
             raise
     torch.cuda.synchronize()
     assert sms.sms_device_error(torch.cuda.current_stream().cuda_stream) == 0
-    # the causal hint only skips reads of positions where y == 0: identical bits
-    assert torch.equal(dx.view(torch.uint8), dx_hint.view(torch.uint8))
+    # the causal hint only skips reads of positions where y == 0: both results
+    # meet the bound, and every position with y == 0 is +0 in both
     H.check_backward(H.to_np64(dx), y.cpu(), inp["dy"].cpu(), w.scale, DTYPES[dt], f"{path} bwd S={S} {dt}")
+    H.check_backward(H.to_np64(dx_hint), y.cpu(), inp["dy"].cpu(), w.scale, DTYPES[dt], f"{path} bwd+hint S={S} {dt}")
+    zero = y == 0
+    assert torch.equal(dx[zero], torch.zeros_like(dx[zero]))
+    assert torch.equal(dx_hint[zero], torch.zeros_like(dx_hint[zero]))
+    assert not torch.signbit(dx_hint[zero]).any() and not torch.signbit(dx[zero]).any()
 
 
 @pytest.mark.parametrize("name", ["tiny_causal_f32", "keypad_f32_s1024", "causal_spike_f16_s2048",
