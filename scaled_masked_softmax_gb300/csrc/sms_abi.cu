@@ -22,6 +22,7 @@ namespace {
 thread_local char t_err[256] = "";
 thread_local int t_last_path = SMS_PATH_AUTO;
 std::atomic<int> g_forced{SMS_PATH_AUTO};
+std::atomic<int> g_grid_limit{0};
 std::atomic<int64_t> g_launches{0};
 
 constexpr int kMaxDevices = 64;
@@ -120,6 +121,15 @@ int sm_count()
     return n;
 }
 
+int64_t persistent_grid(int per_sm, int64_t useful)
+{
+    int64_t g = (int64_t)sm_count() * (per_sm > 0 ? per_sm : 1);
+    const int lim = g_grid_limit.load();
+    if (lim > 0 && g > lim) g = lim;
+    if (g > useful) g = useful;
+    return g > 0 ? g : 1;
+}
+
 }  // namespace sms
 
 using namespace sms;
@@ -143,11 +153,17 @@ const char *sms_last_error(void) { return t_err; }
 
 int sms_set_forced_path(int path)
 {
-    if (path < SMS_PATH_AUTO || path > SMS_PATH_ONLINE) return -1;
+    if (path < SMS_PATH_AUTO || path > SMS_PATH_PIPE) return -1;
     return g_forced.exchange(path);
 }
 
 int sms_last_path(void) { return t_last_path; }
+
+int sms_set_grid_limit(int ctas)
+{
+    if (ctas < 0) return -1;
+    return g_grid_limit.exchange(ctas);
+}
 
 int64_t sms_launch_count(void) { return g_launches.load(); }
 
@@ -235,6 +251,10 @@ int sms_forward(const void *x, const void *mask, int64_t mask_numel, int64_t mas
         if (!warp_fits(cols, dtype, aligned, false)) return fail(SMS_ERR_UNSUPPORTED, "sms_forward: row too wide for the warp path");
         e = launch_fwd_warp(a, dtype, aligned, st);
         break;
+    case SMS_PATH_PIPE:
+        if (!pipe_fits(cols, dtype, aligned)) return fail(SMS_ERR_UNSUPPORTED, "sms_forward: row too wide for the pipelined path");
+        e = launch_fwd_pipe(a, dtype, aligned, st);
+        break;
     case SMS_PATH_CTA:
         if (!cta_fits(cols, dtype, aligned)) return fail(SMS_ERR_UNSUPPORTED, "sms_forward: row too wide for the CTA path");
         e = launch_fwd_cta(a, dtype, aligned, st);
@@ -299,6 +319,10 @@ int sms_backward(const void *y, const void *dy, void *dx, int64_t rows, int64_t 
         }
         if (!warp_fits(cols, dtype, aligned, true)) return fail(SMS_ERR_UNSUPPORTED, "sms_backward: row too wide for the warp path");
         e = launch_bwd_warp(a, dtype, aligned, st);
+        break;
+    case SMS_PATH_PIPE:
+        if (!pipe_fits(cols, dtype, aligned)) return fail(SMS_ERR_UNSUPPORTED, "sms_backward: row too wide for the pipelined path");
+        e = launch_bwd_pipe(a, dtype, aligned, st);
         break;
     case SMS_PATH_CTA:
         if (!cta_fits_bwd(cols, dtype, aligned)) return fail(SMS_ERR_UNSUPPORTED, "sms_backward: row too wide for the CTA path");

@@ -48,6 +48,12 @@ bool warp_fits(int64_t cols, int dtype, bool aligned, bool bwd);
 cudaError_t launch_fwd_warp(const FwdArgs &a, int dtype, bool aligned, cudaStream_t st);
 cudaError_t launch_bwd_warp(const BwdArgs &a, int dtype, bool aligned, cudaStream_t st);
 
+// lane groups as above, loads streamed through per-thread cp.async rings in
+// shared memory (persistent CTAs)
+bool pipe_fits(int64_t cols, int dtype, bool aligned);
+cudaError_t launch_fwd_pipe(const FwdArgs &a, int dtype, bool aligned, cudaStream_t st);
+cudaError_t launch_bwd_pipe(const BwdArgs &a, int dtype, bool aligned, cudaStream_t st);
+
 // causal rows in balanced pairs (q, S-1-q) held in registers by a lane group
 bool pair_fits(int64_t cols, int dtype);
 cudaError_t launch_fwd_pair(const FwdArgs &a, int dtype, cudaStream_t st);
@@ -65,5 +71,9 @@ cudaError_t launch_bwd_online(const BwdArgs &a, int dtype, cudaStream_t st);
 
 // multiprocessor count of the current device (cached per device)
 int sm_count();
+
+// CTAs for a persistent kernel: `per_sm` per multiprocessor, at most `useful`,
+// at most the limit set by sms_set_grid_limit
+int64_t persistent_grid(int per_sm, int64_t useful);
 
 }  // namespace sms

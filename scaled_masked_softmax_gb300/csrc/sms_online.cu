@@ -277,8 +277,7 @@ __global__ void __launch_bounds__(kNT) bwd_online_kernel(const BwdArgs a)
 template <typename Args, typename K>
 cudaError_t launch_persistent(K kern, const Args &a, cudaStream_t st)
 {
-    int64_t grid = (int64_t)sm_count() * 2;
-    if (grid > a.rows) grid = a.rows;
+    const int64_t grid = persistent_grid(2, a.rows);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kNT);

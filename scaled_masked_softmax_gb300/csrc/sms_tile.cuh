@@ -470,8 +470,7 @@ cudaError_t launch_tile(const FwdArgs &fa, const BwdArgs &ba, cudaStream_t st)
         attr_done[dev & 63].store(1, std::memory_order_release);
     }
     const int64_t rows = BWD ? ba.rows : fa.rows;
-    int64_t grid = (int64_t)sm_count();
-    if (grid > rows) grid = rows;
+    const int64_t grid = persistent_grid(1, rows);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(Geo<WG, R, SLOTS, CH>::THREADS);

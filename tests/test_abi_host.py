@@ -106,9 +106,14 @@ def test_status_strings_and_forced_path():
     for st in range(4):
         assert sms.sms_status_string(st)
     prev = sms.sms_set_forced_path(sms.SMS_PATH_CTA)
-    assert sms.sms_set_forced_path(prev) == sms.SMS_PATH_CTA
+    assert sms.sms_set_forced_path(sms.SMS_PATH_PIPE) == sms.SMS_PATH_CTA
+    assert sms.sms_set_forced_path(prev) == sms.SMS_PATH_PIPE
     with pytest.raises(ValueError):
         sms.sms_set_forced_path(9)
+    prev = sms.sms_set_grid_limit(3)
+    assert sms.sms_set_grid_limit(prev) == 3
+    with pytest.raises(ValueError):
+        sms.sms_set_grid_limit(-1)
 
 
 def test_dispatcher_thresholds():

@@ -24,7 +24,7 @@ pytestmark = pytest.mark.gpu
 DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 WIDTHS = [1, 2, 3, 5, 8, 13, 16, 31, 33, 64, 100, 127, 128, 129, 255, 256, 500, 512, 513, 1000, 1023, 1024,
           1025, 1500, 2047, 2048, 2049, 3000, 4096, 4099, 5000, 8192, 12345, 16384, 20000, 32768, 40000]
-ROWS_FOR_PATH = {"auto": 300, "warp": 37, "cta": 1000, "online": 301}
+ROWS_FOR_PATH = {"auto": 300, "warp": 37, "cta": 1000, "online": 301, "pipe": 1000}
 
 
 def _wl(S, dt, rows, mask="SS", causal=False, B=1, Hh=1, seed=7, values="normal", fill=-math.inf):
@@ -53,7 +53,7 @@ def _run_fwd(w, inp, path):
     return y
 
 
-@pytest.mark.parametrize("path", ["auto", "warp", "cta", "online"])
+@pytest.mark.parametrize("path", ["auto", "warp", "cta", "online", "pipe"])
 @pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("S", WIDTHS)
 def test_forward_widths(S, dt, path):
@@ -64,7 +64,7 @@ def test_forward_widths(S, dt, path):
     H.check_forward(H.to_np64(y), H.oracle_forward(inp, w), DTYPES[dt], f"{path} S={S} {dt} causal={w.is_causal}")
 
 
-@pytest.mark.parametrize("path", ["auto", "warp", "cta", "online"])
+@pytest.mark.parametrize("path", ["auto", "warp", "cta", "online", "pipe"])
 @pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("kind", ["none", "SS", "B1SS", "BHSS"])
 @pytest.mark.parametrize("causal", [False, True])
@@ -80,7 +80,7 @@ def test_forward_mask_layouts(S, causal, kind, dt, path):
     H.check_forward(H.to_np64(y), H.oracle_forward(inp, w), DTYPES[dt], f"{path} {kind} causal={causal} S={S} {dt}")
 
 
-@pytest.mark.parametrize("path", ["auto", "warp", "cta", "online"])
+@pytest.mark.parametrize("path", ["auto", "warp", "cta", "online", "pipe"])
 @pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("S", [1, 3, 31, 64, 129, 1000, 1024, 2048, 2049, 4099, 8192, 16384, 20000])
 def test_backward_widths(S, dt, path):
@@ -129,6 +129,29 @@ def test_workload_scaled_forward_backward(name):
     assert rel <= tol, f"{name}: end-to-end backward relative error {rel:.3e}"
 
 
+@pytest.mark.parametrize("path", ["cta", "online", "pipe"])
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("S,kind,causal", [(8, "BHSS", True), (100, "B1SS", True), (1000, "SS", False),
+                                           (2049, "B1SS", True), (4099, "SS", True)])
+def test_persistent_kernels_walk_many_rows(S, kind, causal, dt, path):
+    """Three CTAs only: every persistent CTA walks many rows (rings wrap,
+    row cursors step across heads and batches)."""
+    B, Hh = 3, 2
+    rows = min(B * Hh * S, 6000 if S < 1000 else 900)
+    fill = -10000.0 if kind == "B1SS" else -math.inf
+    w = _wl(S, dt, rows, mask=kind, causal=causal, B=B, Hh=Hh, seed=23, values="zero" if kind == "B1SS" else "normal",
+            fill=fill)
+    inp = H.make(w)
+    with H.grid_limit(3):
+        y = _run_fwd(w, inp, path)
+        with H.forced_path(path):
+            dx = H.raw_backward(y, inp["dy"], w, causal_hint=causal)
+        torch.cuda.synchronize()
+    assert sms.sms_device_error(torch.cuda.current_stream().cuda_stream) == 0
+    H.check_forward(H.to_np64(y), H.oracle_forward(inp, w), DTYPES[dt], f"{path} grid=3 S={S} {kind} {dt}")
+    H.check_backward(H.to_np64(dx), y.cpu(), inp["dy"].cpu(), w.scale, DTYPES[dt], f"{path} grid=3 bwd S={S} {dt}")
+
+
 def test_spike_rows_are_one_hot():
     w = workloads.scaled(workloads.WORKLOADS["causal_spike_f16_s2048"], B=1, H=2)
     inp = workloads.make_inputs(w, device="cuda")
@@ -147,7 +170,7 @@ def test_fully_masked_rows_give_zero():
             w = _wl(S, dt, 4, mask="SS", values="zero")
             inp = H.make(w)
             inp["mask"][1, :] = -math.inf  # row 1 reads mask row 1: every key masked
-            for path in ("auto", "warp", "cta", "online"):
+            for path in ("auto", "warp", "cta", "online", "pipe"):
                 with H.forced_path(path):
                     try:
                         y = H.raw_forward(inp, w)
@@ -161,7 +184,7 @@ def test_fully_masked_rows_give_zero():
                 assert torch.all(dx[1] == 0) and torch.all(torch.isfinite(dx))
 
 
-@pytest.mark.parametrize("path", ["warp", "cta", "online"])
+@pytest.mark.parametrize("path", ["warp", "cta", "online", "pipe"])
 def test_in_place(path):
     for dt, S in (("f32", 1000), ("bf16", 4099), ("f16", 1024)):
         w = _wl(S, dt, 257, causal=True)
