@@ -77,6 +77,35 @@ struct PipeGeo {
 
 // ------------------------------------------------------------------ forward
 
+// Issue this thread's cp.async copies of the x vectors of the unit whose first
+// row is at cursor c0 into ring stage `stage`.
+template <typename T, int G, int NV, int RPG, bool ALIGNED, int SLOTS>
+__device__ __forceinline__ void fwd_issue(const FwdArgs &a, const Cursor &c0, int stage, bool need_pos, int gl, int tid,
+                                          uint4 *sbuf, uint64_t pol)
+{
+    constexpr int VEC = Dt<T>::VEC;
+    Cursor c = c0;
+#pragma unroll
+    for (int i = 0; i < RPG; ++i) {
+        if (i > 0) {
+            if (need_pos) cursor_next(c, a.cols, a.heads); else ++c.r;
+        }
+        if (c.r < a.rows) {
+            const int limit = a.causal ? (int)(c.q + 1) : (int)a.cols;
+            const int64_t x0 = c.r * a.cols;
+            const int xoff = ALIGNED ? 0 : (int)(x0 & (VEC - 1));
+            const int64_t xb = x0 - xoff;
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                const int vi = k * G + gl;
+                if (vi * VEC - xoff < limit && (ALIGNED || xb + (int64_t)(vi + 1) * VEC <= a.x_total))
+                    cp_async16(&sbuf[((size_t)stage * SLOTS + i * NV + k) * kNT + tid],
+                               reinterpret_cast<const T *>(a.x) + xb + (int64_t)vi * VEC, pol);
+            }
+        }
+    }
+}
+
 template <typename T, int G, int NV, int RPG, bool ALIGNED>
 __global__ void __launch_bounds__(kNT, 1) fwd_pipe_kernel(const FwdArgs a, int64_t units)
 {
@@ -113,38 +142,17 @@ __global__ void __launch_bounds__(kNT, 1) fwd_pipe_kernel(const FwdArgs a, int64
     }
     ci = cc;
 
-    auto issue = [&](const Cursor &c0, int stage) {
-        Cursor c = c0;
-#pragma unroll
-        for (int i = 0; i < RPG; ++i) {
-            if (i > 0) {
-                if (need_pos) cursor_next(c, cols, heads); else ++c.r;
-            }
-            if (c.r >= a.rows) continue;
-            const int limit = a.causal ? (int)(c.q + 1) : (int)cols;
-            const int64_t x0 = c.r * cols;
-            const int xoff = ALIGNED ? 0 : (int)(x0 & (VEC - 1));
-            const int64_t xb = x0 - xoff;
-#pragma unroll
-            for (int k = 0; k < NV; ++k) {
-                const int vi = k * G + gl;
-                if (vi * VEC - xoff < limit && (ALIGNED || xb + (int64_t)(vi + 1) * VEC <= a.x_total))
-                    cp_async16(&sbuf[((size_t)stage * PG::SLOTS + i * NV + k) * kNT + tid],
-                               reinterpret_cast<const T *>(a.x) + xb + (int64_t)vi * VEC, pol);
-            }
-        }
-    };
-
     // prologue: K-1 units in flight
 #pragma unroll
     for (int p = 0; p < K - 1; ++p) {
-        if (p < n_units) issue(ci, p);
+        if (p < n_units) fwd_issue<T, G, NV, RPG, ALIGNED, PG::SLOTS>(a, ci, p, need_pos, gl, tid, sbuf, pol);
         cp_async_commit();
         if (need_pos) cursor_step(ci, D, dq, dhh, db, cols, heads); else ci.r += D;
     }
 
     for (int64_t it = 0; it < n_units; ++it) {
-        if (it + K - 1 < n_units) issue(ci, (int)((it + K - 1) % K));
+        if (it + K - 1 < n_units)
+            fwd_issue<T, G, NV, RPG, ALIGNED, PG::SLOTS>(a, ci, (int)((it + K - 1) % K), need_pos, gl, tid, sbuf, pol);
         cp_async_commit();
         if (need_pos) cursor_step(ci, D, dq, dhh, db, cols, heads); else ci.r += D;
         const int stage = (int)(it % K);
@@ -181,11 +189,13 @@ __global__ void __launch_bounds__(kNT, 1) fwd_pipe_kernel(const FwdArgs a, int64
                 if (a.mask && vi * VEC - xoff[i] < limit[i]) {
                     const int64_t mb = mA[i] + (int64_t)vi * VEC;
                     const T *mk = reinterpret_cast<const T *>(a.mask);
-                    if (ALIGNED) {
+                    if constexpr (ALIGNED) {
                         mr[i][k] = ld_keep(mk + mb);
-                    } else if (mb >= 0 && mb + (msh[i] ? 2 : 1) * VEC <= a.mask_total) {
-                        mr[i][k] = ld_keep(mk + mb);
-                        if (msh[i]) mr2[i][k] = ld_keep(mk + mb + VEC);
+                    } else {
+                        if (mb >= 0 && mb + (msh[i] ? 2 : 1) * VEC <= a.mask_total) {
+                            mr[i][k] = ld_keep(mk + mb);
+                            if (msh[i]) mr2[i][k] = ld_keep(mk + mb + VEC);
+                        }
                     }
                 }
             }
@@ -251,6 +261,7 @@ __global__ void __launch_bounds__(kNT, 1) fwd_pipe_kernel(const FwdArgs a, int64
         // exp(s - m) = 2^(s*log2e - m*log2e); the rounding of m*log2e is common
         // to the row and cancels in the normalisation
         float fac[RPG];
+        __syncwarp();  // every lane of the warp takes part in the shuffles below
         if constexpr (G <= 32) {
 #pragma unroll
             for (int i = 0; i < RPG; ++i) {
@@ -338,6 +349,37 @@ __global__ void __launch_bounds__(kNT, 1) fwd_pipe_kernel(const FwdArgs a, int64
 
 // ----------------------------------------------------------------- backward
 
+// Issue this thread's cp.async copies of the y and dy vectors of a unit.
+template <typename T, int G, int NV, int RPG, bool ALIGNED, int SLOTS>
+__device__ __forceinline__ void bwd_issue(const BwdArgs &a, const Cursor &c0, int stage, bool need_pos, int gl, int tid,
+                                          uint4 *sbuf, uint64_t pol)
+{
+    constexpr int VEC = Dt<T>::VEC;
+    Cursor c = c0;
+#pragma unroll
+    for (int i = 0; i < RPG; ++i) {
+        if (i > 0) {
+            if (need_pos) cursor_next(c, a.cols, 1); else ++c.r;
+        }
+        if (c.r < a.rows) {
+            const int limit = a.causal ? (int)(c.q + 1) : (int)a.cols;
+            const int64_t x0 = c.r * a.cols;
+            const int xoff = ALIGNED ? 0 : (int)(x0 & (VEC - 1));
+            const int64_t xb = x0 - xoff;
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                const int vi = k * G + gl;
+                if (vi * VEC - xoff < limit && (ALIGNED || xb + (int64_t)(vi + 1) * VEC <= a.total)) {
+                    const size_t s0 = (((size_t)stage * 2 + 0) * SLOTS + i * NV + k) * kNT + tid;
+                    const size_t s1 = (((size_t)stage * 2 + 1) * SLOTS + i * NV + k) * kNT + tid;
+                    cp_async16(&sbuf[s0], reinterpret_cast<const T *>(a.y) + xb + (int64_t)vi * VEC, pol);
+                    cp_async16(&sbuf[s1], reinterpret_cast<const T *>(a.dy) + xb + (int64_t)vi * VEC, pol);
+                }
+            }
+        }
+    }
+}
+
 template <typename T, int G, int NV, int RPG, bool ALIGNED>
 __global__ void __launch_bounds__(kNT, 1) bwd_pipe_kernel(const BwdArgs a, int64_t units)
 {
@@ -370,41 +412,20 @@ __global__ void __launch_bounds__(kNT, 1) bwd_pipe_kernel(const BwdArgs a, int64
     }
     ci = cc;
 
-    auto slot = [&](int stage, int stream, int i, int k) -> uint4 * {
-        return &sbuf[(((size_t)stage * 2 + stream) * PG::SLOTS + i * NV + k) * kNT + tid];
-    };
-    auto issue = [&](const Cursor &c0, int stage) {
-        Cursor c = c0;
-#pragma unroll
-        for (int i = 0; i < RPG; ++i) {
-            if (i > 0) {
-                if (need_pos) cursor_next(c, cols, 1); else ++c.r;
-            }
-            if (c.r >= a.rows) continue;
-            const int limit = a.causal ? (int)(c.q + 1) : (int)cols;
-            const int64_t x0 = c.r * cols;
-            const int xoff = ALIGNED ? 0 : (int)(x0 & (VEC - 1));
-            const int64_t xb = x0 - xoff;
-#pragma unroll
-            for (int k = 0; k < NV; ++k) {
-                const int vi = k * G + gl;
-                if (vi * VEC - xoff < limit && (ALIGNED || xb + (int64_t)(vi + 1) * VEC <= a.total)) {
-                    cp_async16(slot(stage, 0, i, k), reinterpret_cast<const T *>(a.y) + xb + (int64_t)vi * VEC, pol);
-                    cp_async16(slot(stage, 1, i, k), reinterpret_cast<const T *>(a.dy) + xb + (int64_t)vi * VEC, pol);
-                }
-            }
-        }
+    auto slot_idx = [](int stage, int stream, int i, int k, int t) -> size_t {
+        return (((size_t)stage * 2 + stream) * PG::SLOTS + i * NV + k) * kNT + t;
     };
 
 #pragma unroll
     for (int p = 0; p < K - 1; ++p) {
-        if (p < n_units) issue(ci, p);
+        if (p < n_units) bwd_issue<T, G, NV, RPG, ALIGNED, PG::SLOTS>(a, ci, p, need_pos, gl, tid, sbuf, pol);
         cp_async_commit();
         if (need_pos) cursor_step(ci, D, dq, dhh, db, cols, 1); else ci.r += D;
     }
 
     for (int64_t it = 0; it < n_units; ++it) {
-        if (it + K - 1 < n_units) issue(ci, (int)((it + K - 1) % K));
+        if (it + K - 1 < n_units)
+            bwd_issue<T, G, NV, RPG, ALIGNED, PG::SLOTS>(a, ci, (int)((it + K - 1) % K), need_pos, gl, tid, sbuf, pol);
         cp_async_commit();
         if (need_pos) cursor_step(ci, D, dq, dhh, db, cols, 1); else ci.r += D;
         const int stage = (int)(it % K);
@@ -440,8 +461,8 @@ __global__ void __launch_bounds__(kNT, 1) bwd_pipe_kernel(const BwdArgs a, int64
                 yr[i][k] = gr[i][k] = make_uint4(0, 0, 0, 0);
                 if (j0 < limit[i]) {
                     if (ALIGNED || xb + (int64_t)(vi + 1) * VEC <= a.total) {
-                        yr[i][k] = *slot(stage, 0, i, k);
-                        gr[i][k] = *slot(stage, 1, i, k);
+                        yr[i][k] = sbuf[slot_idx(stage, 0, i, k, tid)];
+                        gr[i][k] = sbuf[slot_idx(stage, 1, i, k, tid)];
                     } else {  // last partial vector of the tensor: not staged
                         float tv[VEC], tg[VEC];
 #pragma unroll
@@ -469,6 +490,7 @@ __global__ void __launch_bounds__(kNT, 1) bwd_pipe_kernel(const BwdArgs a, int64
                 }
             }
         }
+        __syncwarp();  // every lane of the warp takes part in the shuffles below
         if constexpr (G <= 32) {
 #pragma unroll
             for (int i = 0; i < RPG; ++i) dot[i] = group_sum<G>(dot[i]);
