@@ -86,9 +86,7 @@ typedef enum {
     SMS_PATH_AUTO = 0,
     SMS_PATH_WARP = 1,   /* rows held in registers by a warp (or part of one)          */
     SMS_PATH_CTA = 2,    /* persistent CTA per row, rows staged by bulk (TMA) copies   */
-    SMS_PATH_ONLINE = 3, /* streaming two pass: online max/sum, then re-read and write */
-    SMS_PATH_PIPE = 4    /* lane groups as SMS_PATH_WARP, loads staged per thread in a
-                            cp.async shared-memory ring by persistent CTAs          */
+    SMS_PATH_ONLINE = 3  /* streaming two pass: online max/sum, then re-read and write */
 } sms_path;
 
 /*
@@ -138,8 +136,8 @@ SMS_API const char *sms_last_error(void);
 SMS_API int sms_set_forced_path(int path);
 
 /*
- * Cap the CTAs of the persistent kernel families (SMS_PATH_CTA, SMS_PATH_PIPE,
- * SMS_PATH_ONLINE) at `ctas` (0 = one per SM, the default): each CTA then
+ * Cap the CTAs of the persistent kernel families (SMS_PATH_CTA, SMS_PATH_ONLINE)
+ * at `ctas` (0 = as many as the device holds, the default): each CTA then
  * walks more rows, which lets small tests cover multi-row pipelines.
  * Returns the previous cap, or -1 for a negative argument.  Process-wide.
  */

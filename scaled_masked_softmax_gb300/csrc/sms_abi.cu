@@ -153,7 +153,7 @@ const char *sms_last_error(void) { return t_err; }
 
 int sms_set_forced_path(int path)
 {
-    if (path < SMS_PATH_AUTO || path > SMS_PATH_PIPE) return -1;
+    if (path < SMS_PATH_AUTO || path > SMS_PATH_ONLINE) return -1;
     return g_forced.exchange(path);
 }
 
@@ -251,10 +251,6 @@ int sms_forward(const void *x, const void *mask, int64_t mask_numel, int64_t mas
         if (!warp_fits(cols, dtype, aligned, false)) return fail(SMS_ERR_UNSUPPORTED, "sms_forward: row too wide for the warp path");
         e = launch_fwd_warp(a, dtype, aligned, st);
         break;
-    case SMS_PATH_PIPE:
-        if (!pipe_fits(cols, dtype, aligned)) return fail(SMS_ERR_UNSUPPORTED, "sms_forward: row too wide for the pipelined path");
-        e = launch_fwd_pipe(a, dtype, aligned, st);
-        break;
     case SMS_PATH_CTA:
         if (!cta_fits(cols, dtype, aligned)) return fail(SMS_ERR_UNSUPPORTED, "sms_forward: row too wide for the CTA path");
         e = launch_fwd_cta(a, dtype, aligned, st);
@@ -319,10 +315,6 @@ int sms_backward(const void *y, const void *dy, void *dx, int64_t rows, int64_t 
         }
         if (!warp_fits(cols, dtype, aligned, true)) return fail(SMS_ERR_UNSUPPORTED, "sms_backward: row too wide for the warp path");
         e = launch_bwd_warp(a, dtype, aligned, st);
-        break;
-    case SMS_PATH_PIPE:
-        if (!pipe_fits(cols, dtype, aligned)) return fail(SMS_ERR_UNSUPPORTED, "sms_backward: row too wide for the pipelined path");
-        e = launch_bwd_pipe(a, dtype, aligned, st);
         break;
     case SMS_PATH_CTA:
         if (!cta_fits_bwd(cols, dtype, aligned)) return fail(SMS_ERR_UNSUPPORTED, "sms_backward: row too wide for the CTA path");

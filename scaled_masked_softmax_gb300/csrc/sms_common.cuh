@@ -87,11 +87,6 @@ template <> __device__ __forceinline__ uint4 pack<__nv_bfloat16>(const float *f)
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-__device__ __forceinline__ uint32_t smem_u32_of(const void *p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
 // Elements S .. S+VEC-1 of the 2*VEC elements held by two consecutive 16-byte
 // vectors (lo, hi): realigns a row that starts mid-vector relative to another.
 template <int VEC, int S> __device__ __forceinline__ uint4 window_fixed(const uint4 &lo, const uint4 &hi)
@@ -132,17 +127,6 @@ template <int VEC> __device__ __forceinline__ uint4 window(const uint4 &lo, cons
 __device__ __forceinline__ uint4 ld_stream(const void *p) { return __ldcs(reinterpret_cast<const uint4 *>(p)); }
 __device__ __forceinline__ uint4 ld_keep(const void *p) { return __ldg(reinterpret_cast<const uint4 *>(p)); }
 __device__ __forceinline__ void st_stream(void *p, const uint4 &v) { __stcs(reinterpret_cast<uint4 *>(p), v); }
-
-// Per-thread asynchronous 16-byte copy global -> shared (LDGSTS), bypassing L1,
-// with an L2 eviction policy; completion is tracked per thread in commit
-// groups (cp.async.commit_group / cp.async.wait_group), nothing spins.
-__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src, uint64_t policy)
-{
-    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;"
-                 :: "r"(smem_u32_of(smem_dst)), "l"(gmem_src), "l"(policy) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N> __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
 
 // ------------------------------------------------------------ arithmetic ---
 // 2^x on the special-function unit (PTX ex2.approx, subnormal results flushed

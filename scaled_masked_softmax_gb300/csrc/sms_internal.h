@@ -48,12 +48,6 @@ bool warp_fits(int64_t cols, int dtype, bool aligned, bool bwd);
 cudaError_t launch_fwd_warp(const FwdArgs &a, int dtype, bool aligned, cudaStream_t st);
 cudaError_t launch_bwd_warp(const BwdArgs &a, int dtype, bool aligned, cudaStream_t st);
 
-// lane groups as above, loads streamed through per-thread cp.async rings in
-// shared memory (persistent CTAs)
-bool pipe_fits(int64_t cols, int dtype, bool aligned);
-cudaError_t launch_fwd_pipe(const FwdArgs &a, int dtype, bool aligned, cudaStream_t st);
-cudaError_t launch_bwd_pipe(const BwdArgs &a, int dtype, bool aligned, cudaStream_t st);
-
 // causal rows in balanced pairs (q, S-1-q) held in registers by a lane group
 bool pair_fits(int64_t cols, int dtype);
 cudaError_t launch_fwd_pair(const FwdArgs &a, int dtype, cudaStream_t st);

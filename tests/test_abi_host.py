@@ -106,8 +106,10 @@ def test_status_strings_and_forced_path():
     for st in range(4):
         assert sms.sms_status_string(st)
     prev = sms.sms_set_forced_path(sms.SMS_PATH_CTA)
-    assert sms.sms_set_forced_path(sms.SMS_PATH_PIPE) == sms.SMS_PATH_CTA
-    assert sms.sms_set_forced_path(prev) == sms.SMS_PATH_PIPE
+    assert sms.sms_set_forced_path(sms.SMS_PATH_ONLINE) == sms.SMS_PATH_CTA
+    assert sms.sms_set_forced_path(prev) == sms.SMS_PATH_ONLINE
+    with pytest.raises(ValueError):
+        sms.sms_set_forced_path(4)
     with pytest.raises(ValueError):
         sms.sms_set_forced_path(9)
     prev = sms.sms_set_grid_limit(3)
