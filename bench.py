@@ -171,6 +171,38 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ------------------------------------------------------- ranks (weak) ---
+
+def dist_env():
+    """(world, rank, local_rank) from the launcher's environment; one process
+    per GPU, each running the whole workload on its own rows (replicas)."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def init_dist(world, rank):
+    if world > 1:
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend, rank=rank, world_size=world)
+
+
+def max_over_ranks(ms, world, device=None):
+    """The slowest rank's time: the job is done when every rank is."""
+    if world <= 1:
+        return ms
+    on_gpu = torch.distributed.get_backend() == "nccl"
+    t = torch.tensor([ms], dtype=torch.float64, device=device if on_gpu else "cpu")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbs(step_bytes, world, step_ms):
+    """Whole-job throughput: every rank moves step_bytes per step (weak
+    scaling), all of them within the slowest rank's step time."""
+    return step_bytes * world / (step_ms * 1e6)
+
+
 # ------------------------------------------------------------------ ours ---
 
 def run_ours(args, rank, world, device):
@@ -251,10 +283,7 @@ def run_ours(args, rank, world, device):
     # with an L2 flush between steps the step time is the kernels' own time
     step_ms = (kern_ms if flush else region_ms) / K
 
-    if world > 1:
-        tt = torch.tensor([step_ms], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(tt.item())
+    step_ms = max_over_ranks(step_ms, world, device)
 
     peak, peak_kind = _peaks()
     f_ms, b_ms = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
@@ -270,7 +299,7 @@ def run_ours(args, rank, world, device):
     roof = {"kernel": dom, "bound": "hbm", "achieved": kernels[dom]["gbs"], "peak": peak, "unit": "GB/s",
             "frac": round(kernels[dom]["gbs"] / peak, 4), "traffic": traffic, "peak_source": peak_kind}
 
-    value = step_bytes * world / (step_ms * 1e6)
+    value = aggregate_gbs(step_bytes, world, step_ms)
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
@@ -456,13 +485,8 @@ def main():
     ap.add_argument("--all-paths", action="store_true", help="with --all: every kernel family per workload")
     args = ap.parse_args()
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        backend = "nccl" if torch.cuda.is_available() else "gloo"
-        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
-        torch.distributed.init_process_group(backend, rank=rank, world_size=world)
+    world, rank, local = dist_env()
+    init_dist(world, rank)
 
     if args.impl == "reference":
         res = run_reference(args, rank, world)

@@ -113,8 +113,7 @@ SMS_API int sms_forward(const void *x, const void *mask, int64_t mask_numel, int
  *   dx             result [rows, cols] (device, `dtype`); may equal dy (in place)
  *   is_causal_hint nonzero promises that y[r, j] == 0 for every j > q (true for a
  *                  forward run with is_causal); the kernels then skip reading y
- *                  and dy there and write dx = +0, and may pair rows q and
- *                  S-1-q to balance the work.  For finite dy the result equals
+ *                  and dy there and write dx = +0.  For finite dy the result equals
  *                  the unhinted one up to the rounding of the row sum's
  *                  summation order; positions with y == 0 are +0 either way.
  * rows == 0 (with cols >= 1) is a valid no-op; the pointers may then be NULL.

@@ -100,13 +100,13 @@ int launch_status(cudaError_t e, const char *what)
 constexpr int64_t kMaxCols = (int64_t)1 << 30;
 constexpr int64_t kMaxElems = (int64_t)1 << 60;
 
-int pick_path(int forced, int64_t cols, int dtype, bool aligned, bool bwd, bool causal)
+int pick_path(int forced, int64_t cols, int dtype, bool aligned, bool bwd)
 {
     if (forced != SMS_PATH_AUTO) return forced;
-    // Register-resident lane groups while a row (or, under the causal flag, a
-    // balanced pair of rows) fits them; wider rows go to the staged CTA path
-    // while they fit its registers; beyond that, stream twice.
-    if (warp_fits(cols, dtype, aligned, bwd) || (causal && pair_fits(cols, dtype))) return SMS_PATH_WARP;
+    // Register-resident lane groups while a row fits them; wider rows go to
+    // the staged CTA path while they fit its registers; beyond that, stream
+    // twice.
+    if (warp_fits(cols, dtype, aligned, bwd)) return SMS_PATH_WARP;
     if (bwd ? cta_fits_bwd(cols, dtype, aligned) : cta_fits(cols, dtype, aligned)) return SMS_PATH_CTA;
     return SMS_PATH_ONLINE;
 }
@@ -172,7 +172,7 @@ int sms_select_path(int64_t rows, int64_t cols, int dtype, int is_backward)
     (void)rows;
     if (cols <= 0 || dtype < SMS_F32 || dtype > SMS_BF16) return -1;
     const bool aligned = cols % vec_elems(dtype) == 0;
-    return pick_path(SMS_PATH_AUTO, cols, dtype, aligned, is_backward != 0, false);
+    return pick_path(SMS_PATH_AUTO, cols, dtype, aligned, is_backward != 0);
 }
 
 int sms_forward(const void *x, const void *mask, int64_t mask_numel, int64_t mask_stride_b, int64_t mask_stride_h,
@@ -240,14 +240,10 @@ int sms_forward(const void *x, const void *mask, int64_t mask_numel, int64_t mas
     a.dcols = FastDiv((uint32_t)cols);
     a.dheads = FastDiv((uint32_t)heads);
 
-    const int path = pick_path(g_forced.load(), cols, dtype, aligned, false, a.causal != 0);
+    const int path = pick_path(g_forced.load(), cols, dtype, aligned, false);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (path) {
     case SMS_PATH_WARP:
-        if (a.causal && pair_fits(cols, dtype)) {
-            e = launch_fwd_pair(a, dtype, st);
-            break;
-        }
         if (!warp_fits(cols, dtype, aligned, false)) return fail(SMS_ERR_UNSUPPORTED, "sms_forward: row too wide for the warp path");
         e = launch_fwd_warp(a, dtype, aligned, st);
         break;
@@ -305,14 +301,10 @@ int sms_backward(const void *y, const void *dy, void *dx, int64_t rows, int64_t 
     a.scale = scale; a.causal = is_causal_hint ? 1 : 0; a.err = err;
     a.dcols = FastDiv((uint32_t)cols);
 
-    const int path = pick_path(g_forced.load(), cols, dtype, aligned, true, a.causal != 0);
+    const int path = pick_path(g_forced.load(), cols, dtype, aligned, true);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (path) {
     case SMS_PATH_WARP:
-        if (a.causal && pair_fits(cols, dtype)) {
-            e = launch_bwd_pair(a, dtype, st);
-            break;
-        }
         if (!warp_fits(cols, dtype, aligned, true)) return fail(SMS_ERR_UNSUPPORTED, "sms_backward: row too wide for the warp path");
         e = launch_bwd_warp(a, dtype, aligned, st);
         break;

@@ -48,10 +48,6 @@ bool warp_fits(int64_t cols, int dtype, bool aligned, bool bwd);
 cudaError_t launch_fwd_warp(const FwdArgs &a, int dtype, bool aligned, cudaStream_t st);
 cudaError_t launch_bwd_warp(const BwdArgs &a, int dtype, bool aligned, cudaStream_t st);
 
-// causal rows in balanced pairs (q, S-1-q) held in registers by a lane group
-bool pair_fits(int64_t cols, int dtype);
-cudaError_t launch_fwd_pair(const FwdArgs &a, int dtype, cudaStream_t st);
-cudaError_t launch_bwd_pair(const BwdArgs &a, int dtype, cudaStream_t st);
 
 // persistent CTA per row, bulk-copy (TMA) staging ring, rows in registers
 bool cta_fits(int64_t cols, int dtype, bool aligned);      // forward

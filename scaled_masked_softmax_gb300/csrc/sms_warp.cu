@@ -402,6 +402,9 @@ cudaError_t launch_one(const Args &a, cudaStream_t st)
 // mask stream is served by L2).  More vectors per lane stop fitting the 128
 // registers that keep two CTAs per SM, and loads then serialise.  Short rows
 // use few lanes with several vectors each: fewer shuffle rounds per row.
+// Aligned 16-bit forward rows beyond 256*5 vectors take 6 or 8 vectors per
+// lane (no realignment registers are needed there): measured faster than the
+// staged CTA path at those widths, slower than 4-5 vectors below them.
 template <typename T, bool ALIGNED, bool BWD, typename Args>
 cudaError_t launch_t(const Args &a, cudaStream_t st)
 {
@@ -418,6 +421,7 @@ cudaError_t launch_t(const Args &a, cudaStream_t st)
         SMS_TRY(4, 1, 4) SMS_TRY(4, 2, 2) SMS_TRY(4, 4, 1) SMS_TRY(8, 4, 1) SMS_TRY(16, 4, 1) SMS_TRY(32, 4, 1)
         SMS_TRY(64, 4, 1) SMS_TRY(64, 5, 1) SMS_TRY(128, 4, 1) SMS_TRY(128, 5, 1) SMS_TRY(256, 4, 1)
         SMS_TRY(256, 5, 1)
+        if constexpr (!BWD && ALIGNED) { SMS_TRY(256, 6, 1) SMS_TRY(256, 8, 1) }
     }
 #undef SMS_TRY
     return cudaErrorNotSupported;
@@ -444,7 +448,7 @@ bool warp_fits(int64_t cols, int dtype, bool aligned, bool bwd)
 {
     const int vec = vec_elems(dtype);
     const int64_t need = (cols + vec - 1) / vec + (aligned ? 0 : 1);
-    const int64_t cap = (vec == 4 && !bwd) ? 256 * 8 : 256 * 5;  // widest shapes (see launch_t)
+    const int64_t cap = (!bwd && (vec == 4 || aligned)) ? 256 * 8 : 256 * 5;  // widest shapes (see launch_t)
     return need <= cap;
 }
 

@@ -125,7 +125,12 @@ def test_dispatcher_thresholds():
         assert sms.sms_select_path(1000, 1024, dt) == W
         assert sms.sms_select_path(1000, 4096, dt) == W
         assert sms.sms_select_path(1000, 8192, dt) == W
-        assert sms.sms_select_path(1000, 16384, dt) == C
+        # aligned 16-bit forward rows stay register-resident up to 256 lanes x 8 vectors
+        assert sms.sms_select_path(1000, 16384, dt) == (C if dt == 0 else W)
+        assert sms.sms_select_path(1000, 16384, dt, True) == C
+        assert sms.sms_select_path(1000, 16392, dt) == O  # beyond the staged path's forward registers
+        assert sms.sms_select_path(1000, 10248, dt) == (C if dt == 0 else W)  # 16-bit: 1281 vectors, 256 x 6
+        assert sms.sms_select_path(1000, 10249, dt) == C  # unaligned 16-bit rows stop at 256 x 5 vectors
         assert sms.sms_select_path(1000, 1 << 20, dt) == O
         assert sms.sms_select_path(1000, 1 << 20, dt, True) == O
     assert sms.sms_select_path(1, 0, 0) == -1
