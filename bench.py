@@ -480,7 +480,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--all", metavar="JSONL", default=None, help="also bench every workload into this file")
-    ap.add_argument("--path", choices=["auto", "warp", "cta", "online"], default="auto",
+    ap.add_argument("--path", choices=["auto", "warp", "stream", "ring", "cta", "online"], default="auto",
                     help="force one kernel family (tuning); the default lets the dispatcher choose")
     ap.add_argument("--all-paths", action="store_true", help="with --all: every kernel family per workload")
     args = ap.parse_args()
@@ -505,7 +505,7 @@ def main():
     __graft_entry__.build()
     import scaled_masked_softmax_gb300 as sms
 
-    path_code = {"auto": 0, "warp": 1, "cta": 2, "online": 3}
+    path_code = {"auto": 0, "warp": 1, "cta": 2, "online": 3, "stream": 4, "ring": 5}
     sms.sms_set_forced_path(path_code[args.path])
     res, (w, inp, _y, _dx) = run_ours(args, rank, world, device)
     if rank == 0:
@@ -522,7 +522,7 @@ def main():
     if args.all and rank == 0 and world == 1:
         from scaled_masked_softmax_gb300 import workloads
 
-        paths = ["auto", "warp", "cta", "online"] if args.all_paths else [args.path]
+        paths = ["auto", "warp", "stream", "ring", "cta", "online"] if args.all_paths else [args.path]
         with open(args.all, "w") as f:
             for name in workloads.WORKLOADS:
                 for pth in paths:

@@ -86,7 +86,9 @@ typedef enum {
     SMS_PATH_AUTO = 0,
     SMS_PATH_WARP = 1,   /* rows held in registers by a warp (or part of one)          */
     SMS_PATH_CTA = 2,    /* persistent CTA per row, rows staged by bulk (TMA) copies   */
-    SMS_PATH_ONLINE = 3  /* streaming two pass: online max/sum, then re-read and write */
+    SMS_PATH_ONLINE = 3, /* streaming two pass: online max/sum, then re-read and write */
+    SMS_PATH_STREAM = 4, /* persistent lane groups, rows in registers, next row prefetched */
+    SMS_PATH_RING = 5    /* a warp per row, fed by its own ring of bulk (TMA) copies       */
 } sms_path;
 
 /*
@@ -135,14 +137,15 @@ SMS_API const char *sms_last_error(void);
 SMS_API int sms_set_forced_path(int path);
 
 /*
- * Cap the CTAs of the persistent kernel families (SMS_PATH_CTA, SMS_PATH_ONLINE)
+ * Cap the CTAs of the persistent kernel families (SMS_PATH_STREAM, SMS_PATH_RING,
+ * SMS_PATH_CTA, SMS_PATH_ONLINE)
  * at `ctas` (0 = as many as the device holds, the default): each CTA then
  * walks more rows, which lets small tests cover multi-row pipelines.
  * Returns the previous cap, or -1 for a negative argument.  Process-wide.
  */
 SMS_API int sms_set_grid_limit(int ctas);
 
-/* The family the dispatcher would pick for this forward (or backward) shape. */
+/* The family the dispatcher would pick for this forward (or backward) shape of non-causal rows. */
 SMS_API int sms_select_path(int64_t rows, int64_t cols, int dtype, int is_backward);
 
 /* The family taken by the last successful call on this host thread. */

@@ -15,8 +15,9 @@ LIB_PATH = os.path.join(_PKG, "libsms.so")
 
 SMS_F32, SMS_F16, SMS_BF16 = 0, 1, 2
 SMS_OK, SMS_ERR_INVALID_ARG, SMS_ERR_UNSUPPORTED, SMS_ERR_CUDA = 0, 1, 2, 3
-SMS_PATH_AUTO, SMS_PATH_WARP, SMS_PATH_CTA, SMS_PATH_ONLINE = 0, 1, 2, 3
-PATH_NAMES = {SMS_PATH_AUTO: "auto", SMS_PATH_WARP: "warp", SMS_PATH_CTA: "cta", SMS_PATH_ONLINE: "online"}
+SMS_PATH_AUTO, SMS_PATH_WARP, SMS_PATH_CTA, SMS_PATH_ONLINE, SMS_PATH_STREAM, SMS_PATH_RING = 0, 1, 2, 3, 4, 5
+PATH_NAMES = {SMS_PATH_AUTO: "auto", SMS_PATH_WARP: "warp", SMS_PATH_CTA: "cta", SMS_PATH_ONLINE: "online",
+              SMS_PATH_STREAM: "stream", SMS_PATH_RING: "ring"}
 
 # every function include/sms.h declares: name -> (restype, argtypes)
 _i64, _i32, _f32, _vp, _cp = ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_char_p

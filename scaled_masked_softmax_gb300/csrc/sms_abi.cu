@@ -100,13 +100,20 @@ int launch_status(cudaError_t e, const char *what)
 constexpr int64_t kMaxCols = (int64_t)1 << 30;
 constexpr int64_t kMaxElems = (int64_t)1 << 60;
 
-int pick_path(int forced, int64_t cols, int dtype, bool aligned, bool bwd)
+int pick_path(int forced, int64_t cols, int dtype, bool aligned, bool bwd, bool causal)
 {
     if (forced != SMS_PATH_AUTO) return forced;
-    // Register-resident lane groups while a row fits them; wider rows go to
-    // the staged CTA path while they fit its registers; beyond that, stream
-    // twice.
+    // By measurement on GB300 (per-family sweeps over the benchmark shapes):
+    //  * causal forward rows read a variable prefix; the per-warp bulk-copy
+    //    rings keep enough of them in flight (registers do not): ring;
+    //  * short aligned fp32 forward rows: the persistent prefetching groups;
+    //  * otherwise register-resident lane groups while a row fits them;
+    //  * 16-bit backward rows too wide for registers: ring, then the staged
+    //    CTA path while a row fits its registers; beyond that, stream twice.
+    if (!bwd && causal && aligned && ring_fits(cols, dtype, aligned)) return SMS_PATH_RING;
+    if (!bwd && dtype == SMS_F32 && aligned && cols <= 512) return SMS_PATH_STREAM;
     if (warp_fits(cols, dtype, aligned, bwd)) return SMS_PATH_WARP;
+    if (bwd && dtype != SMS_F32 && ring_fits(cols, dtype, aligned)) return SMS_PATH_RING;
     if (bwd ? cta_fits_bwd(cols, dtype, aligned) : cta_fits(cols, dtype, aligned)) return SMS_PATH_CTA;
     return SMS_PATH_ONLINE;
 }
@@ -153,7 +160,7 @@ const char *sms_last_error(void) { return t_err; }
 
 int sms_set_forced_path(int path)
 {
-    if (path < SMS_PATH_AUTO || path > SMS_PATH_ONLINE) return -1;
+    if (path < SMS_PATH_AUTO || path > SMS_PATH_RING) return -1;
     return g_forced.exchange(path);
 }
 
@@ -172,7 +179,7 @@ int sms_select_path(int64_t rows, int64_t cols, int dtype, int is_backward)
     (void)rows;
     if (cols <= 0 || dtype < SMS_F32 || dtype > SMS_BF16) return -1;
     const bool aligned = cols % vec_elems(dtype) == 0;
-    return pick_path(SMS_PATH_AUTO, cols, dtype, aligned, is_backward != 0);
+    return pick_path(SMS_PATH_AUTO, cols, dtype, aligned, is_backward != 0, false);
 }
 
 int sms_forward(const void *x, const void *mask, int64_t mask_numel, int64_t mask_stride_b, int64_t mask_stride_h,
@@ -240,12 +247,21 @@ int sms_forward(const void *x, const void *mask, int64_t mask_numel, int64_t mas
     a.dcols = FastDiv((uint32_t)cols);
     a.dheads = FastDiv((uint32_t)heads);
 
-    const int path = pick_path(g_forced.load(), cols, dtype, aligned, false);
+    const int path = pick_path(g_forced.load(), cols, dtype, aligned, false, a.causal != 0);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (path) {
     case SMS_PATH_WARP:
         if (!warp_fits(cols, dtype, aligned, false)) return fail(SMS_ERR_UNSUPPORTED, "sms_forward: row too wide for the warp path");
         e = launch_fwd_warp(a, dtype, aligned, st);
+        break;
+    case SMS_PATH_RING:
+        if (!ring_fits(cols, dtype, aligned)) return fail(SMS_ERR_UNSUPPORTED, "sms_forward: row too wide for the ring path");
+        e = launch_fwd_ring(a, dtype, aligned, st);
+        break;
+    case SMS_PATH_STREAM:
+        if (!stream_fits(cols, dtype, aligned, false))
+            return fail(SMS_ERR_UNSUPPORTED, "sms_forward: row too wide for the stream path");
+        e = launch_fwd_stream(a, dtype, aligned, st);
         break;
     case SMS_PATH_CTA:
         if (!cta_fits(cols, dtype, aligned)) return fail(SMS_ERR_UNSUPPORTED, "sms_forward: row too wide for the CTA path");
@@ -301,12 +317,21 @@ int sms_backward(const void *y, const void *dy, void *dx, int64_t rows, int64_t 
     a.scale = scale; a.causal = is_causal_hint ? 1 : 0; a.err = err;
     a.dcols = FastDiv((uint32_t)cols);
 
-    const int path = pick_path(g_forced.load(), cols, dtype, aligned, true);
+    const int path = pick_path(g_forced.load(), cols, dtype, aligned, true, a.causal != 0);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (path) {
     case SMS_PATH_WARP:
         if (!warp_fits(cols, dtype, aligned, true)) return fail(SMS_ERR_UNSUPPORTED, "sms_backward: row too wide for the warp path");
         e = launch_bwd_warp(a, dtype, aligned, st);
+        break;
+    case SMS_PATH_RING:
+        if (!ring_fits(cols, dtype, aligned)) return fail(SMS_ERR_UNSUPPORTED, "sms_backward: row too wide for the ring path");
+        e = launch_bwd_ring(a, dtype, aligned, st);
+        break;
+    case SMS_PATH_STREAM:
+        if (!stream_fits(cols, dtype, aligned, true))
+            return fail(SMS_ERR_UNSUPPORTED, "sms_backward: row too wide for the stream path");
+        e = launch_bwd_stream(a, dtype, aligned, st);
         break;
     case SMS_PATH_CTA:
         if (!cta_fits_bwd(cols, dtype, aligned)) return fail(SMS_ERR_UNSUPPORTED, "sms_backward: row too wide for the CTA path");

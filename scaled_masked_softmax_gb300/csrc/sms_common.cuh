@@ -127,7 +127,6 @@ template <int VEC> __device__ __forceinline__ uint4 window(const uint4 &lo, cons
 __device__ __forceinline__ uint4 ld_stream(const void *p) { return __ldcs(reinterpret_cast<const uint4 *>(p)); }
 __device__ __forceinline__ uint4 ld_keep(const void *p) { return __ldg(reinterpret_cast<const uint4 *>(p)); }
 __device__ __forceinline__ void st_stream(void *p, const uint4 &v) { __stcs(reinterpret_cast<uint4 *>(p), v); }
-
 // ------------------------------------------------------------ arithmetic ---
 // 2^x on the special-function unit (PTX ex2.approx, subnormal results flushed
 // to zero; 2^-inf = +0).

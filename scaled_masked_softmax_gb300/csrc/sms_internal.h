@@ -49,6 +49,16 @@ cudaError_t launch_fwd_warp(const FwdArgs &a, int dtype, bool aligned, cudaStrea
 cudaError_t launch_bwd_warp(const BwdArgs &a, int dtype, bool aligned, cudaStream_t st);
 
 
+// persistent lane groups walking rows with a one-row register prefetch
+bool stream_fits(int64_t cols, int dtype, bool aligned, bool bwd);  // forward: aligned rows only
+cudaError_t launch_fwd_stream(const FwdArgs &a, int dtype, bool aligned, cudaStream_t st);
+cudaError_t launch_bwd_stream(const BwdArgs &a, int dtype, bool aligned, cudaStream_t st);
+
+// a warp per row, each warp feeding itself through a ring of bulk copies (TMA)
+bool ring_fits(int64_t cols, int dtype, bool aligned);
+cudaError_t launch_fwd_ring(const FwdArgs &a, int dtype, bool aligned, cudaStream_t st);
+cudaError_t launch_bwd_ring(const BwdArgs &a, int dtype, bool aligned, cudaStream_t st);
+
 // persistent CTA per row, bulk-copy (TMA) staging ring, rows in registers
 bool cta_fits(int64_t cols, int dtype, bool aligned);      // forward
 bool cta_fits_bwd(int64_t cols, int dtype, bool aligned);  // backward (y and dy both held)

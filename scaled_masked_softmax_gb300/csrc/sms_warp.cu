@@ -13,8 +13,7 @@
 // vi*VEC - xoff .. vi*VEC - xoff + VEC - 1 where xoff = (row*cols) mod VEC, so a
 // row that starts mid-vector (cols not a multiple of VEC) still moves with
 // 16-byte loads; the partial head and tail vectors are stored element-wise.
-#include "sms_common.cuh"
-#include "sms_internal.h"
+#include "sms_rowmath.cuh"
 
 namespace sms {
 namespace {
@@ -379,6 +378,39 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_warp_kernel(const BwdArgs a)
     }
 }
 
+// One row per lane group: the shared row math of sms_rowmath.cuh (one
+// switch per row realigns a misaligned mask, bounds are tested once per row,
+// paired elements use the packed fp32x2 forms).
+template <typename T, int G, int NV, bool ALIGNED>
+__global__ void __launch_bounds__(kThreads, 2) fwd_row_kernel(const FwdArgs a)
+{
+    using namespace rowmath;
+    constexpr int GPC = kThreads / G;
+    constexpr int W = G > 32 ? G / 32 : 1;
+    __shared__ float red_m[GPC][W], red_l[GPC][W];
+    const int gl = threadIdx.x % G;
+    const int gi = threadIdx.x / G;
+    const RowPos p = fwd_pos<Dt<T>::VEC, ALIGNED>(a, (int64_t)blockIdx.x * GPC + gi);
+    FwdBuf<NV, ALIGNED> B;
+    fwd_issue<T, G, NV, ALIGNED>(a, p, gl, B);
+    fwd_finish<T, G, NV, ALIGNED>(a, p, gl, gi, B, red_m, red_l);
+}
+
+template <typename T, int G, int NV, bool ALIGNED>
+__global__ void __launch_bounds__(kThreads, 2) bwd_row_kernel(const BwdArgs a)
+{
+    using namespace rowmath;
+    constexpr int GPC = kThreads / G;
+    constexpr int W = G > 32 ? G / 32 : 1;
+    __shared__ float red[GPC][W];
+    const int gl = threadIdx.x % G;
+    const int gi = threadIdx.x / G;
+    const BRowPos p = bwd_pos<Dt<T>::VEC, ALIGNED>(a, (int64_t)blockIdx.x * GPC + gi);
+    BwdBuf<NV> B;
+    bwd_issue<T, G, NV, ALIGNED>(a, p, gl, B);
+    bwd_finish<T, G, NV, ALIGNED>(a, p, gl, gi, B, red);
+}
+
 template <typename T, int G, int NV, int RPG, bool ALIGNED, bool BWD, typename Args>
 cudaError_t launch_one(const Args &a, cudaStream_t st)
 {
@@ -389,10 +421,17 @@ cudaError_t launch_one(const Args &a, cudaStream_t st)
     cfg.gridDim = dim3((unsigned)blocks);
     cfg.blockDim = dim3(kThreads);
     cfg.stream = st;
-    if constexpr (BWD)
-        return cudaLaunchKernelEx(&cfg, bwd_warp_kernel<T, G, NV, RPG, ALIGNED>, a);
-    else
-        return cudaLaunchKernelEx(&cfg, fwd_warp_kernel<T, G, NV, RPG, ALIGNED>, a);
+    if constexpr (RPG == 1) {
+        if constexpr (BWD)
+            return cudaLaunchKernelEx(&cfg, bwd_row_kernel<T, G, NV, ALIGNED>, a);
+        else
+            return cudaLaunchKernelEx(&cfg, fwd_row_kernel<T, G, NV, ALIGNED>, a);
+    } else {
+        if constexpr (BWD)
+            return cudaLaunchKernelEx(&cfg, bwd_warp_kernel<T, G, NV, RPG, ALIGNED>, a);
+        else
+            return cudaLaunchKernelEx(&cfg, fwd_warp_kernel<T, G, NV, RPG, ALIGNED>, a);
+    }
 }
 
 // (lanes per row, vectors per lane per row, rows per lane group), smallest

@@ -16,7 +16,8 @@ FWD_ATOL = {torch.float32: 2e-6, torch.float16: 1e-3, torch.bfloat16: 8e-3}
 # unit roundoff of the stored dtype, used by the backward bound
 UNIT = {torch.float32: 2.0 ** -24, torch.float16: 2.0 ** -11, torch.bfloat16: 2.0 ** -8}
 
-PATHS = {"auto": sms.SMS_PATH_AUTO, "warp": sms.SMS_PATH_WARP, "cta": sms.SMS_PATH_CTA, "online": sms.SMS_PATH_ONLINE}
+PATHS = {"auto": sms.SMS_PATH_AUTO, "warp": sms.SMS_PATH_WARP, "cta": sms.SMS_PATH_CTA, "online": sms.SMS_PATH_ONLINE,
+         "stream": sms.SMS_PATH_STREAM, "ring": sms.SMS_PATH_RING}
 
 
 @contextlib.contextmanager

@@ -108,8 +108,10 @@ def test_status_strings_and_forced_path():
     prev = sms.sms_set_forced_path(sms.SMS_PATH_CTA)
     assert sms.sms_set_forced_path(sms.SMS_PATH_ONLINE) == sms.SMS_PATH_CTA
     assert sms.sms_set_forced_path(prev) == sms.SMS_PATH_ONLINE
+    assert sms.sms_set_forced_path(sms.SMS_PATH_STREAM) == sms.SMS_PATH_AUTO
+    assert sms.sms_set_forced_path(sms.SMS_PATH_AUTO) == sms.SMS_PATH_STREAM
     with pytest.raises(ValueError):
-        sms.sms_set_forced_path(4)
+        sms.sms_set_forced_path(6)
     with pytest.raises(ValueError):
         sms.sms_set_forced_path(9)
     prev = sms.sms_set_grid_limit(3)
@@ -119,18 +121,26 @@ def test_status_strings_and_forced_path():
 
 
 def test_dispatcher_thresholds():
-    W, C, O = sms.SMS_PATH_WARP, sms.SMS_PATH_CTA, sms.SMS_PATH_ONLINE
+    W, C, O, R = sms.SMS_PATH_WARP, sms.SMS_PATH_CTA, sms.SMS_PATH_ONLINE, sms.SMS_PATH_RING
     for dt in (0, 1, 2):
-        assert sms.sms_select_path(1000, 64, dt) == W
+        sixteen = dt != 0
+        S = sms.SMS_PATH_STREAM
+        assert sms.sms_select_path(1000, 64, dt) == (W if sixteen else S)  # short fp32 rows: prefetching groups
+        assert sms.sms_select_path(1000, 512, dt) == (W if sixteen else S)
+        assert sms.sms_select_path(1000, 513, dt) == W
+        assert sms.sms_select_path(1000, 64, dt, True) == W
         assert sms.sms_select_path(1000, 1024, dt) == W
         assert sms.sms_select_path(1000, 4096, dt) == W
         assert sms.sms_select_path(1000, 8192, dt) == W
         # aligned 16-bit forward rows stay register-resident up to 256 lanes x 8 vectors
-        assert sms.sms_select_path(1000, 16384, dt) == (C if dt == 0 else W)
-        assert sms.sms_select_path(1000, 16384, dt, True) == C
-        assert sms.sms_select_path(1000, 16392, dt) == O  # beyond the staged path's forward registers
-        assert sms.sms_select_path(1000, 10248, dt) == (C if dt == 0 else W)  # 16-bit: 1281 vectors, 256 x 6
+        assert sms.sms_select_path(1000, 16384, dt) == (W if sixteen else C)
+        assert sms.sms_select_path(1000, 10248, dt) == (W if sixteen else C)  # 16-bit: 1281 vectors, 256 x 6
         assert sms.sms_select_path(1000, 10249, dt) == C  # unaligned 16-bit rows stop at 256 x 5 vectors
+        assert sms.sms_select_path(1000, 16392, dt) == O  # beyond the staged path's forward registers
+        # backward: 16-bit rows too wide for registers go to the bulk-copy rings (up to 2048 vectors)
+        assert sms.sms_select_path(1000, 8192, dt, True) == (W if sixteen else C)
+        assert sms.sms_select_path(1000, 16384, dt, True) == (R if sixteen else C)
+        assert sms.sms_select_path(1000, 16392, dt, True) == (C if sixteen else O)
         assert sms.sms_select_path(1000, 1 << 20, dt) == O
         assert sms.sms_select_path(1000, 1 << 20, dt, True) == O
     assert sms.sms_select_path(1, 0, 0) == -1

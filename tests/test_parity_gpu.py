@@ -24,7 +24,7 @@ pytestmark = pytest.mark.gpu
 DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 WIDTHS = [1, 2, 3, 5, 8, 13, 16, 31, 33, 64, 100, 127, 128, 129, 255, 256, 500, 512, 513, 1000, 1023, 1024,
           1025, 1500, 2047, 2048, 2049, 3000, 4096, 4099, 5000, 8192, 12345, 16384, 20000, 32768, 40000]
-ROWS_FOR_PATH = {"auto": 300, "warp": 37, "cta": 1000, "online": 301}
+ROWS_FOR_PATH = {"auto": 300, "warp": 37, "stream": 2500, "ring": 3000, "cta": 1000, "online": 301}
 
 
 def _wl(S, dt, rows, mask="SS", causal=False, B=1, Hh=1, seed=7, values="normal", fill=-math.inf):
@@ -53,7 +53,7 @@ def _run_fwd(w, inp, path):
     return y
 
 
-@pytest.mark.parametrize("path", ["auto", "warp", "cta", "online"])
+@pytest.mark.parametrize("path", ["auto", "warp", "stream", "ring", "cta", "online"])
 @pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("S", WIDTHS)
 def test_forward_widths(S, dt, path):
@@ -64,7 +64,7 @@ def test_forward_widths(S, dt, path):
     H.check_forward(H.to_np64(y), H.oracle_forward(inp, w), DTYPES[dt], f"{path} S={S} {dt} causal={w.is_causal}")
 
 
-@pytest.mark.parametrize("path", ["auto", "warp", "cta", "online"])
+@pytest.mark.parametrize("path", ["auto", "warp", "stream", "ring", "cta", "online"])
 @pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("kind", ["none", "SS", "B1SS", "BHSS"])
 @pytest.mark.parametrize("causal", [False, True])
@@ -80,7 +80,7 @@ def test_forward_mask_layouts(S, causal, kind, dt, path):
     H.check_forward(H.to_np64(y), H.oracle_forward(inp, w), DTYPES[dt], f"{path} {kind} causal={causal} S={S} {dt}")
 
 
-@pytest.mark.parametrize("path", ["auto", "warp", "cta", "online"])
+@pytest.mark.parametrize("path", ["auto", "warp", "stream", "ring", "cta", "online"])
 @pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("S", [1, 3, 31, 64, 129, 1000, 1024, 2048, 2049, 4099, 8192, 16384, 20000])
 def test_backward_widths(S, dt, path):
@@ -129,7 +129,7 @@ def test_workload_scaled_forward_backward(name):
     assert rel <= tol, f"{name}: end-to-end backward relative error {rel:.3e}"
 
 
-@pytest.mark.parametrize("path", ["cta", "online"])
+@pytest.mark.parametrize("path", ["stream", "ring", "cta", "online"])
 @pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("S,kind,causal", [(8, "BHSS", True), (100, "B1SS", True), (1000, "SS", False),
                                            (2049, "B1SS", True), (4099, "SS", True)])
@@ -170,7 +170,7 @@ def test_fully_masked_rows_give_zero():
             w = _wl(S, dt, 4, mask="SS", values="zero")
             inp = H.make(w)
             inp["mask"][1, :] = -math.inf  # row 1 reads mask row 1: every key masked
-            for path in ("auto", "warp", "cta", "online"):
+            for path in ("auto", "warp", "stream", "ring", "cta", "online"):
                 with H.forced_path(path):
                     try:
                         y = H.raw_forward(inp, w)
@@ -184,7 +184,7 @@ def test_fully_masked_rows_give_zero():
                 assert torch.all(dx[1] == 0) and torch.all(torch.isfinite(dx))
 
 
-@pytest.mark.parametrize("path", ["warp", "cta", "online"])
+@pytest.mark.parametrize("path", ["warp", "stream", "ring", "cta", "online"])
 def test_in_place(path):
     for dt, S in (("f32", 1000), ("bf16", 4099), ("f16", 1024)):
         w = _wl(S, dt, 257, causal=True)
