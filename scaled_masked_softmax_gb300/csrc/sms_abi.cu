@@ -108,10 +108,12 @@ int pick_path(int forced, int64_t cols, int dtype, bool aligned, bool bwd, bool 
     //    rings keep enough of them in flight (registers do not): ring;
     //  * short aligned fp32 forward rows: the persistent prefetching groups;
     //  * otherwise register-resident lane groups while a row fits them;
-    //  * 16-bit backward rows too wide for registers: ring, then the staged
-    //    CTA path while a row fits its registers; beyond that, stream twice.
+    //  * 16-bit backward rows too wide for registers, or wide and starting
+    //    mid-vector: ring, then the staged CTA path while a row fits its
+    //    registers; beyond that, stream twice.
     if (!bwd && causal && aligned && ring_fits(cols, dtype, aligned)) return SMS_PATH_RING;
     if (!bwd && dtype == SMS_F32 && aligned && cols <= 512) return SMS_PATH_STREAM;
+    if (bwd && dtype != SMS_F32 && !aligned && cols > 2048 && ring_fits(cols, dtype, aligned)) return SMS_PATH_RING;
     if (warp_fits(cols, dtype, aligned, bwd)) return SMS_PATH_WARP;
     if (bwd && dtype != SMS_F32 && ring_fits(cols, dtype, aligned)) return SMS_PATH_RING;
     if (bwd ? cta_fits_bwd(cols, dtype, aligned) : cta_fits(cols, dtype, aligned)) return SMS_PATH_CTA;

@@ -307,7 +307,8 @@ cudaError_t launch_ring(const FwdArgs &fa, const BwdArgs &ba, cudaStream_t st)
 constexpr int kStages = 3;
 
 // Rows of up to 2048 vectors: one warp with 1, 2, 4 or 8 vectors per lane,
-// then 2, 4 or 8 warps with 8.
+// then groups of 2 to 8 warps with 6 or 8 (the 6-vector groups keep rows
+// just past a power of two, 4099 say, from doubling their stage and group).
 template <typename T, bool MB, bool ALIGNED, bool BWD>
 cudaError_t launch_t(const FwdArgs &fa, const BwdArgs &ba, cudaStream_t st)
 {
@@ -316,8 +317,8 @@ cudaError_t launch_t(const FwdArgs &fa, const BwdArgs &ba, cudaStream_t st)
     const int64_t need = (cols + VEC - 1) / VEC + (ALIGNED ? 0 : 1);
 #define SMS_RING(G, NV) \
     if (need <= (G) * (NV)) return launch_ring<T, G, NV, kStages, MB, ALIGNED, BWD>(fa, ba, st);
-    SMS_RING(32, 1) SMS_RING(32, 2) SMS_RING(32, 4) SMS_RING(32, 8) SMS_RING(64, 8) SMS_RING(128, 8)
-    SMS_RING(256, 8)
+    SMS_RING(32, 1) SMS_RING(32, 2) SMS_RING(32, 4) SMS_RING(32, 8) SMS_RING(64, 8) SMS_RING(96, 6)
+    SMS_RING(128, 8) SMS_RING(192, 6) SMS_RING(256, 8)
 #undef SMS_RING
     return cudaErrorNotSupported;
 }

@@ -380,9 +380,12 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_warp_kernel(const BwdArgs a)
 
 // One row per lane group: the shared row math of sms_rowmath.cuh (one
 // switch per row realigns a misaligned mask, bounds are tested once per row,
-// paired elements use the packed fp32x2 forms).
+// paired elements use the packed fp32x2 forms).  fp32 rows are held in at
+// most 80 registers, three CTAs per multiprocessor: measured faster than two
+// CTAs with more registers (S=4099: 66% against 43% of the copy rate; S=1024:
+// +5%); the 16-bit forms gain nothing from it and would spill.
 template <typename T, int G, int NV, bool ALIGNED>
-__global__ void __launch_bounds__(kThreads, 2) fwd_row_kernel(const FwdArgs a)
+__global__ void __launch_bounds__(kThreads, Dt<T>::VEC == 4 ? 3 : 2) fwd_row_kernel(const FwdArgs a)
 {
     using namespace rowmath;
     constexpr int GPC = kThreads / G;
