@@ -509,7 +509,8 @@ def main():
     sms.sms_set_forced_path(path_code[args.path])
     res, (w, inp, _y, _dx) = run_ours(args, rank, world, device)
     if rank == 0:
-        res["e2e"] = run_e2e(args, w, inp, device, args.e2e_steps)
+        # --e2e-steps 0 (profiling runs only) leaves the host-buffer leg out
+        res["e2e"] = run_e2e(args, w, inp, device, args.e2e_steps) if args.e2e_steps > 0 else None
         if world == 1 and not args.no_cpu_baseline:
             res["cpu_baseline"] = run_cpu_baseline(w, {k: (v.cpu() if isinstance(v, torch.Tensor) else v)
                                                        for k, v in inp.items()}, args.cpu_seconds)
