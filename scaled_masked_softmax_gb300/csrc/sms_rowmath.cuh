@@ -117,7 +117,9 @@ template <int NV, bool ALIGNED> struct FwdBuf {
 };
 
 // Issue every 16-byte load of row p: x, then the mask (two aligned mask
-// vectors per x vector when the mask row is misaligned relative to x).
+// vectors per x vector when the mask row is misaligned relative to x).  The
+// per-vector bounds tests of rows at the ends of the buffers live in their
+// own loop: one warp-uniform branch per row keeps them out of the common path.
 template <typename T, int G, int NV, bool ALIGNED>
 __device__ __forceinline__ void fwd_issue(const FwdArgs &a, const RowPos &p, int gl, FwdBuf<NV, ALIGNED> &B)
 {
@@ -126,22 +128,29 @@ __device__ __forceinline__ void fwd_issue(const FwdArgs &a, const RowPos &p, int
     const T *mk = reinterpret_cast<const T *>(a.mask) + p.mA;
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
-        const int vi = k * G + gl;
-        const int j0 = vi * VEC - p.xoff;
         B.x[k] = make_uint4(0, 0, 0, 0);
         B.m[k] = make_uint4(0, 0, 0, 0);
         if constexpr (!ALIGNED) B.m2[k] = make_uint4(0, 0, 0, 0);
-        if (j0 < p.limit) {
-            if constexpr (ALIGNED) {
-                B.x[k] = ld_stream(xs + vi * VEC);
-                if (a.mask) B.m[k] = ld_keep(mk + vi * VEC);
-            } else if (p.fast) {
+    }
+    if (ALIGNED || p.fast) {
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int vi = k * G + gl;
+            if (vi * VEC - p.xoff < p.limit) {
                 B.x[k] = ld_stream(xs + vi * VEC);
                 if (a.mask) {
                     B.m[k] = ld_keep(mk + vi * VEC);
-                    if (p.msh) B.m2[k] = ld_keep(mk + vi * VEC + VEC);
+                    if constexpr (!ALIGNED) {
+                        if (p.msh) B.m2[k] = ld_keep(mk + vi * VEC + VEC);
+                    }
                 }
-            } else {  // a row at an end of x or of the mask buffer
+            }
+        }
+    } else if constexpr (!ALIGNED) {  // a row at an end of x or of the mask buffer
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int vi = k * G + gl;
+            if (vi * VEC - p.xoff < p.limit) {
                 if (p.xb + (int64_t)(vi + 1) * VEC <= a.x_total) B.x[k] = ld_stream(xs + vi * VEC);
                 if (a.mask) {
                     const int64_t mb = p.mA + (int64_t)vi * VEC;
@@ -177,46 +186,14 @@ __device__ __forceinline__ void realign(uint4 (&m)[NV], const uint4 (&m2)[NV], i
     }
 }
 
-// Scores of vector slot k of row p (x and mask already realigned on the fast
-// path); returns them in s and folds them into the running max.
-template <typename T, int G, int NV, bool ALIGNED>
-__device__ __forceinline__ void fwd_scores(const FwdArgs &a, const RowPos &p, int gl, int k,
-                                           const FwdBuf<NV, ALIGNED> &B, float (&s)[Dt<T>::VEC], float &mx)
+// Scores s = x*scale + mask of one vector (-inf outside [0, limit)), folded
+// into the running max.
+template <int VEC>
+__device__ __forceinline__ void score_vec(const float (&xv)[VEC], const float (&mv)[VEC], float scale, int j0,
+                                          int limit, float (&s)[VEC], float &mx)
 {
-    constexpr int VEC = Dt<T>::VEC;
-    const int vi = k * G + gl;
-    const int j0 = vi * VEC - p.xoff;
-    float xv[VEC], mv[VEC];
-    unpack<T>(B.x[k], xv);
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) mv[e] = 0.f;
-    if (ALIGNED || p.fast) {
-        if (a.mask) unpack<T>(B.m[k], mv);
-    } else if constexpr (!ALIGNED) {
-        const T *xs = reinterpret_cast<const T *>(a.x) + p.xb;
-        const T *ms = reinterpret_cast<const T *>(a.mask) + p.mA + p.msh;  // ms[vi*VEC + e]: element j0 + e
-        if (j0 < p.limit) {
-            if (p.xb + (int64_t)(vi + 1) * VEC > a.x_total) {  // last partial vector of the tensor
-#pragma unroll
-                for (int e = 0; e < VEC; ++e)
-                    xv[e] = p.xb + vi * VEC + e < a.x_total ? to_f32<T>(xs[vi * VEC + e]) : 0.f;
-            }
-            if (a.mask) {
-                const int64_t mb = p.mA + (int64_t)vi * VEC;
-                if (mb >= 0 && mb + (p.msh ? 2 : 1) * VEC <= a.mask_total) {
-                    unpack<T>(window<VEC>(B.m[k], B.m2[k], p.msh), mv);
-                } else {  // mask vectors at the ends of the mask buffer: element loads
-#pragma unroll
-                    for (int e = 0; e < VEC; ++e) {
-                        const int j = j0 + e;
-                        mv[e] = (j >= 0 && j < p.limit) ? to_f32<T>(ms[vi * VEC + e]) : 0.f;
-                    }
-                }
-            }
-        }
-    }
-    if (j0 >= 0 && j0 + VEC <= p.limit) {  // interior vector: every element is read
-        const float2 sc = make_float2(a.scale, a.scale);
+    if (j0 >= 0 && j0 + VEC <= limit) {  // interior vector: every element is read
+        const float2 sc = make_float2(scale, scale);
 #pragma unroll
         for (int e = 0; e < VEC; e += 2) {
             const float2 t = __ffma2_rn(make_float2(xv[e], xv[e + 1]), sc, make_float2(mv[e], mv[e + 1]));
@@ -228,10 +205,65 @@ __device__ __forceinline__ void fwd_scores(const FwdArgs &a, const RowPos &p, in
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
             const int j = j0 + e;
-            s[e] = (j >= 0 && j < p.limit) ? fmaf(xv[e], a.scale, mv[e]) : neg_inf();
+            s[e] = (j >= 0 && j < limit) ? fmaf(xv[e], scale, mv[e]) : neg_inf();
             mx = fmaxf(mx, s[e]);
         }
     }
+}
+
+// Scores of vector slot k on the common path: every vector read lies inside
+// x and the mask, and the mask is already realigned.
+template <typename T, int G, int NV, bool ALIGNED>
+__device__ __forceinline__ void fwd_scores(const FwdArgs &a, const RowPos &p, int gl, int k,
+                                           const FwdBuf<NV, ALIGNED> &B, float (&s)[Dt<T>::VEC], float &mx)
+{
+    constexpr int VEC = Dt<T>::VEC;
+    float xv[VEC], mv[VEC];
+    unpack<T>(B.x[k], xv);
+    if (a.mask) {
+        unpack<T>(B.m[k], mv);
+    } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) mv[e] = 0.f;
+    }
+    score_vec<VEC>(xv, mv, a.scale, (k * G + gl) * VEC - p.xoff, p.limit, s, mx);
+}
+
+// Scores of vector slot k of a row at an end of x or of the mask buffer:
+// partial vectors are read element by element.
+template <typename T, int G, int NV>
+__device__ __forceinline__ void fwd_scores_edge(const FwdArgs &a, const RowPos &p, int gl, int k,
+                                                const FwdBuf<NV, false> &B, float (&s)[Dt<T>::VEC], float &mx)
+{
+    constexpr int VEC = Dt<T>::VEC;
+    const int vi = k * G + gl;
+    const int j0 = vi * VEC - p.xoff;
+    float xv[VEC], mv[VEC];
+    unpack<T>(B.x[k], xv);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) mv[e] = 0.f;
+    const T *xs = reinterpret_cast<const T *>(a.x) + p.xb;
+    const T *ms = reinterpret_cast<const T *>(a.mask) + p.mA + p.msh;  // ms[vi*VEC + e]: element j0 + e
+    if (j0 < p.limit) {
+        if (p.xb + (int64_t)(vi + 1) * VEC > a.x_total) {  // last partial vector of the tensor
+#pragma unroll
+            for (int e = 0; e < VEC; ++e)
+                xv[e] = p.xb + vi * VEC + e < a.x_total ? to_f32<T>(xs[vi * VEC + e]) : 0.f;
+        }
+        if (a.mask) {
+            const int64_t mb = p.mA + (int64_t)vi * VEC;
+            if (mb >= 0 && mb + (p.msh ? 2 : 1) * VEC <= a.mask_total) {
+                unpack<T>(window<VEC>(B.m[k], B.m2[k], p.msh), mv);
+            } else {  // mask vectors at the ends of the mask buffer: element loads
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const int j = j0 + e;
+                    mv[e] = (j >= 0 && j < p.limit) ? to_f32<T>(ms[vi * VEC + e]) : 0.f;
+                }
+            }
+        }
+    }
+    score_vec<VEC>(xv, mv, a.scale, j0, p.limit, s, mx);
 }
 
 // exp of every score against the offset c = -m*log2e (in place); returns the
@@ -276,12 +308,17 @@ __device__ __forceinline__ float fwd_reduce(const FwdArgs &a, const RowPos &p, i
 {
     constexpr int VEC = Dt<T>::VEC;
     constexpr int W = G > 32 ? G / 32 : 1;
-    if constexpr (!ALIGNED) {
-        if (a.mask && p.fast) realign<VEC, NV>(B.m, B.m2, p.msh);
-    }
     float mx = neg_inf();
+    if (ALIGNED || p.fast) {
+        if constexpr (!ALIGNED) {
+            if (a.mask) realign<VEC, NV>(B.m, B.m2, p.msh);
+        }
 #pragma unroll
-    for (int k = 0; k < NV; ++k) fwd_scores<T, G, NV, ALIGNED>(a, p, gl, k, B, s[k], mx);
+        for (int k = 0; k < NV; ++k) fwd_scores<T, G, NV, ALIGNED>(a, p, gl, k, B, s[k], mx);
+    } else if constexpr (!ALIGNED) {
+#pragma unroll
+        for (int k = 0; k < NV; ++k) fwd_scores_edge<T, G, NV>(a, p, gl, k, B, s[k], mx);
+    }
 
     if constexpr (G <= 32) {
         mx = group_max<G>(mx);
@@ -432,6 +469,25 @@ __device__ __forceinline__ void bwd_edge(const BwdArgs &a, const BRowPos &p, int
     }
 }
 
+// Row dot contribution of vector slot k: packed for interior vectors,
+// element-wise (within [0, limit)) for the others.
+template <typename T, int VEC>
+__device__ __forceinline__ float dot_slot(const uint4 &y, const uint4 &g, int j0, int limit, float dot)
+{
+    if (j0 >= 0 && j0 + VEC <= limit) return dot_vec<T>(y, g, dot);
+    if (j0 < limit) {
+        float yv[VEC], gv[VEC];
+        unpack<T>(y, yv);
+        unpack<T>(g, gv);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            const int j = j0 + e;
+            if (j >= 0 && j < limit) dot = fmaf(yv[e], gv[e], dot);
+        }
+    }
+    return dot;
+}
+
 // The row dot sum_j y_j dy_j over the group (with the barrier rule of fwd_reduce).
 template <typename T, int G, int NV, bool ALIGNED>
 __device__ __forceinline__ float bwd_reduce(const BwdArgs &a, const BRowPos &p, int gl, int gi, const BwdBuf<NV> &B,
@@ -440,19 +496,22 @@ __device__ __forceinline__ float bwd_reduce(const BwdArgs &a, const BRowPos &p, 
     constexpr int VEC = Dt<T>::VEC;
     constexpr int W = G > 32 ? G / 32 : 1;
     float dot = 0.f;
+    if (ALIGNED || p.fast) {
 #pragma unroll
-    for (int k = 0; k < NV; ++k) {
-        const int vi = k * G + gl;
-        const int j0 = vi * VEC - p.xoff;
-        if (j0 >= 0 && j0 + VEC <= p.limit) {
-            dot = dot_vec<T>(B.y[k], B.g[k], dot);
-        } else if (j0 < p.limit) {
-            float yv[VEC], gv[VEC];
-            bwd_edge<T, G, NV, ALIGNED>(a, p, vi, yv, gv, B, k);
+        for (int k = 0; k < NV; ++k) dot = dot_slot<T, VEC>(B.y[k], B.g[k], (k * G + gl) * VEC - p.xoff, p.limit, dot);
+    } else if constexpr (!ALIGNED) {  // a row at the end of the tensors: partial last vector
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const int j = j0 + e;
-                if (j >= 0 && j < p.limit) dot = fmaf(yv[e], gv[e], dot);
+        for (int k = 0; k < NV; ++k) {
+            const int vi = k * G + gl;
+            const int j0 = vi * VEC - p.xoff;
+            if (j0 < p.limit) {
+                float yv[VEC], gv[VEC];
+                bwd_edge<T, G, NV, ALIGNED>(a, p, vi, yv, gv, B, k);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const int j = j0 + e;
+                    if (j >= 0 && j < p.limit) dot = fmaf(yv[e], gv[e], dot);
+                }
             }
         }
     }
@@ -470,6 +529,31 @@ __device__ __forceinline__ float bwd_reduce(const BwdArgs &a, const BRowPos &p, 
     }
 }
 
+// dx of one vector: packed for interior vectors; element-wise for the rest
+// (+0 beyond [0, limit) and where y == 0).
+template <typename T, int VEC>
+__device__ __forceinline__ void dx_vec(const float (&yv)[VEC], const float (&gv)[VEC], int j0, int limit, float dot,
+                                       float scale, float (&o)[VEC])
+{
+    if (j0 >= 0 && j0 + VEC <= limit) {
+        const float2 nd = make_float2(-dot, -dot), sc = make_float2(scale, scale), z = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int e = 0; e < VEC; e += 2) {
+            const float2 w = __fmul2_rn(__fadd2_rn(make_float2(gv[e], gv[e + 1]), nd), sc);
+            const float2 t = __ffma2_rn(make_float2(yv[e], yv[e + 1]), w, z);  // y == 0 gives +0
+            o[e] = t.x;
+            o[e + 1] = t.y;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            const int j = j0 + e;
+            const bool valid = j >= 0 && j < limit;  // beyond the diagonal (or y == 0): +0
+            o[e] = (!valid || yv[e] == 0.f) ? 0.f : (gv[e] - dot) * scale * yv[e];
+        }
+    }
+}
+
 // dx = (dy - dot) * scale * y for every element the lane holds.
 template <typename T, int G, int NV, bool ALIGNED>
 __device__ __forceinline__ void bwd_store(const BwdArgs &a, const BRowPos &p, int gl, const BwdBuf<NV> &B, float dot)
@@ -478,34 +562,20 @@ __device__ __forceinline__ void bwd_store(const BwdArgs &a, const BRowPos &p, in
     if (p.limit == 0) return;
     T *dxs = reinterpret_cast<T *>(a.dx) + p.xb;
     const int64_t cols = a.cols;
-    const float2 nd = make_float2(-dot, -dot), sc = make_float2(a.scale, a.scale), z = make_float2(0.f, 0.f);
+    const bool fast = ALIGNED || p.fast;
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
         const int vi = k * G + gl;
         const int j0 = vi * VEC - p.xoff;
         if (j0 >= cols) continue;
-        float o[VEC];
-        if (j0 >= 0 && j0 + VEC <= p.limit) {
-            float yv[VEC], gv[VEC];
+        float yv[VEC], gv[VEC], o[VEC];
+        if (fast) {
             unpack<T>(B.y[k], yv);
             unpack<T>(B.g[k], gv);
-#pragma unroll
-            for (int e = 0; e < VEC; e += 2) {
-                const float2 w = __fmul2_rn(__fadd2_rn(make_float2(gv[e], gv[e + 1]), nd), sc);
-                const float2 t = __ffma2_rn(make_float2(yv[e], yv[e + 1]), w, z);  // y == 0 gives +0
-                o[e] = t.x;
-                o[e + 1] = t.y;
-            }
-        } else {
-            float yv[VEC], gv[VEC];
+        } else if constexpr (!ALIGNED) {
             bwd_edge<T, G, NV, ALIGNED>(a, p, vi, yv, gv, B, k);
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const int j = j0 + e;
-                const bool valid = j >= 0 && j < p.limit;  // beyond the diagonal (or y == 0): +0
-                o[e] = (!valid || yv[e] == 0.f) ? 0.f : (gv[e] - dot) * a.scale * yv[e];
-            }
         }
+        dx_vec<T, VEC>(yv, gv, j0, p.limit, dot, a.scale, o);
         if (ALIGNED || (j0 >= 0 && j0 + VEC <= cols)) {
             st_stream(dxs + vi * VEC, pack<T>(o));
         } else {

@@ -383,9 +383,15 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_warp_kernel(const BwdArgs a)
 // paired elements use the packed fp32x2 forms).  fp32 rows are held in at
 // most 80 registers, three CTAs per multiprocessor: measured faster than two
 // CTAs with more registers (S=4099: 66% against 43% of the copy rate; S=1024:
-// +5%); the 16-bit forms gain nothing from it and would spill.
+// +5%).  Not for the 16-bit forms (no gain, they would spill) nor for
+// misaligned fp32 rows of 6 or 8 vectors per lane (they would spill).
+template <typename T, int NV, bool ALIGNED> constexpr int fwd_min_ctas()
+{
+    return (Dt<T>::VEC == 4 && (ALIGNED || NV <= 5)) ? 3 : 2;
+}
+
 template <typename T, int G, int NV, bool ALIGNED>
-__global__ void __launch_bounds__(kThreads, Dt<T>::VEC == 4 ? 3 : 2) fwd_row_kernel(const FwdArgs a)
+__global__ void __launch_bounds__(kThreads, fwd_min_ctas<T, NV, ALIGNED>()) fwd_row_kernel(const FwdArgs a)
 {
     using namespace rowmath;
     constexpr int GPC = kThreads / G;
