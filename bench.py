@@ -483,6 +483,7 @@ def main():
     ap.add_argument("--path", choices=["auto", "warp", "stream", "ring", "cta", "online"], default="auto",
                     help="force one kernel family (tuning); the default lets the dispatcher choose")
     ap.add_argument("--all-paths", action="store_true", help="with --all: every kernel family per workload")
+    ap.add_argument("--only", default=None, help="with --all: comma-separated workload names")
     args = ap.parse_args()
 
     world, rank, local = dist_env()
@@ -525,7 +526,8 @@ def main():
 
         paths = ["auto", "warp", "stream", "ring", "cta", "online"] if args.all_paths else [args.path]
         with open(args.all, "w") as f:
-            for name in workloads.WORKLOADS:
+            names = args.only.split(",") if args.only else list(workloads.WORKLOADS)
+            for name in names:
                 for pth in paths:
                     a2 = argparse.Namespace(**vars(args))
                     a2.workload = name
