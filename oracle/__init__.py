@@ -54,7 +54,7 @@ def _load():
             build()
             lib = ctypes.CDLL(_LIB)
             i64, dbl, vp, i32 = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int
-            lib.oracle_forward.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, dbl, i32, i32, vp]
+            lib.oracle_forward.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, vp, dbl, i32, i32, vp]
             lib.oracle_forward.restype = i32
             lib.oracle_backward.argtypes = [vp, i32, vp, i32, i64, i64, dbl, vp]
             lib.oracle_backward.restype = i32
@@ -114,11 +114,13 @@ def decode(a, dtype_code=None) -> np.ndarray:
 
 def forward(x_rows, cols: int, scale: float, is_causal: bool = False, mask=None,
             mask_stride_b: int = 0, mask_stride_h: int = 0, heads: int = 1,
-            row_index=None, dtype_code=None) -> np.ndarray:
+            row_index=None, dtype_code=None, key_lengths=None) -> np.ndarray:
     """fp64 forward of the rows in ``x_rows`` (any shape with last dim ``cols``).
 
     ``row_index`` gives each row's logical index in the [rows, cols] view (for
     the causal position q = r mod cols and the mask row); default 0..n-1.
+    ``key_lengths`` (one integer per batch b = r // (heads*cols)) keeps only
+    the keys j < key_lengths[b] (clamped to [0, cols]) of each row.
     ``scale`` is used as given (pass the float32 value the kernel sees).
     Returns an fp64 array shaped like x_rows.
     """
@@ -136,11 +138,25 @@ def forward(x_rows, cols: int, scale: float, is_causal: bool = False, mask=None,
         ri = np.ascontiguousarray(np.asarray(row_index, dtype=np.int64).reshape(-1))
         if ri.size != n:
             raise ValueError("row_index length must equal the number of rows")
+    la = None
+    if key_lengths is not None:
+        try:
+            import torch
+
+            if isinstance(key_lengths, torch.Tensor):
+                key_lengths = key_lengths.detach().to("cpu").numpy()
+        except ImportError:  # pragma: no cover
+            pass
+        la = np.ascontiguousarray(np.asarray(key_lengths, dtype=np.int64).clip(-(2 ** 31), 2 ** 31 - 1)
+                                  .astype(np.int32).reshape(-1))
+        last = (int(ri.max()) if ri is not None and ri.size else n - 1) // (cols * heads)
+        if la.size <= last:
+            raise ValueError("key_lengths has fewer entries than the rows' batches")
     y = np.empty((n, cols), dtype=np.float64)
     rc = _load().oracle_forward(
         xa.ctypes.data, n, None if ri is None else ri.ctypes.data, cols,
         None if ma is None else ma.ctypes.data, mask_stride_b, mask_stride_h, heads,
-        float(scale), int(bool(is_causal)), code, y.ctypes.data)
+        None if la is None else la.ctypes.data, float(scale), int(bool(is_causal)), code, y.ctypes.data)
     if rc != 0:
         raise ValueError("oracle_forward rejected its arguments")
     return y.reshape(xa.shape)

@@ -26,6 +26,11 @@
  *     dot  = sum_j dy_j * y_j
  *     dx_j = (dy_j - dot) * y_j * scale           (the mask gets no gradient)
  *
+ * Key lengths (optional): row r of batch b keeps only the keys j < L_b,
+ * L_b = lengths[b] clamped to [0, cols]; s_j = -inf for j >= L_b.  This is the
+ * key-padding mask of [P3 §2.1] written as lengths; [P2 §2.2] makes a padded
+ * key's score -inf.  It is applied with the causal override, after the mask.
+ *
  * Mask broadcasting: row r = ((b*heads) + h)*cols + q of the [rows, cols] view
  * reads the additive mask row starting at element
  *     b*mask_stride_b + h*mask_stride_h + q*cols
@@ -134,12 +139,13 @@ void oracle_set_num_threads(int n)
  *   row_index logical row id of each of those rows in the [rows, cols] view
  *             (fixes q, b, h); NULL means 0..n_rows-1
  *   mask      NULL for no mask, else additive mask values of `dtype`
+ *   lengths   NULL, or the per-batch key lengths (int32, one per batch b)
  *   y         n_rows x cols fp64 output
  * Returns 0, or -1 for an argument it cannot interpret.
  */
 int oracle_forward(const void *x_rows, int64_t n_rows, const int64_t *row_index, int64_t cols,
                    const void *mask, int64_t mask_stride_b, int64_t mask_stride_h, int64_t heads,
-                   double scale, int is_causal, int dtype, double *y)
+                   const int32_t *lengths, double scale, int is_causal, int dtype, double *y)
 {
     if (!x_rows || !y || n_rows < 0 || cols <= 0 || heads <= 0 || !dtype_ok(dtype))
         return -1;
@@ -152,12 +158,22 @@ int oracle_forward(const void *x_rows, int64_t n_rows, const int64_t *row_index,
         int64_t b = r / (cols * heads);
         double *s = y + i * cols; /* the output row holds the scores first */
         int64_t j;
+        int64_t kept = cols; /* keys j < kept survive the key-length mask */
+        if (lengths) {
+            kept = lengths[b];
+            if (kept < 0)
+                kept = 0;
+            if (kept > cols)
+                kept = cols;
+        }
 
         for (j = 0; j < cols; j++) {
             double v = load_elem(x_rows, i * cols + j, dtype) * scale;
             if (mask)
                 v += load_elem(mask, b * mask_stride_b + h * mask_stride_h + q * cols + j, dtype);
             if (is_causal && j > q)
+                v = -INFINITY;
+            if (j >= kept)
                 v = -INFINITY;
             s[j] = v;
         }

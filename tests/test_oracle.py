@@ -44,7 +44,8 @@ def test_forward_closed_forms(case):
         mask = _arr(case["mask"], dt) if "mask" in case else None
         scale = float(np.float32(_val(case["scale"])))
         y = oracle.forward(x, case["cols"], scale, case["is_causal"], mask,
-                           case.get("mask_stride_b", 0), case.get("mask_stride_h", 0), case.get("heads", 1))
+                           case.get("mask_stride_b", 0), case.get("mask_stride_h", 0), case.get("heads", 1),
+                           key_lengths=case.get("key_lengths"))
         want = _arr(case["y"], torch.float64).numpy()
         np.testing.assert_allclose(y, want, rtol=0, atol=1e-12, err_msg=f"{case['name']} {dn}")
         # masked entries are exactly zero, not merely small
@@ -277,3 +278,55 @@ def test_oracle_rejects_bad_arguments():
         oracle.forward(np.zeros((2, 3)), 4, 1.0)
     with pytest.raises(ValueError):
         oracle.backward(np.zeros((2, 3)), np.zeros((2, 4)), 3, 1.0)
+
+
+# ------------------------------------------------------------ key lengths ---
+
+@pytest.mark.parametrize("dt", [torch.float64, torch.float32, torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_lengths_equal_an_expanded_minus_inf_mask(dt, causal):
+    """The key-length path and the additive-mask path of the oracle are two
+    different mechanisms; a [B,1,S,S] mask of 0 below L_b and -inf from L_b
+    on must give the same result bit for bit."""
+    g = torch.Generator().manual_seed(31)
+    B, H, S = 3, 2, 37
+    x = (torch.randn(B * H * S, S, generator=g, dtype=torch.float64) * 8).to(dt)
+    L = torch.tensor([0, 17, 37], dtype=torch.int32)
+    mask = torch.zeros(B, 1, S, S, dtype=torch.float64)
+    for b in range(B):
+        mask[b, :, :, int(L[b]):] = -math.inf
+    y_len = oracle.forward(x, S, 0.125, causal, heads=H, key_lengths=L)
+    y_mask = oracle.forward(x, S, 0.125, causal, mask.to(dt), S * S, 0, H)
+    assert np.array_equal(y_len, y_mask)
+
+
+@pytest.mark.parametrize("dt", [torch.float64, torch.float32, torch.float16, torch.bfloat16])
+def test_key_lengths_match_library_softmax(dt):
+    """Rows with at least one kept key against torch.softmax of the scores
+    with the padded keys filled with -inf."""
+    g = torch.Generator().manual_seed(37)
+    B, H, S = 4, 3, 50
+    x = (torch.randn(B * H * S, S, generator=g, dtype=torch.float64) * 8).to(dt)
+    L = torch.tensor([1, 25, 49, 50], dtype=torch.int32)
+    y = oracle.forward(x, S, 0.125, False, heads=H, key_lengths=L)
+    s = x.to(torch.float64) * float(np.float32(0.125))
+    b = torch.arange(B * H * S) // (H * S)
+    pad = torch.arange(S)[None, :] >= L.to(torch.int64)[b][:, None]
+    ref = torch.softmax(s.masked_fill(pad, -math.inf), dim=-1).numpy()
+    np.testing.assert_allclose(y, ref, rtol=0, atol=1e-14)
+    assert np.all(y[pad.numpy()] == 0.0)
+
+
+def test_key_lengths_with_row_index_and_clamping():
+    """A row sample by row_index picks each row's batch; lengths below 0 or
+    above cols are clamped."""
+    g = torch.Generator().manual_seed(41)
+    B, H, S = 3, 2, 9
+    x = torch.randn(B * H * S, S, generator=g, dtype=torch.float64)
+    L = torch.tensor([-5, 4, 100], dtype=torch.int32)
+    full = oracle.forward(x, S, 1.0, True, heads=H, key_lengths=L)
+    idx = np.array([53, 0, 20, 36, 17], dtype=np.int64)
+    part = oracle.forward(x[torch.as_tensor(idx)], S, 1.0, True, heads=H, key_lengths=L, row_index=idx)
+    assert np.array_equal(part, full[idx])
+    assert np.all(full[: H * S] == 0.0)  # L = -5 -> 0: every key of batch 0 masked
+    np.testing.assert_array_equal(full[2 * H * S:], oracle.forward(x[2 * H * S:], S, 1.0, True))  # L = 100 -> S
