@@ -75,11 +75,25 @@ def _traffic_record(workload: str, kernel: str):
     return rec.get("bytes_per_launch")
 
 
-def fwd_bytes(w, inp) -> int:
+def _kept_elems(w, inp) -> float:
+    """Elements a key-length run reads per tensor: min(L_b, q + 1 under causal) per row."""
+    L = inp["key_lengths"].to("cpu", torch.float64).clamp(0, w.cols)
+    r = torch.arange(w.rows, dtype=torch.float64)
+    b = torch.div(r, w.H * w.cols, rounding_mode="floor").long()
+    lim = L[b]
+    if w.is_causal:
+        lim = torch.minimum(lim, torch.remainder(r, w.cols) + 1)
+    return float(lim.sum())
+
+
+def fwd_bytes(w, inp, lengths=False) -> int:
     """Algorithmic bytes of one forward: x read (only j <= q under causal),
-    unique mask bytes read (same causal rule), y written in full."""
+    unique mask bytes read (same causal rule), y written in full.  With key
+    lengths: x read only below min(L_b, q + 1), the lengths array, no mask."""
     eb = w.elem_bytes
     rows, S = w.rows, w.cols
+    if lengths:
+        return int(_kept_elems(w, inp) * eb + inp["key_lengths"].numel() * 4 + rows * S * eb)
     if w.is_causal:
         # row q reads q+1 elements
         q = torch.arange(rows, dtype=torch.float64) % S
@@ -99,11 +113,13 @@ def fwd_bytes(w, inp) -> int:
     return int(x_read + mask_read + rows * S * eb)
 
 
-def bwd_bytes(w) -> int:
+def bwd_bytes(w, inp=None, lengths=False) -> int:
     """Algorithmic bytes of one backward: y and dy read (only j <= q with the
-    causal hint), dx written in full."""
+    causal hint, only below L_b with key lengths), dx written in full."""
     eb = w.elem_bytes
     rows, S = w.rows, w.cols
+    if lengths:
+        return int(_kept_elems(w, inp) * 2 * eb + inp["key_lengths"].numel() * 4 + rows * S * eb)
     if w.is_causal:
         q = torch.arange(rows, dtype=torch.float64) % S
         read = float((q + 1).sum()) * 2 * eb
@@ -222,19 +238,32 @@ def run_ours(args, rank, world, device):
     mnum = 0 if mask is None else mask.numel()
     L = sms.binding.lib()
 
+    use_len = bool(getattr(args, "lengths", False))
+    if use_len and inp["key_lengths"] is None:
+        raise RuntimeError(f"--lengths: workload {w.name} has no key-padding mask")
+    lptr = inp["key_lengths"].data_ptr() if use_len else None
+
     def fwd():
-        rc = L.sms_forward(x.data_ptr(), mptr, mnum, inp["mask_stride_b"], inp["mask_stride_h"], inp["heads"],
-                           y.data_ptr(), w.rows, w.cols, w.scale, int(w.is_causal), dt, st)
+        if use_len:
+            rc = L.sms_forward_lengths(x.data_ptr(), lptr, w.H, y.data_ptr(), w.rows, w.cols, w.scale,
+                                       int(w.is_causal), dt, st)
+        else:
+            rc = L.sms_forward(x.data_ptr(), mptr, mnum, inp["mask_stride_b"], inp["mask_stride_h"], inp["heads"],
+                               y.data_ptr(), w.rows, w.cols, w.scale, int(w.is_causal), dt, st)
         if rc:
             raise RuntimeError(sms.sms_last_error())
 
     def bwd():
-        rc = L.sms_backward(y.data_ptr(), dy.data_ptr(), dx.data_ptr(), w.rows, w.cols, w.scale, int(w.is_causal),
-                            dt, st)
+        if use_len:
+            rc = L.sms_backward_lengths(y.data_ptr(), dy.data_ptr(), dx.data_ptr(), lptr, w.H, w.rows, w.cols,
+                                        w.scale, int(w.is_causal), dt, st)
+        else:
+            rc = L.sms_backward(y.data_ptr(), dy.data_ptr(), dx.data_ptr(), w.rows, w.cols, w.scale,
+                                int(w.is_causal), dt, st)
         if rc:
             raise RuntimeError(sms.sms_last_error())
 
-    fb, bb = fwd_bytes(w, inp), bwd_bytes(w)
+    fb, bb = fwd_bytes(w, inp, use_len), bwd_bytes(w, inp, use_len)
     step_bytes = fb + bb
     working_set = (x.numel() * 4 * x.element_size()) + (0 if mask is None else mask.numel() * mask.element_size())
     flush = working_set < 2 * L2_BYTES
@@ -305,7 +334,9 @@ def run_ours(args, rank, world, device):
         "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": DTYPE_NAME[x.dtype], "data": "synthetic (seeded, see workloads.py)",
         "config": {"workload": w.name, "shape": [w.B, w.H, w.S, w.S] if w.rows_override is None else [w.rows, w.S],
-                   "rows": w.rows, "cols": w.cols, "mask": w.mask, "is_causal": w.is_causal,
+                   "rows": w.rows, "cols": w.cols,
+                   "mask": ("key lengths int32 [B] (sms_forward_lengths)" if use_len else w.mask),
+                   "is_causal": w.is_causal,
                    "step": "forward + backward (dy ~ N(0,1))", "scale": w.scale,
                    "l2": ("flushed between steps (2x L2 write), step = kernel time" if flush
                           else "inputs larger than L2, no flush"),
@@ -484,6 +515,8 @@ def main():
                     help="force one kernel family (tuning); the default lets the dispatcher choose")
     ap.add_argument("--all-paths", action="store_true", help="with --all: every kernel family per workload")
     ap.add_argument("--only", default=None, help="with --all: comma-separated workload names")
+    ap.add_argument("--lengths", action="store_true",
+                    help="key-padding workloads through the key-length entry points instead of the [B,1,S,S] mask")
     args = ap.parse_args()
 
     world, rank, local = dist_env()

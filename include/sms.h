@@ -123,6 +123,43 @@ SMS_API int sms_forward(const void *x, const void *mask, int64_t mask_numel, int
 SMS_API int sms_backward(const void *y, const void *dy, void *dx, int64_t rows, int64_t cols, float scale,
                  int is_causal_hint, int dtype, void *stream);
 
+/*
+ * Key-padding forward with per-batch lengths.  The second article
+ * (pnsm.cn/news/1983787) lists key-padding masks among the masks to fuse
+ * (§2.1 input contract, §4.4 and §5 on fusing several mask kinds), and the
+ * page "用CUDA自定义融合Softmax算子并封装进PyTorch" §2.2 defines a padded key as
+ * one whose score is -inf.  Here the padding is given by lengths instead of an
+ * additive [B,1,S,S] tensor: row r of batch b = r / (heads * cols) keeps the
+ * keys j < L_b, L_b = lengths[b] clamped to [0, cols]:
+ *       s_j = x_j * scale            for j < L_b,   s_j = -inf  for j >= L_b
+ *       s_j = -inf if is_causal and j > q;  y as in sms_forward
+ * which equals sms_forward with a [B,1,S,S] mask holding 0 for j < L_b and
+ * -inf beyond.  A row with no kept key (L_b = 0) gives y = 0.  x is never
+ * read at j >= L_b, and no mask tensor is read at all.
+ *   lengths  device int32 array, 4-byte aligned, at least
+ *            ceil(rows / (heads * cols)) entries (one per batch); the caller
+ *            keeps it unchanged until the kernel has run
+ *   heads    H of the [B,H,S,S] view (>= 1): locates b
+ *   other arguments as sms_forward (x, y, rows, cols, scale, is_causal, dtype,
+ *   stream); y may equal x, and must not overlap lengths.
+ * Errors as sms_forward, plus SMS_ERR_INVALID_ARG for a NULL or unaligned
+ * lengths pointer.
+ */
+SMS_API int sms_forward_lengths(const void *x, const int32_t *lengths, int64_t heads, void *y, int64_t rows,
+                                int64_t cols, float scale, int is_causal, int dtype, void *stream);
+
+/*
+ * Backward of sms_forward_lengths: sms_backward with a key-length hint.  The
+ * caller promises y[r, j] == 0 for j >= L_b (true for a forward run with the
+ * same lengths); the kernels skip reading y and dy there and write dx = +0,
+ * as under is_causal_hint (which may be combined with it).  The result equals
+ * sms_backward's up to the rounding of the row sum's summation order.
+ * lengths and heads as in sms_forward_lengths; dx must not overlap lengths.
+ */
+SMS_API int sms_backward_lengths(const void *y, const void *dy, void *dx, const int32_t *lengths, int64_t heads,
+                                 int64_t rows, int64_t cols, float scale, int is_causal_hint, int dtype,
+                                 void *stream);
+
 /* Static description of a status code. */
 SMS_API const char *sms_status_string(int status);
 

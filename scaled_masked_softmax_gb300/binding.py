@@ -24,6 +24,8 @@ _i64, _i32, _f32, _vp, _cp = ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctype
 SIGNATURES = {
     "sms_forward": (_i32, [_vp, _vp, _i64, _i64, _i64, _i64, _vp, _i64, _i64, _f32, _i32, _i32, _vp]),
     "sms_backward": (_i32, [_vp, _vp, _vp, _i64, _i64, _f32, _i32, _i32, _vp]),
+    "sms_forward_lengths": (_i32, [_vp, _vp, _i64, _vp, _i64, _i64, _f32, _i32, _i32, _vp]),
+    "sms_backward_lengths": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _f32, _i32, _i32, _vp]),
     "sms_status_string": (_cp, [_i32]),
     "sms_last_error": (_cp, []),
     "sms_set_forced_path": (_i32, [_i32]),
@@ -80,6 +82,15 @@ def sms_forward(x, mask, mask_numel, mask_stride_b, mask_stride_h, heads, y, row
 
 def sms_backward(y, dy, dx, rows, cols, scale, is_causal_hint, dtype, stream) -> None:
     _check(lib().sms_backward(y, dy, dx, rows, cols, scale, int(bool(is_causal_hint)), dtype, stream))
+
+
+def sms_forward_lengths(x, lengths, heads, y, rows, cols, scale, is_causal, dtype, stream) -> None:
+    _check(lib().sms_forward_lengths(x, lengths, heads, y, rows, cols, scale, int(bool(is_causal)), dtype, stream))
+
+
+def sms_backward_lengths(y, dy, dx, lengths, heads, rows, cols, scale, is_causal_hint, dtype, stream) -> None:
+    _check(lib().sms_backward_lengths(y, dy, dx, lengths, heads, rows, cols, scale, int(bool(is_causal_hint)), dtype,
+                                      stream))
 
 
 def sms_set_forced_path(path: int) -> int:

@@ -184,45 +184,59 @@ int sms_select_path(int64_t rows, int64_t cols, int dtype, int is_backward)
     return pick_path(SMS_PATH_AUTO, cols, dtype, aligned, is_backward != 0, false);
 }
 
-int sms_forward(const void *x, const void *mask, int64_t mask_numel, int64_t mask_stride_b, int64_t mask_stride_h,
-                int64_t heads, void *y, int64_t rows, int64_t cols, float scale, int is_causal, int dtype,
-                void *stream)
+}  // extern "C"
+
+namespace {
+
+// Validation and dispatch shared by sms_forward and sms_forward_lengths
+// (`who` names the entry point in error messages).
+int forward_impl(const char *who, const void *x, const void *mask, int64_t mask_numel, int64_t mask_stride_b,
+                 int64_t mask_stride_h, int64_t heads, const int32_t *lengths, void *y, int64_t rows, int64_t cols,
+                 float scale, int is_causal, int dtype, void *stream)
 {
     t_err[0] = '\0';
-    if (dtype < SMS_F32 || dtype > SMS_BF16) return fail(SMS_ERR_INVALID_ARG, "sms_forward: unknown dtype %d", dtype);
-    if (rows < 0) return fail(SMS_ERR_INVALID_ARG, "sms_forward: rows < 0");
+    if (dtype < SMS_F32 || dtype > SMS_BF16) return fail(SMS_ERR_INVALID_ARG, "%s: unknown dtype %d", who, dtype);
+    if (rows < 0) return fail(SMS_ERR_INVALID_ARG, "%s: rows < 0", who);
     if (rows == 0 && cols > 0) {  // empty problem: nothing is read, pointers may be NULL
         t_last_path = SMS_PATH_AUTO;
         return SMS_OK;
     }
-    if (!x || !y) return fail(SMS_ERR_INVALID_ARG, "sms_forward: x and y must not be NULL");
-    if (cols <= 0 || cols > kMaxCols) return fail(SMS_ERR_INVALID_ARG, "sms_forward: cols must be in [1, 2^30]");
-    if (rows > 0 && rows > kMaxElems / cols) return fail(SMS_ERR_INVALID_ARG, "sms_forward: rows*cols too large");
-    if (!std::isfinite(scale)) return fail(SMS_ERR_INVALID_ARG, "sms_forward: scale must be finite");
-    if (!aligned16(x) || !aligned16(y)) return fail(SMS_ERR_INVALID_ARG, "sms_forward: x and y must be 16-byte aligned");
+    if (!x || !y) return fail(SMS_ERR_INVALID_ARG, "%s: x and y must not be NULL", who);
+    if (cols <= 0 || cols > kMaxCols) return fail(SMS_ERR_INVALID_ARG, "%s: cols must be in [1, 2^30]", who);
+    if (rows > 0 && rows > kMaxElems / cols) return fail(SMS_ERR_INVALID_ARG, "%s: rows*cols too large", who);
+    if (!std::isfinite(scale)) return fail(SMS_ERR_INVALID_ARG, "%s: scale must be finite", who);
+    if (!aligned16(x) || !aligned16(y)) return fail(SMS_ERR_INVALID_ARG, "%s: x and y must be 16-byte aligned", who);
     const int eb = elem_bytes(dtype);
     const int64_t total = rows * cols;
     if (x != y && overlap(x, total * eb, y, total * eb))
-        return fail(SMS_ERR_INVALID_ARG, "sms_forward: y partially overlaps x");
+        return fail(SMS_ERR_INVALID_ARG, "%s: y partially overlaps x", who);
+    if (mask || lengths) {
+        if (heads <= 0 || heads > ((int64_t)1 << 31)) return fail(SMS_ERR_INVALID_ARG, "%s: heads must be in [1, 2^31]", who);
+    }
+    if (lengths) {
+        if (reinterpret_cast<uintptr_t>(lengths) & 3u)
+            return fail(SMS_ERR_INVALID_ARG, "%s: lengths must be 4-byte aligned", who);
+        const int64_t nb = (rows + cols * heads - 1) / (cols * heads);  // batches: entries read from lengths
+        if (overlap(lengths, nb * 4, y, total * eb)) return fail(SMS_ERR_INVALID_ARG, "%s: y overlaps lengths", who);
+    }
     if (mask) {
-        if (heads <= 0 || heads > ((int64_t)1 << 31)) return fail(SMS_ERR_INVALID_ARG, "sms_forward: heads must be in [1, 2^31]");
         if (mask_stride_b < 0 || mask_stride_h < 0)
-            return fail(SMS_ERR_INVALID_ARG, "sms_forward: mask strides must be >= 0");
-        if (!aligned16(mask)) return fail(SMS_ERR_INVALID_ARG, "sms_forward: mask must be 16-byte aligned");
-        if (mask_numel < 0 || mask_numel > kMaxElems) return fail(SMS_ERR_INVALID_ARG, "sms_forward: bad mask_numel");
+            return fail(SMS_ERR_INVALID_ARG, "%s: mask strides must be >= 0", who);
+        if (!aligned16(mask)) return fail(SMS_ERR_INVALID_ARG, "%s: mask must be 16-byte aligned", who);
+        if (mask_numel < 0 || mask_numel > kMaxElems) return fail(SMS_ERR_INVALID_ARG, "%s: bad mask_numel", who);
         if (rows > 0) {
             // guard the extent arithmetic against overflow before evaluating it
             const double est = (double)(rows / (cols * heads) + 1) * (double)mask_stride_b +
                                (double)heads * (double)mask_stride_h + (double)cols * (double)cols;
-            if (est > 4e18) return fail(SMS_ERR_INVALID_ARG, "sms_forward: mask strides too large");
+            if (est > 4e18) return fail(SMS_ERR_INVALID_ARG, "%s: mask strides too large", who);
             const int64_t ext = mask_extent(rows, cols, heads, mask_stride_b, mask_stride_h);
             if (ext > mask_numel)
-                return fail(SMS_ERR_INVALID_ARG, "sms_forward: rows reach mask element %lld but mask_numel is %lld",
+                return fail(SMS_ERR_INVALID_ARG, "%s: rows reach mask element %lld but mask_numel is %lld", who,
                             (long long)ext - 1, (long long)mask_numel);
             if (overlap(mask, mask_numel * eb, y, total * eb))
-                return fail(SMS_ERR_INVALID_ARG, "sms_forward: y overlaps the mask");
+                return fail(SMS_ERR_INVALID_ARG, "%s: y overlaps the mask", who);
         }
-    } else if (heads <= 0) {
+    } else if (!lengths && heads <= 0) {
         heads = 1;
     }
     if (rows == 0) {
@@ -235,7 +249,7 @@ int sms_forward(const void *x, const void *mask, int64_t mask_numel, int64_t mas
     cudaError_t e = device_info(dev, nsm, err);
     if (e != cudaSuccess) {
         cudaGetLastError();
-        return fail(SMS_ERR_CUDA, "sms_forward: device query failed: %s", cuda_msg(e));
+        return fail(SMS_ERR_CUDA, "%s: device query failed: %s", who, cuda_msg(e));
     }
 
     const int vec = vec_elems(dtype);
@@ -248,57 +262,68 @@ int sms_forward(const void *x, const void *mask, int64_t mask_numel, int64_t mas
     a.scale = scale; a.causal = is_causal ? 1 : 0; a.err = err;
     a.dcols = FastDiv((uint32_t)cols);
     a.dheads = FastDiv((uint32_t)heads);
+    a.lengths = lengths;
 
     const int path = pick_path(g_forced.load(), cols, dtype, aligned, false, a.causal != 0);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (path) {
     case SMS_PATH_WARP:
-        if (!warp_fits(cols, dtype, aligned, false)) return fail(SMS_ERR_UNSUPPORTED, "sms_forward: row too wide for the warp path");
+        if (!warp_fits(cols, dtype, aligned, false)) return fail(SMS_ERR_UNSUPPORTED, "%s: row too wide for the warp path", who);
         e = launch_fwd_warp(a, dtype, aligned, st);
         break;
     case SMS_PATH_RING:
-        if (!ring_fits(cols, dtype, aligned)) return fail(SMS_ERR_UNSUPPORTED, "sms_forward: row too wide for the ring path");
+        if (!ring_fits(cols, dtype, aligned)) return fail(SMS_ERR_UNSUPPORTED, "%s: row too wide for the ring path", who);
         e = launch_fwd_ring(a, dtype, aligned, st);
         break;
     case SMS_PATH_STREAM:
         if (!stream_fits(cols, dtype, aligned, false))
-            return fail(SMS_ERR_UNSUPPORTED, "sms_forward: row too wide for the stream path");
+            return fail(SMS_ERR_UNSUPPORTED, "%s: row too wide for the stream path", who);
         e = launch_fwd_stream(a, dtype, aligned, st);
         break;
     case SMS_PATH_CTA:
-        if (!cta_fits(cols, dtype, aligned)) return fail(SMS_ERR_UNSUPPORTED, "sms_forward: row too wide for the CTA path");
+        if (!cta_fits(cols, dtype, aligned)) return fail(SMS_ERR_UNSUPPORTED, "%s: row too wide for the CTA path", who);
         e = launch_fwd_cta(a, dtype, aligned, st);
         break;
     default:
         e = launch_fwd_online(a, dtype, st);
         break;
     }
-    const int rc = launch_status(e, "sms_forward");
+    const int rc = launch_status(e, who);
     if (rc == SMS_OK) t_last_path = path;
     return rc;
 }
 
-int sms_backward(const void *y, const void *dy, void *dx, int64_t rows, int64_t cols, float scale,
-                 int is_causal_hint, int dtype, void *stream)
+// Validation and dispatch shared by sms_backward and sms_backward_lengths.
+int backward_impl(const char *who, const void *y, const void *dy, void *dx, const int32_t *lengths, int64_t heads,
+                  int64_t rows, int64_t cols, float scale, int is_causal_hint, int dtype, void *stream)
 {
     t_err[0] = '\0';
-    if (dtype < SMS_F32 || dtype > SMS_BF16) return fail(SMS_ERR_INVALID_ARG, "sms_backward: unknown dtype %d", dtype);
-    if (rows < 0) return fail(SMS_ERR_INVALID_ARG, "sms_backward: rows < 0");
+    if (dtype < SMS_F32 || dtype > SMS_BF16) return fail(SMS_ERR_INVALID_ARG, "%s: unknown dtype %d", who, dtype);
+    if (rows < 0) return fail(SMS_ERR_INVALID_ARG, "%s: rows < 0", who);
     if (rows == 0 && cols > 0) {  // empty problem: nothing is read, pointers may be NULL
         t_last_path = SMS_PATH_AUTO;
         return SMS_OK;
     }
-    if (!y || !dy || !dx) return fail(SMS_ERR_INVALID_ARG, "sms_backward: y, dy and dx must not be NULL");
-    if (cols <= 0 || cols > kMaxCols) return fail(SMS_ERR_INVALID_ARG, "sms_backward: cols must be in [1, 2^30]");
-    if (rows > 0 && rows > kMaxElems / cols) return fail(SMS_ERR_INVALID_ARG, "sms_backward: rows*cols too large");
-    if (!std::isfinite(scale)) return fail(SMS_ERR_INVALID_ARG, "sms_backward: scale must be finite");
+    if (!y || !dy || !dx) return fail(SMS_ERR_INVALID_ARG, "%s: y, dy and dx must not be NULL", who);
+    if (cols <= 0 || cols > kMaxCols) return fail(SMS_ERR_INVALID_ARG, "%s: cols must be in [1, 2^30]", who);
+    if (rows > 0 && rows > kMaxElems / cols) return fail(SMS_ERR_INVALID_ARG, "%s: rows*cols too large", who);
+    if (!std::isfinite(scale)) return fail(SMS_ERR_INVALID_ARG, "%s: scale must be finite", who);
     if (!aligned16(y) || !aligned16(dy) || !aligned16(dx))
-        return fail(SMS_ERR_INVALID_ARG, "sms_backward: y, dy and dx must be 16-byte aligned");
+        return fail(SMS_ERR_INVALID_ARG, "%s: y, dy and dx must be 16-byte aligned", who);
     const int eb = elem_bytes(dtype);
     const int64_t total = rows * cols;
-    if (overlap(dx, total * eb, y, total * eb)) return fail(SMS_ERR_INVALID_ARG, "sms_backward: dx overlaps y");
+    if (overlap(dx, total * eb, y, total * eb)) return fail(SMS_ERR_INVALID_ARG, "%s: dx overlaps y", who);
     if (dx != dy && overlap(dx, total * eb, dy, total * eb))
-        return fail(SMS_ERR_INVALID_ARG, "sms_backward: dx partially overlaps dy");
+        return fail(SMS_ERR_INVALID_ARG, "%s: dx partially overlaps dy", who);
+    if (lengths) {
+        if (heads <= 0 || heads > ((int64_t)1 << 31)) return fail(SMS_ERR_INVALID_ARG, "%s: heads must be in [1, 2^31]", who);
+        if (reinterpret_cast<uintptr_t>(lengths) & 3u)
+            return fail(SMS_ERR_INVALID_ARG, "%s: lengths must be 4-byte aligned", who);
+        const int64_t nb = (rows + cols * heads - 1) / (cols * heads);
+        if (overlap(lengths, nb * 4, dx, total * eb)) return fail(SMS_ERR_INVALID_ARG, "%s: dx overlaps lengths", who);
+    } else {
+        heads = 1;
+    }
     if (rows == 0) {
         t_last_path = SMS_PATH_AUTO;
         return SMS_OK;
@@ -309,7 +334,7 @@ int sms_backward(const void *y, const void *dy, void *dx, int64_t rows, int64_t 
     cudaError_t e = device_info(dev, nsm, err);
     if (e != cudaSuccess) {
         cudaGetLastError();
-        return fail(SMS_ERR_CUDA, "sms_backward: device query failed: %s", cuda_msg(e));
+        return fail(SMS_ERR_CUDA, "%s: device query failed: %s", who, cuda_msg(e));
     }
 
     const bool aligned = cols % vec_elems(dtype) == 0;
@@ -318,34 +343,77 @@ int sms_backward(const void *y, const void *dy, void *dx, int64_t rows, int64_t 
     a.rows = rows; a.cols = cols; a.total = total;
     a.scale = scale; a.causal = is_causal_hint ? 1 : 0; a.err = err;
     a.dcols = FastDiv((uint32_t)cols);
+    a.lengths = lengths;
+    a.heads = heads;
+    a.dheads = FastDiv((uint32_t)heads);
 
     const int path = pick_path(g_forced.load(), cols, dtype, aligned, true, a.causal != 0);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (path) {
     case SMS_PATH_WARP:
-        if (!warp_fits(cols, dtype, aligned, true)) return fail(SMS_ERR_UNSUPPORTED, "sms_backward: row too wide for the warp path");
+        if (!warp_fits(cols, dtype, aligned, true)) return fail(SMS_ERR_UNSUPPORTED, "%s: row too wide for the warp path", who);
         e = launch_bwd_warp(a, dtype, aligned, st);
         break;
     case SMS_PATH_RING:
-        if (!ring_fits(cols, dtype, aligned)) return fail(SMS_ERR_UNSUPPORTED, "sms_backward: row too wide for the ring path");
+        if (!ring_fits(cols, dtype, aligned)) return fail(SMS_ERR_UNSUPPORTED, "%s: row too wide for the ring path", who);
         e = launch_bwd_ring(a, dtype, aligned, st);
         break;
     case SMS_PATH_STREAM:
         if (!stream_fits(cols, dtype, aligned, true))
-            return fail(SMS_ERR_UNSUPPORTED, "sms_backward: row too wide for the stream path");
+            return fail(SMS_ERR_UNSUPPORTED, "%s: row too wide for the stream path", who);
         e = launch_bwd_stream(a, dtype, aligned, st);
         break;
     case SMS_PATH_CTA:
-        if (!cta_fits_bwd(cols, dtype, aligned)) return fail(SMS_ERR_UNSUPPORTED, "sms_backward: row too wide for the CTA path");
+        if (!cta_fits_bwd(cols, dtype, aligned)) return fail(SMS_ERR_UNSUPPORTED, "%s: row too wide for the CTA path", who);
         e = launch_bwd_cta(a, dtype, aligned, st);
         break;
     default:
         e = launch_bwd_online(a, dtype, st);
         break;
     }
-    const int rc = launch_status(e, "sms_backward");
+    const int rc = launch_status(e, who);
     if (rc == SMS_OK) t_last_path = path;
     return rc;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sms_forward(const void *x, const void *mask, int64_t mask_numel, int64_t mask_stride_b, int64_t mask_stride_h,
+                int64_t heads, void *y, int64_t rows, int64_t cols, float scale, int is_causal, int dtype,
+                void *stream)
+{
+    return forward_impl("sms_forward", x, mask, mask_numel, mask_stride_b, mask_stride_h, heads, nullptr, y, rows,
+                        cols, scale, is_causal, dtype, stream);
+}
+
+int sms_forward_lengths(const void *x, const int32_t *lengths, int64_t heads, void *y, int64_t rows, int64_t cols,
+                        float scale, int is_causal, int dtype, void *stream)
+{
+    if (!lengths) {
+        t_err[0] = '\0';
+        return fail(SMS_ERR_INVALID_ARG, "sms_forward_lengths: lengths must not be NULL");
+    }
+    return forward_impl("sms_forward_lengths", x, nullptr, 0, 0, 0, heads, lengths, y, rows, cols, scale, is_causal,
+                        dtype, stream);
+}
+
+int sms_backward(const void *y, const void *dy, void *dx, int64_t rows, int64_t cols, float scale,
+                 int is_causal_hint, int dtype, void *stream)
+{
+    return backward_impl("sms_backward", y, dy, dx, nullptr, 1, rows, cols, scale, is_causal_hint, dtype, stream);
+}
+
+int sms_backward_lengths(const void *y, const void *dy, void *dx, const int32_t *lengths, int64_t heads, int64_t rows,
+                         int64_t cols, float scale, int is_causal_hint, int dtype, void *stream)
+{
+    if (!lengths) {
+        t_err[0] = '\0';
+        return fail(SMS_ERR_INVALID_ARG, "sms_backward_lengths: lengths must not be NULL");
+    }
+    return backward_impl("sms_backward_lengths", y, dy, dx, lengths, heads, rows, cols, scale, is_causal_hint, dtype,
+                         stream);
 }
 
 int sms_device_error(void *stream)

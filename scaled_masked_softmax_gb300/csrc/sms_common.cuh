@@ -276,6 +276,17 @@ __device__ __forceinline__ int64_t row_q(int64_t r, int64_t cols, const FastDiv 
     return r % cols;
 }
 
+// Elements a row reads: `limit` (q + 1 under the causal flag, else cols),
+// further cut to the first lengths[b] keys when per-batch key lengths are
+// given (a length outside [0, cols] is clamped).  0 is a live row with no
+// kept key: its output is all zero.
+__device__ __forceinline__ int key_limit(const int32_t *lengths, int64_t b, int64_t cols, int limit)
+{
+    if (!lengths) return limit;
+    const int L = min(max(__ldg(lengths + b), 0), (int)cols);
+    return min(limit, L);
+}
+
 // Records the first failure code in the library's device error word (its
 // address is passed to every kernel that waits on a barrier).
 __device__ __forceinline__ void report_error(int *err, int code)

@@ -26,6 +26,7 @@ struct FwdArgs {
     int causal;
     int *err;              // device error word
     FastDiv dcols, dheads; // division by cols and by heads
+    const int32_t *lengths;  // per-batch key lengths (device), nullptr: none
 };
 
 struct BwdArgs {
@@ -38,6 +39,9 @@ struct BwdArgs {
     int causal;            // the causal hint: y == 0 beyond the diagonal
     int *err;
     FastDiv dcols;         // division by cols
+    const int32_t *lengths;  // key-length hint: y == 0 at j >= lengths[b]; nullptr: none
+    int64_t heads;         // heads of the [B,H,S,S] view (locates b for the lengths)
+    FastDiv dheads;        // division by heads
 };
 
 // "aligned" means every row (and every mask row) starts on a 16-byte boundary:

@@ -31,12 +31,13 @@ struct OnlineRow {
 };
 
 template <int VEC>
-__device__ __forceinline__ OnlineRow online_geom(int64_t r, int64_t cols, int causal, int64_t q)
+__device__ __forceinline__ OnlineRow online_geom(int64_t r, int64_t cols, int causal, int64_t q,
+                                                 const int32_t *lengths, int64_t b)
 {
     OnlineRow g;
     g.x0 = r * cols;
     g.xoff = (int)(g.x0 & (VEC - 1));
-    g.limit = causal ? (int)(q + 1) : (int)cols;
+    g.limit = key_limit(lengths, b, cols, causal ? (int)(q + 1) : (int)cols);
     g.nv_read = (g.xoff + g.limit + VEC - 1) / VEC;
     g.nv_row = (int)((g.xoff + cols + VEC - 1) / VEC);
     return g;
@@ -98,7 +99,7 @@ __global__ void __launch_bounds__(kNT) fwd_online_kernel(const FwdArgs a)
     for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x, rp ^= 1) {
         int64_t q, hh, bb;
         split_row(r, a.cols, a.heads, a.dcols, a.dheads, q, hh, bb);
-        const OnlineRow g = online_geom<VEC>(r, a.cols, a.causal, q);
+        const OnlineRow g = online_geom<VEC>(r, a.cols, a.causal, q, a.lengths, bb);
         const T *xs = reinterpret_cast<const T *>(a.x) + (g.x0 - g.xoff);
         const T *ms = nullptr;
         int64_t m0 = 0;
@@ -221,7 +222,10 @@ __global__ void __launch_bounds__(kNT) bwd_online_kernel(const BwdArgs a)
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     int rp = 0;
     for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x, rp ^= 1) {
-        const OnlineRow g = online_geom<VEC>(r, a.cols, a.causal, row_q(r, a.cols, a.dcols));
+        int64_t q = 0, hh = 0, bb = 0;
+        if (a.lengths) split_row(r, a.cols, a.heads, a.dcols, a.dheads, q, hh, bb);
+        else q = row_q(r, a.cols, a.dcols);
+        const OnlineRow g = online_geom<VEC>(r, a.cols, a.causal, q, a.lengths, bb);
         const T *ys = reinterpret_cast<const T *>(a.y) + (g.x0 - g.xoff);
         const T *gs = reinterpret_cast<const T *>(a.dy) + (g.x0 - g.xoff);
         float dot = 0.f;

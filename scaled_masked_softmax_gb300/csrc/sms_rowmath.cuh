@@ -83,7 +83,8 @@ struct RowPos {
     int64_t mA;   // flat mask index of the first aligned mask vector of the row
     int xoff;     // row start mod VEC
     int msh;      // mask elements to shift by (mask row misaligned relative to x)
-    int limit;    // elements read: q + 1 under causal, cols otherwise; 0 for a dead row
+    int limit;    // elements read: q + 1 under causal, cols otherwise, cut to the key length; 0 for a dead row
+    bool live;    // r < rows (a live row with limit 0 still writes its zeros)
     bool fast;    // every vector read lies inside x and the mask: no per-vector bounds tests
 };
 
@@ -96,8 +97,9 @@ __device__ __forceinline__ RowPos fwd_pos(const FwdArgs &a, int64_t r)
     p.xoff = (ALIGNED || !live) ? 0 : (int)(x0 & (VEC - 1));  // dead row: no vector has j0 < limit = 0
     p.xb = x0 - p.xoff;
     int64_t q = 0, h = 0, b = 0;
-    if (live && (a.causal || a.mask)) split_row(r, a.cols, a.heads, a.dcols, a.dheads, q, h, b);
-    p.limit = live ? (a.causal ? (int)(q + 1) : (int)a.cols) : 0;
+    if (live && (a.causal || a.mask || a.lengths)) split_row(r, a.cols, a.heads, a.dcols, a.dheads, q, h, b);
+    p.live = live;
+    p.limit = live ? key_limit(a.lengths, b, a.cols, a.causal ? (int)(q + 1) : (int)a.cols) : 0;
     const int64_t D = b * a.msb + h * a.msh + q * a.cols - p.xoff;
     p.msh = ALIGNED ? 0 : (int)(D & (VEC - 1));
     p.mA = D - p.msh;
@@ -360,7 +362,7 @@ __device__ __forceinline__ void fwd_store(const FwdArgs &a, const RowPos &p, int
                                           float fac)
 {
     constexpr int VEC = Dt<T>::VEC;
-    if (p.limit == 0) return;  // dead row (a live row reads at least one element)
+    if (!p.live) return;
     T *ys = reinterpret_cast<T *>(a.y) + p.xb;
     const int64_t cols = a.cols;
     const float2 f2 = make_float2(fac, fac);
@@ -405,7 +407,8 @@ __device__ __forceinline__ void fwd_finish(const FwdArgs &a, const RowPos &p, in
 struct BRowPos {
     int64_t xb;
     int xoff;
-    int limit;   // elements read: q + 1 under the causal hint, cols otherwise; 0 for a dead row
+    int limit;   // elements read: q + 1 under the causal hint, cols otherwise, cut to the key length; 0 for a dead row
+    bool live;   // r < rows
     bool fast;   // every vector read lies inside the tensors
 };
 
@@ -417,8 +420,11 @@ __device__ __forceinline__ BRowPos bwd_pos(const BwdArgs &a, int64_t r)
     const int64_t x0 = r * a.cols;
     p.xoff = (ALIGNED || !live) ? 0 : (int)(x0 & (VEC - 1));
     p.xb = x0 - p.xoff;
-    const int64_t q = (live && a.causal) ? row_q(r, a.cols, a.dcols) : 0;
-    p.limit = live ? (a.causal ? (int)(q + 1) : (int)a.cols) : 0;
+    int64_t q = 0, h = 0, b = 0;
+    if (live && a.lengths) split_row(r, a.cols, a.heads, a.dcols, a.dheads, q, h, b);
+    else if (live && a.causal) q = row_q(r, a.cols, a.dcols);
+    p.live = live;
+    p.limit = live ? key_limit(a.lengths, b, a.cols, a.causal ? (int)(q + 1) : (int)a.cols) : 0;
     const int64_t nv = (p.xoff + p.limit + VEC - 1) / VEC;
     p.fast = ALIGNED || p.xb + nv * VEC <= a.total;
     return p;
@@ -559,7 +565,7 @@ template <typename T, int G, int NV, bool ALIGNED>
 __device__ __forceinline__ void bwd_store(const BwdArgs &a, const BRowPos &p, int gl, const BwdBuf<NV> &B, float dot)
 {
     constexpr int VEC = Dt<T>::VEC;
-    if (p.limit == 0) return;
+    if (!p.live) return;
     T *dxs = reinterpret_cast<T *>(a.dx) + p.xb;
     const int64_t cols = a.cols;
     const bool fast = ALIGNED || p.fast;

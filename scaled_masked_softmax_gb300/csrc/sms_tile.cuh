@@ -52,7 +52,7 @@ struct __align__(16) ChunkDesc {
     int32_t pad0;
     int32_t cx_hi;   // one past the last row vector (row-relative) held by the stage
     int32_t xoff;    // x0 mod VEC
-    int32_t limit;   // elements read: q+1 under causal, else cols
+    int32_t limit;   // elements read: q+1 under causal, else cols, cut to the key length
     int32_t nv_read; // vectors holding elements < limit
     int32_t nv_row;  // vectors holding row elements
     int32_t nchunks; // stages the row occupies
@@ -151,19 +151,23 @@ __global__ void __launch_bounds__(Geo<WG, R, SLOTS, CH>::THREADS, 1)
             for (int g = 0; g < R; ++g) {  // rows go to the groups in turn
                 if (r < rows && ok) {
                     int64_t q = 0, hh = 0, bb = 0;
+                    const int32_t *lengths = BWD ? ba.lengths : fa.lengths;
                     if (BWD) {
-                        if (causal) q = row_q(r, cols, ba.dcols);
-                    } else if (causal || srcB) {
+                        if (lengths) split_row(r, cols, ba.heads, ba.dcols, ba.dheads, q, hh, bb);
+                        else if (causal) q = row_q(r, cols, ba.dcols);
+                    } else if (causal || srcB || lengths) {
                         split_row(r, cols, fa.heads, fa.dcols, fa.dheads, q, hh, bb);
                     }
                     ChunkDesc d;
                     d.x0 = r * cols;
                     d.xoff = (int)(d.x0 & (VEC - 1));
                     const int64_t gbase = (d.x0 - d.xoff) / VEC;
-                    d.limit = causal ? (int)(q + 1) : (int)cols;
+                    d.limit = key_limit(lengths, bb, cols, causal ? (int)(q + 1) : (int)cols);
                     d.nv_read = (d.xoff + d.limit + VEC - 1) / VEC;
                     d.nv_row = (int)((d.xoff + cols + VEC - 1) / VEC);
-                    d.nchunks = (d.nv_read + G::PV - 1) / G::PV;
+                    // at least one stage per row, also for a row with no kept key:
+                    // its consumers wait for exactly one stage
+                    d.nchunks = max(1, (d.nv_read + G::PV - 1) / G::PV);
                     d.m0 = (!BWD && srcB) ? bb * fa.msb + hh * fa.msh + q * cols : 0;
                     d.mvec = ((d.m0 - d.xoff) & (VEC - 1)) == 0;
                     d.pad0 = d.pad1 = d.pad2 = 0;

@@ -23,11 +23,13 @@ constexpr int kThreads = 256;  // 8 warps per CTA
 // Positions of the RPG consecutive rows row0 .. row0+RPG-1 of a lane group:
 // the first is split with the invariant-divisor division, the others follow
 // by stepping one row (q+1, wrapping into the next head and batch).  Rows at
-// or beyond `rows` get limit 0: they read and write nothing.
+// or beyond `rows` get limit 0: they read and write nothing.  With per-batch
+// key lengths the limit is cut to the row's batch length.
 template <int RPG>
 __device__ __forceinline__ void group_rows(int64_t row0, int64_t rows, int64_t cols, int64_t heads, bool causal,
                                            bool need_pos, const FastDiv &dc, const FastDiv &dh, int64_t msb,
-                                           int64_t msh, int (&limit)[RPG], int64_t (&m0)[RPG])
+                                           int64_t msh, const int32_t *lengths, int (&limit)[RPG],
+                                           int64_t (&m0)[RPG])
 {
     int64_t q = 0, h = 0, b = 0;
     if (need_pos && row0 < rows) split_row(row0, cols, heads, dc, dh, q, h, b);
@@ -40,7 +42,7 @@ __device__ __forceinline__ void group_rows(int64_t row0, int64_t rows, int64_t c
             }
         }
         const bool live = row0 + i < rows;
-        limit[i] = live ? (causal ? (int)(q + 1) : (int)cols) : 0;
+        limit[i] = live ? key_limit(lengths, b, cols, causal ? (int)(q + 1) : (int)cols) : 0;
         m0[i] = b * msb + h * msh + q * cols;
     }
 }
@@ -63,8 +65,8 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_warp_kernel(const FwdArgs a)
 
     int limit[RPG];
     int64_t m0[RPG];
-    group_rows<RPG>(row0, a.rows, cols, a.heads, a.causal, a.causal || a.mask, a.dcols, a.dheads, a.msb, a.msh, limit,
-                    m0);
+    group_rows<RPG>(row0, a.rows, cols, a.heads, a.causal, a.causal || a.mask || a.lengths, a.dcols, a.dheads, a.msb,
+                    a.msh, a.lengths, limit, m0);
     // The mask row of row i starts D = m0 - xoff elements into the x-aligned
     // vector grid: its elements for x vector vi sit at A + vi*VEC + sh ..,
     // A = D - sh aligned, sh = D mod VEC.  sh == 0: one 16-byte load per
@@ -269,7 +271,8 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_warp_kernel(const BwdArgs a)
 
     int limit[RPG];
     int64_t unused_m0[RPG];
-    group_rows<RPG>(row0, a.rows, cols, 1, a.causal, a.causal, a.dcols, FastDiv(), 0, 0, limit, unused_m0);
+    group_rows<RPG>(row0, a.rows, cols, a.heads, a.causal, a.causal || a.lengths, a.dcols, a.dheads, 0, 0, a.lengths,
+                    limit, unused_m0);
     int xoff[RPG];
     uint4 yr[RPG][NV], gr[RPG][NV];
 #pragma unroll

@@ -6,7 +6,10 @@ size(-1), §4.2), the mask is additive, of x's dtype, and may be omitted (§2.2)
 ``ScaledMaskSoftmaxFunction`` keeps only the output y for the backward and
 returns no gradient for mask, scale or is_causal (§4.3).  Boolean masks must be
 converted by the caller, e.g. ``mask.to(x.dtype) * -inf`` with 0 where kept
-(§2.2 and §5.1 warn that adding a bool mask as 1.0 is wrong).
+(§2.2 and §5.1 warn that adding a bool mask as 1.0 is wrong).  A key-padding
+mask can instead be given as ``key_lengths`` (int32 [B], the valid keys of
+each batch): the same result as the additive mask with -inf beyond L_b, with
+no mask tensor read and the padded scores never read.
 
 PyTorch provides only memory, device placement and the current stream here;
 the computation runs in libsms through the C ABI.
@@ -64,9 +67,23 @@ def mask_layout(x_shape, mask_shape):
     return sb, sh, H
 
 
+def _key_lengths(key_lengths: torch.Tensor, x_shape, device) -> tuple:
+    """(contiguous int32 lengths, heads) for x read as [B, H, S, S]."""
+    if len(x_shape) < 2 or x_shape[-2] != x_shape[-1]:
+        raise ValueError("key_lengths needs square score matrices (x.shape[-2] == x.shape[-1])")
+    if key_lengths.dtype != torch.int32 or key_lengths.device != device:
+        raise TypeError("key_lengths must be an int32 tensor on x's device")
+    H = x_shape[-3] if len(x_shape) >= 3 else 1
+    B = math.prod(x_shape[:-3]) if len(x_shape) > 3 else 1
+    if key_lengths.numel() != B:
+        raise ValueError(f"key_lengths has {key_lengths.numel()} entries, x has {B} batches")
+    return key_lengths.contiguous(), H
+
+
 def forward(x: torch.Tensor, mask: Optional[torch.Tensor] = None, scale: float = 1.0, is_causal: bool = False,
-            out: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """y = softmax(x * scale + mask) over the last dim, j > q masked if is_causal."""
+            out: Optional[torch.Tensor] = None, key_lengths: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """y = softmax(x * scale + mask) over the last dim, j > q masked if is_causal,
+    keys j >= key_lengths[b] masked when key_lengths is given."""
     if not x.is_cuda:
         raise ValueError("x must be a CUDA tensor (there is no CPU path)")
     if x.dtype not in _DTYPE_CODE:
@@ -84,6 +101,17 @@ def forward(x: torch.Tensor, mask: Optional[torch.Tensor] = None, scale: float =
             (y.numel() and y.data_ptr() % 16):
         raise ValueError("out must be a contiguous, 16-byte aligned tensor like x")
     mptr, mnum, sb, sh, heads = None, 0, 0, 0, (x.shape[-3] if x.dim() >= 3 else 1)
+    if key_lengths is not None:
+        if mask is not None:
+            raise ValueError("give either an additive mask or key_lengths, not both")
+        lengths, heads = _key_lengths(key_lengths, x.shape, x.device)
+        if rows == 0:
+            return y
+        with torch.cuda.device(x.device):
+            stream = torch.cuda.current_stream(x.device).cuda_stream
+            binding.sms_forward_lengths(x.data_ptr(), lengths.data_ptr(), heads, y.data_ptr(), rows, cols,
+                                        float(scale), bool(is_causal), dt, stream)
+        return y
     if mask is not None:
         if mask.dtype != x.dtype:
             raise TypeError(f"mask dtype {mask.dtype} must equal x dtype {x.dtype} (convert a bool mask "
@@ -103,8 +131,9 @@ def forward(x: torch.Tensor, mask: Optional[torch.Tensor] = None, scale: float =
 
 
 def backward(y: torch.Tensor, dy: torch.Tensor, scale: float = 1.0, is_causal_hint: bool = False,
-             out: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """dx = (dy - sum(dy*y)) * y * scale over the last dim."""
+             out: Optional[torch.Tensor] = None, key_lengths: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """dx = (dy - sum(dy*y)) * y * scale over the last dim; key_lengths (and
+    is_causal_hint) promise y == 0 beyond them, so those positions are not read."""
     if not (y.is_cuda and dy.is_cuda):
         raise ValueError("y and dy must be CUDA tensors (there is no CPU path)")
     if y.dtype not in _DTYPE_CODE or dy.dtype != y.dtype:
@@ -122,6 +151,13 @@ def backward(y: torch.Tensor, dy: torch.Tensor, scale: float = 1.0, is_causal_hi
         raise ValueError("out must be a contiguous, 16-byte aligned tensor like y")
     if rows == 0:
         return dx
+    if key_lengths is not None:
+        lengths, heads = _key_lengths(key_lengths, y.shape, y.device)
+        with torch.cuda.device(y.device):
+            stream = torch.cuda.current_stream(y.device).cuda_stream
+            binding.sms_backward_lengths(y.data_ptr(), dy.data_ptr(), dx.data_ptr(), lengths.data_ptr(), heads, rows,
+                                         cols, float(scale), bool(is_causal_hint), _DTYPE_CODE[y.dtype], stream)
+        return dx
     with torch.cuda.device(y.device):
         stream = torch.cuda.current_stream(y.device).cuda_stream
         binding.sms_backward(y.data_ptr(), dy.data_ptr(), dx.data_ptr(), rows, cols, float(scale),
@@ -130,12 +166,14 @@ def backward(y: torch.Tensor, dy: torch.Tensor, scale: float = 1.0, is_causal_hi
 
 
 class ScaledMaskSoftmaxFunction(torch.autograd.Function):
-    """Saves y (not x) for backward; no gradient for mask, scale, is_causal."""
+    """Saves y (not x) for backward; no gradient for mask, scale, is_causal or
+    key_lengths."""
 
     @staticmethod
-    def forward(ctx, x, mask, scale, is_causal):
-        y = forward(x, mask, scale, is_causal)
+    def forward(ctx, x, mask, scale, is_causal, key_lengths=None):
+        y = forward(x, mask, scale, is_causal, key_lengths=key_lengths)
         ctx.save_for_backward(y)
+        ctx.key_lengths = key_lengths
         ctx.scale = float(scale)
         ctx.is_causal = bool(is_causal)
         return y
@@ -143,13 +181,14 @@ class ScaledMaskSoftmaxFunction(torch.autograd.Function):
     @staticmethod
     def backward(ctx, grad_y):
         (y,) = ctx.saved_tensors
-        dx = backward(y, grad_y, ctx.scale, is_causal_hint=ctx.is_causal)
-        return dx, None, None, None
+        dx = backward(y, grad_y, ctx.scale, is_causal_hint=ctx.is_causal, key_lengths=ctx.key_lengths)
+        return dx, None, None, None, None
 
 
 def scaled_mask_softmax(x: torch.Tensor, mask: Optional[torch.Tensor] = None, scale: float = 1.0,
-                        is_causal: bool = False) -> torch.Tensor:
-    """Fused softmax(x * scale + mask) over the last dim, differentiable in x."""
+                        is_causal: bool = False, key_lengths: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Fused softmax(x * scale + mask) over the last dim, differentiable in x.
+    key_lengths (int32 [B]) masks keys j >= key_lengths[b] without a mask tensor."""
     if not math.isfinite(float(scale)):
         raise ValueError("scale must be finite")
-    return ScaledMaskSoftmaxFunction.apply(x, mask, scale, is_causal)
+    return ScaledMaskSoftmaxFunction.apply(x, mask, scale, is_causal, key_lengths)

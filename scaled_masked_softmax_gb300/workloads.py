@@ -126,7 +126,8 @@ def make_inputs(w: Workload, device="cpu", with_dy: Optional[bool] = None):
     """Draw x, the additive mask and dy for workload ``w`` on ``device``.
 
     Returns a dict with x [rows, cols], mask (None or its broadcast shape),
-    dy (or None), and the mask broadcast description.  Draws are seeded by
+    dy (or None), the mask broadcast description, and for key-padding
+    workloads the padding as per-batch key lengths (int32 [B], else None).  Draws are seeded by
     ``w.seed``; small integer choices (padding lengths, spike rows/columns)
     are drawn on the CPU so they do not depend on the device.
     """
@@ -150,9 +151,11 @@ def make_inputs(w: Workload, device="cpu", with_dy: Optional[bool] = None):
         x[r_idx.to(dev), c_idx.to(dev)] = torch.tensor(w.spike_value, dtype=dt, device=dev)
 
     mask = None
+    key_lengths = None
     if w.mask == "B1SS":
         lo = int(math.ceil(w.pad_lo * S))
         L = torch.randint(lo, S + 1, (w.B,), generator=g_cpu)
+        key_lengths = L.to(torch.int32).to(dev)  # the same padding as per-batch key lengths
         cols_idx = torch.arange(S, device=dev)
         keep = cols_idx[None, :] < L.to(dev)[:, None]  # [B, S]
         mrow = torch.where(keep, torch.tensor(0.0, device=dev), torch.tensor(w.pad_fill, device=dev))
@@ -179,5 +182,6 @@ def make_inputs(w: Workload, device="cpu", with_dy: Optional[bool] = None):
         dy = torch.randn(rows, S, generator=g_dev, device=dev, dtype=torch.float32).to(dt)
 
     sb, sh, heads = w.mask_strides()
-    return {"x": x, "mask": mask, "dy": dy, "mask_stride_b": sb, "mask_stride_h": sh, "heads": heads}
+    return {"x": x, "mask": mask, "dy": dy, "mask_stride_b": sb, "mask_stride_h": sh, "heads": heads,
+            "key_lengths": key_lengths}
 

@@ -78,6 +78,23 @@ def raw_forward(inp, w, y=None):
     return y
 
 
+def raw_forward_lengths(x, lengths, heads, w, y=None):
+    """sms_forward_lengths through the C ABI (rows of x, per-batch key lengths)."""
+    y = torch.empty_like(x) if y is None else y
+    dt = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}[x.dtype]
+    sms.sms_forward_lengths(x.data_ptr(), lengths.data_ptr(), heads, y.data_ptr(), w.rows, w.cols, w.scale,
+                            w.is_causal, dt, torch.cuda.current_stream().cuda_stream)
+    return y
+
+
+def raw_backward_lengths(y, dy, lengths, heads, w, causal_hint, dx=None):
+    dx = torch.empty_like(y) if dx is None else dx
+    dt = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}[y.dtype]
+    sms.sms_backward_lengths(y.data_ptr(), dy.data_ptr(), dx.data_ptr(), lengths.data_ptr(), heads, w.rows, w.cols,
+                             w.scale, causal_hint, dt, torch.cuda.current_stream().cuda_stream)
+    return dx
+
+
 def raw_backward(y, dy, w, causal_hint, dx=None):
     dx = torch.empty_like(y) if dx is None else dx
     dt = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}[y.dtype]

@@ -164,3 +164,48 @@ def test_mask_layout(x_shape, m_shape, want):
 def test_mask_layout_rejects(x_shape, m_shape):
     with pytest.raises(ValueError):
         sms.mask_layout(x_shape, m_shape)
+
+
+def _fwd_len(**kw):
+    a = dict(x=0x10000, lengths=0x50000, heads=1, y=0x20000, rows=16, cols=8, scale=1.0, causal=0, dtype=0,
+             stream=None)
+    a.update(kw)
+    return binding.lib().sms_forward_lengths(a["x"], a["lengths"], a["heads"], a["y"], a["rows"], a["cols"],
+                                             a["scale"], a["causal"], a["dtype"], a["stream"])
+
+
+def _bwd_len(**kw):
+    a = dict(y=0x10000, dy=0x20000, dx=0x30000, lengths=0x50000, heads=1, rows=16, cols=8, scale=1.0, causal=0,
+             dtype=0, stream=None)
+    a.update(kw)
+    return binding.lib().sms_backward_lengths(a["y"], a["dy"], a["dx"], a["lengths"], a["heads"], a["rows"],
+                                              a["cols"], a["scale"], a["causal"], a["dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("kw", [
+    dict(lengths=None), dict(lengths=0x50002), dict(heads=0), dict(heads=-3), dict(heads=(1 << 31) + 1),
+    dict(x=None), dict(dtype=5), dict(cols=0), dict(scale=float("nan")), dict(y=0x20004),
+    dict(lengths=0x20000 + 4 * 8 * 16 - 4),  # the lengths array (2 batches) overlaps y
+])
+def test_forward_lengths_rejects_bad_arguments(kw):
+    assert _fwd_len(**kw) == INVALID
+    assert binding.sms_last_error().startswith("sms_forward_lengths")
+
+
+@pytest.mark.parametrize("kw", [
+    dict(lengths=None), dict(lengths=0x50001), dict(heads=0), dict(dx=None), dict(dx=0x10010),
+    dict(lengths=0x30000 + 4),  # overlaps dx
+])
+def test_backward_lengths_rejects_bad_arguments(kw):
+    assert _bwd_len(**kw) == INVALID
+    assert binding.sms_last_error().startswith("sms_backward_lengths")
+
+
+def test_lengths_entry_points_pass_validation():
+    # valid arguments reach the device query (no GPU here: SMS_ERR_CUDA); rows = 0 is a no-op
+    if torch.cuda.is_available():
+        pytest.skip("host-only check")
+    assert _fwd_len() == binding.SMS_ERR_CUDA
+    assert _bwd_len(heads=2, causal=1) == binding.SMS_ERR_CUDA
+    assert _fwd_len(rows=0) == binding.SMS_OK
+    assert _bwd_len(rows=0) == binding.SMS_OK

@@ -152,6 +152,100 @@ def test_persistent_kernels_walk_many_rows(S, kind, causal, dt, path):
     H.check_backward(H.to_np64(dx), y.cpu(), inp["dy"].cpu(), w.scale, DTYPES[dt], f"{path} grid=3 bwd S={S} {dt}")
 
 
+LEN_WIDTHS = [1, 3, 8, 33, 100, 128, 129, 1000, 1024, 2049, 4099, 8192, 12345, 20000]
+
+
+@pytest.mark.parametrize("path", ["auto", "warp", "stream", "ring", "cta", "online"])
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("S", LEN_WIDTHS)
+def test_key_lengths(S, dt, path):
+    """sms_forward_lengths / sms_backward_lengths on every family: the oracle
+    with key lengths, bit-identical to the same family run with the expanded
+    [B,1,S,S] mask (0 below L_b, -inf from L_b on), lengths 0 (all-zero rows),
+    1, beyond S and negative (clamped)."""
+    causal = LEN_WIDTHS.index(S) % 2 == 0
+    Hh = 2
+    lengths = torch.tensor([S // 3 + 1, 0, 1, S, S + 5, -2], dtype=torch.int32)
+    B = lengths.numel()
+    rows = min(B * Hh * S, max(3, 12_000_000 // S))
+    w = _wl(S, dt, rows, mask="none", causal=causal, B=B, Hh=Hh, seed=43)
+    inp = H.make(w)
+    L = lengths.cuda()
+    # the same padding as an additive mask holding only the query rows the
+    # rows reach: [batches, qmax, S], batch stride qmax*S
+    nb, qmax = (rows + Hh * S - 1) // (Hh * S), min(S, rows)
+    mask = torch.zeros(nb, qmax, S, device="cuda")
+    for b in range(nb):
+        mask[b, :, max(0, min(S, int(lengths[b]))):] = -math.inf
+    mask = mask.to(DTYPES[dt])
+    minp = dict(inp, mask=mask, mask_stride_b=qmax * S, mask_stride_h=0, heads=Hh)
+    with H.forced_path(path):
+        try:
+            y = H.raw_forward_lengths(inp["x"], L, Hh, w)
+            y_mask = H.raw_forward(minp, w)
+            dx = H.raw_backward_lengths(y, inp["dy"], L, Hh, w, causal_hint=causal)
+            dx_plain = H.raw_backward(y, inp["dy"], w, causal_hint=False)
+        except sms.SmsError as e:
+            if e.status == 2:
+                pytest.skip(f"{path} path does not take cols={S}")
+            raise
+    torch.cuda.synchronize()
+    assert sms.sms_device_error(torch.cuda.current_stream().cuda_stream) == 0
+    assert torch.equal(y, y_mask), f"{path} S={S} {dt}: key lengths differ from the expanded mask"
+    y_ref = oracle.forward(inp["x"].cpu(), S, w.scale, causal, heads=Hh, key_lengths=lengths)
+    H.check_forward(H.to_np64(y), y_ref, DTYPES[dt], f"{path} lengths S={S} {dt} causal={causal}")
+    H.check_backward(H.to_np64(dx), y.cpu(), inp["dy"].cpu(), w.scale, DTYPES[dt], f"{path} bwd lengths S={S} {dt}")
+    H.check_backward(H.to_np64(dx_plain), y.cpu(), inp["dy"].cpu(), w.scale, DTYPES[dt], f"{path} bwd S={S} {dt}")
+    zero = y == 0
+    assert torch.equal(dx[zero], torch.zeros_like(dx[zero])) and not torch.signbit(dx[zero]).any()
+
+
+@pytest.mark.parametrize("name", ["keypad_f32_s1024", "keypad_causal_bf16_s4096"])
+def test_full_size_key_lengths(name):
+    """The key-padding workloads at full size through the key-length entry
+    points: sampled rows against the oracle, and equal to the additive-mask
+    path on those rows."""
+    w = workloads.WORKLOADS[name]
+    inp = workloads.make_inputs(w, device="cuda", with_dy=True)
+    L = inp["key_lengths"]
+    y = H.raw_forward_lengths(inp["x"], L, w.H, w)
+    torch.cuda.synchronize()
+    assert sms.sms_device_error(torch.cuda.current_stream().cuda_stream) == 0
+    _properties(y, inp, w)
+    idx = _sample_rows(w.rows, w.cols, 96, w.seed + 7)
+    ti = torch.as_tensor(idx, device=y.device)
+    y_ref = oracle.forward(inp["x"][ti].cpu(), w.cols, w.scale, w.is_causal, heads=w.H, key_lengths=L.cpu(),
+                           row_index=idx)
+    H.check_forward(H.to_np64(y[ti]), y_ref, w.torch_dtype, name + " lengths")
+    y_mask = H.raw_forward(inp, w)
+    torch.cuda.synchronize()
+    assert torch.equal(y[ti], y_mask[ti])
+    del y_mask
+    dx = H.raw_backward_lengths(y, inp["dy"], L, w.H, w, causal_hint=w.is_causal)
+    torch.cuda.synchronize()
+    assert sms.sms_device_error(torch.cuda.current_stream().cuda_stream) == 0
+    H.check_backward(H.to_np64(dx[ti]), y[ti].cpu(), inp["dy"][ti].cpu(), w.scale, w.torch_dtype, name + " bwd")
+    del inp, y, dx
+    torch.cuda.empty_cache()
+
+
+def test_autograd_key_lengths():
+    B, Hh, S = 3, 4, 200
+    g = torch.Generator(device="cuda").manual_seed(47)
+    for dt in (torch.float32, torch.float16, torch.bfloat16):
+        x = (torch.randn(B, Hh, S, S, generator=g, device="cuda") * 8).to(dt).requires_grad_(True)
+        L = torch.tensor([S, 73, 0], dtype=torch.int32, device="cuda")
+        y = sms.scaled_mask_softmax(x, None, 0.125, True, key_lengths=L)
+        dy = torch.randn(B, Hh, S, S, generator=g, device="cuda").to(dt)
+        y.backward(dy)
+        torch.cuda.synchronize()
+        y_ref = oracle.forward(x.detach().cpu(), S, 0.125, True, heads=Hh, key_lengths=L.cpu())
+        H.check_forward(H.to_np64(y).reshape(-1, S), y_ref.reshape(-1, S), dt, f"autograd lengths {dt}")
+        H.check_backward(H.to_np64(x.grad).reshape(-1, S), y.detach().cpu().reshape(-1, S),
+                         dy.cpu().reshape(-1, S), 0.125, dt, f"autograd lengths bwd {dt}")
+        assert torch.all(y[2] == 0) and torch.all(x.grad[2] == 0)
+
+
 def test_spike_rows_are_one_hot():
     w = workloads.scaled(workloads.WORKLOADS["causal_spike_f16_s2048"], B=1, H=2)
     inp = workloads.make_inputs(w, device="cuda")
