@@ -328,6 +328,39 @@ def run_ours(args, rank, world, device):
     roof = {"kernel": dom, "bound": "hbm", "achieved": kernels[dom]["gbs"], "peak": peak, "unit": "GB/s",
             "frac": round(kernels[dom]["gbs"] / peak, 4), "traffic": traffic, "peak_source": peak_kind}
 
+    graph = None
+    if getattr(args, "graph", 0) and args.graph > 0:
+        # the same step replayed from a CUDA graph of `args.graph` steps (launch
+        # overhead amortised; each kernel did its one-time set-up in the warm-up)
+        n = args.graph
+        gs = torch.cuda.Stream(device)
+        gs.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(gs):
+            st_saved = st
+            st = gs.cuda_stream
+            with torch.cuda.graph(g, stream=gs):
+                for _ in range(n):
+                    fwd()
+                    bwd()
+            st = st_saved
+        stream.wait_stream(gs)
+        reps = max(1, K // n)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize(device)
+        ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ga.record(stream)
+        for _ in range(reps):
+            g.replay()
+        gb.record(stream)
+        torch.cuda.synchronize(device)
+        g_ms = ga.elapsed_time(gb) / (reps * n)
+        graph = {"steps_per_graph": n, "replays": reps, "ms_per_step": round(g_ms, 5),
+                 "value": round(step_bytes / (g_ms * 1e6), 1), "unit": "GB/s",
+                 "rows_per_s": round(w.rows / (g_ms / 1e3), 1),
+                 "note": "fwd+bwd steps replayed from one CUDA graph on inputs resident in HBM"}
+
     value = aggregate_gbs(step_bytes, world, step_ms)
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
@@ -343,7 +376,7 @@ def run_ours(args, rank, world, device):
                    "parallelism": f"replicas x{world} (independent rows per GPU)"},
         "pct_of_peak": round(100 * value / world / peak, 2),
         "rows_per_s": round(w.rows * world / (step_ms / 1e3), 1),
-        "kernels": kernels, "roofline": roof, "gpu_launches": int(n_launch),
+        "kernels": kernels, "roofline": roof, "gpu_launches": int(n_launch), "graph": graph,
         "clocks": clk,
     }
     return res, (w, inp, y, dx)
@@ -515,6 +548,8 @@ def main():
                     help="force one kernel family (tuning); the default lets the dispatcher choose")
     ap.add_argument("--all-paths", action="store_true", help="with --all: every kernel family per workload")
     ap.add_argument("--only", default=None, help="with --all: comma-separated workload names")
+    ap.add_argument("--graph", type=int, default=0, metavar="N",
+                    help="also time the step replayed from a CUDA graph of N steps (launch-bound shapes)")
     ap.add_argument("--lengths", action="store_true",
                     help="key-padding workloads through the key-length entry points instead of the [B,1,S,S] mask")
     args = ap.parse_args()

@@ -39,6 +39,12 @@
  * article's §4.3 pitfall 3).  Calls are asynchronous: a SMS_OK return means the
  * launch was accepted.
  *
+ * Graphs.  Every launch goes on `stream`, so calls can be captured into a CUDA
+ * graph (the second article's §1.1 and §4.4 on launch overhead).  Make one
+ * eager call per shape and kernel family before capturing: it does that
+ * kernel's one-time set-up (function attributes, occupancy query, the device
+ * error word's address), which must not happen during a capture.
+ *
  * Alignment.  x, y, mask, dy and dx must be 16-byte aligned (every CUDA / PyTorch
  * allocation is); rows may start at any element.
  *
