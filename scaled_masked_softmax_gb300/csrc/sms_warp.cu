@@ -386,11 +386,14 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_warp_kernel(const BwdArgs a)
 // paired elements use the packed fp32x2 forms).  fp32 rows are held in at
 // most 80 registers, three CTAs per multiprocessor: measured faster than two
 // CTAs with more registers (S=4099: 66% against 43% of the copy rate; S=1024:
-// +5%).  Not for the 16-bit forms (no gain, they would spill) nor for
-// misaligned fp32 rows of 6 or 8 vectors per lane (they would spill).
+// +5%).  Not for misaligned fp32 rows of 6 or 8 vectors per lane (they would
+// spill).  The 16-bit forms take three CTAs at 5 vectors per lane: the
+// misaligned ones then spill a few hundred bytes and still gain 9-11 points
+// over two CTAs (S=2049, 2500, 4099); at 4, 6 or 8 vectors two CTAs measured
+// no worse.
 template <typename T, int NV, bool ALIGNED> constexpr int fwd_min_ctas()
 {
-    return (Dt<T>::VEC == 4 && (ALIGNED || NV <= 5)) ? 3 : 2;
+    return (Dt<T>::VEC == 4 && (ALIGNED || NV <= 5)) ? 3 : (NV == 5 ? 3 : 2);
 }
 
 template <typename T, int G, int NV, bool ALIGNED>
@@ -447,7 +450,12 @@ cudaError_t launch_one(const Args &a, cudaStream_t st)
 }
 
 // (lanes per row, vectors per lane per row, rows per lane group), smallest
-// capacity first.  Capacity = G*NV vectors.  Each lane keeps RPG*NV vectors
+// capacity first.  Between the power-of-two lane counts, rows take 5, 6 or 7
+// vectors per lane on fewer lanes instead of twice the lanes half idle
+// (S = 1025 .. 1792 and 2049 .. 3584, often misaligned): measured +10 to +30
+// points there (f16 S=1025: 30% -> 59%, S=3500: 48% -> 62%; fp32 S=1100:
+// 64% -> 90%, S=3500: 84% -> 95% of the copy rate).  128 lanes x 7 is left out
+// of the 16-bit list: 256 x 4 measured faster for those rows (S=7000).  Capacity = G*NV vectors.  Each lane keeps RPG*NV vectors
 // per input stream in flight: 4 (5 for rows just past a power of two) for
 // every backward and 16-bit forward shape, up to 8 for the fp32 forward (its
 // mask stream is served by L2).  More vectors per lane stop fitting the 128
@@ -466,11 +474,13 @@ cudaError_t launch_t(const Args &a, cudaStream_t st)
     if (need <= (G) * (NV)) return launch_one<T, G, NV, (ALIGNED || (RPG) == 1 ? (RPG) : (RPG) / 2), ALIGNED, BWD>(a, st);
     if constexpr (VEC == 4 && !BWD) {
         SMS_TRY(4, 1, 8) SMS_TRY(4, 2, 4) SMS_TRY(8, 2, 4) SMS_TRY(8, 4, 2) SMS_TRY(16, 4, 2) SMS_TRY(32, 4, 2)
-        SMS_TRY(32, 8, 1) SMS_TRY(128, 4, 1) SMS_TRY(128, 5, 1) SMS_TRY(256, 4, 1) SMS_TRY(256, 5, 1)
+        SMS_TRY(32, 8, 1) SMS_TRY(64, 5, 1) SMS_TRY(64, 6, 1) SMS_TRY(64, 7, 1) SMS_TRY(128, 4, 1) SMS_TRY(128, 5, 1)
+        SMS_TRY(128, 6, 1) SMS_TRY(128, 7, 1) SMS_TRY(256, 4, 1) SMS_TRY(256, 5, 1)
         SMS_TRY(256, 6, 1) SMS_TRY(256, 8, 1)
     } else {
         SMS_TRY(4, 1, 4) SMS_TRY(4, 2, 2) SMS_TRY(4, 4, 1) SMS_TRY(8, 4, 1) SMS_TRY(16, 4, 1) SMS_TRY(32, 4, 1)
-        SMS_TRY(64, 4, 1) SMS_TRY(64, 5, 1) SMS_TRY(128, 4, 1) SMS_TRY(128, 5, 1) SMS_TRY(256, 4, 1)
+        SMS_TRY(32, 5, 1) SMS_TRY(32, 6, 1) SMS_TRY(32, 7, 1) SMS_TRY(64, 4, 1) SMS_TRY(64, 5, 1) SMS_TRY(64, 6, 1)
+        SMS_TRY(64, 7, 1) SMS_TRY(128, 4, 1) SMS_TRY(128, 5, 1) SMS_TRY(128, 6, 1) SMS_TRY(256, 4, 1)
         SMS_TRY(256, 5, 1)
         if constexpr (!BWD && ALIGNED) { SMS_TRY(256, 6, 1) SMS_TRY(256, 8, 1) }
     }

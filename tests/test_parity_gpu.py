@@ -23,7 +23,8 @@ pytestmark = pytest.mark.gpu
 
 DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 WIDTHS = [1, 2, 3, 5, 8, 13, 16, 31, 33, 64, 100, 127, 128, 129, 255, 256, 500, 512, 513, 1000, 1023, 1024,
-          1025, 1500, 2047, 2048, 2049, 3000, 4096, 4099, 5000, 8192, 12345, 16384, 20000, 32768, 40000]
+          1025, 1500, 1700, 1750, 2047, 2048, 2049, 3000, 3333, 3500, 4096, 4099, 5000, 8192, 12345, 16384, 20000,
+          32768, 40000]
 ROWS_FOR_PATH = {"auto": 300, "warp": 37, "stream": 2500, "ring": 3000, "cta": 1000, "online": 301}
 
 
@@ -82,7 +83,8 @@ def test_forward_mask_layouts(S, causal, kind, dt, path):
 
 @pytest.mark.parametrize("path", ["auto", "warp", "stream", "ring", "cta", "online"])
 @pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
-@pytest.mark.parametrize("S", [1, 3, 31, 64, 129, 1000, 1024, 2048, 2049, 4099, 8192, 16384, 20000])
+@pytest.mark.parametrize("S", [1, 3, 31, 64, 129, 1000, 1024, 1025, 1700, 1750, 2048, 2049, 3333, 3500, 4099, 8192,
+                               16384, 20000])
 def test_backward_widths(S, dt, path):
     rows = _budget_rows(S, ROWS_FOR_PATH[path])
     causal = S % 2 == 1 or S in (1024, 8192)
