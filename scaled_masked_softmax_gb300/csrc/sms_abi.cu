@@ -107,13 +107,13 @@ int pick_path(int forced, int64_t cols, int dtype, bool aligned, bool bwd, bool 
     //  * causal forward rows read a variable prefix; the per-warp bulk-copy
     //    rings keep enough of them in flight (registers do not): ring;
     //  * short aligned fp32 forward rows: the persistent prefetching groups;
-    //  * otherwise register-resident lane groups while a row fits them;
-    //  * 16-bit backward rows too wide for registers, or wide and starting
-    //    mid-vector: ring, then the staged CTA path while a row fits its
-    //    registers; beyond that, stream twice.
+    //  * otherwise register-resident lane groups while a row fits them
+    //    (misaligned 16-bit backward rows too: 65-75% of the copy rate at
+    //    S = 2049 .. 3333 against 43-57% on the rings);
+    //  * 16-bit backward rows too wide for registers: ring, then the staged
+    //    CTA path while a row fits its registers; beyond that, stream twice.
     if (!bwd && causal && aligned && ring_fits(cols, dtype, aligned)) return SMS_PATH_RING;
     if (!bwd && dtype == SMS_F32 && aligned && cols <= 512) return SMS_PATH_STREAM;
-    if (bwd && dtype != SMS_F32 && !aligned && cols > 2048 && ring_fits(cols, dtype, aligned)) return SMS_PATH_RING;
     if (warp_fits(cols, dtype, aligned, bwd)) return SMS_PATH_WARP;
     if (bwd && dtype != SMS_F32 && ring_fits(cols, dtype, aligned)) return SMS_PATH_RING;
     if (bwd ? cta_fits_bwd(cols, dtype, aligned) : cta_fits(cols, dtype, aligned)) return SMS_PATH_CTA;
