@@ -54,7 +54,7 @@ def _load():
             build()
             lib = ctypes.CDLL(_LIB)
             i64, dbl, vp, i32 = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int
-            lib.oracle_forward.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, vp, dbl, i32, i32, vp]
+            lib.oracle_forward.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, vp, i32, dbl, i32, i32, vp]
             lib.oracle_forward.restype = i32
             lib.oracle_backward.argtypes = [vp, i32, vp, i32, i64, i64, dbl, vp]
             lib.oracle_backward.restype = i32
@@ -120,7 +120,8 @@ def forward(x_rows, cols: int, scale: float, is_causal: bool = False, mask=None,
     ``row_index`` gives each row's logical index in the [rows, cols] view (for
     the causal position q = r mod cols and the mask row); default 0..n-1.
     ``key_lengths`` (one integer per batch b = r // (heads*cols)) keeps only
-    the keys j < key_lengths[b] (clamped to [0, cols]) of each row.
+    the keys j < key_lengths[b] (clamped to [0, cols]) of each row.  A mask of
+    torch.bool / numpy bool or uint8 is a boolean mask: nonzero masks the key.
     ``scale`` is used as given (pass the float32 value the kernel sees).
     Returns an fp64 array shaped like x_rows.
     """
@@ -129,10 +130,22 @@ def forward(x_rows, cols: int, scale: float, is_causal: bool = False, mask=None,
         raise ValueError("x size is not a multiple of cols")
     n = xa.size // cols
     ma = None
+    mask_kind = 0
     if mask is not None:
-        ma, mcode = _raw(mask, code)
-        if mcode != code:
-            raise ValueError("mask dtype must equal x dtype")
+        try:
+            import torch
+
+            if isinstance(mask, torch.Tensor) and mask.dtype in (torch.bool, torch.uint8):
+                mask = mask.detach().to("cpu").numpy()
+        except ImportError:  # pragma: no cover
+            pass
+        if isinstance(mask, np.ndarray) and mask.dtype in (np.bool_, np.uint8):
+            ma = np.ascontiguousarray(mask.astype(np.uint8))
+            mask_kind = 1
+        else:
+            ma, mcode = _raw(mask, code)
+            if mcode != code:
+                raise ValueError("mask dtype must equal x dtype")
     ri = None
     if row_index is not None:
         ri = np.ascontiguousarray(np.asarray(row_index, dtype=np.int64).reshape(-1))
@@ -156,7 +169,7 @@ def forward(x_rows, cols: int, scale: float, is_causal: bool = False, mask=None,
     rc = _load().oracle_forward(
         xa.ctypes.data, n, None if ri is None else ri.ctypes.data, cols,
         None if ma is None else ma.ctypes.data, mask_stride_b, mask_stride_h, heads,
-        None if la is None else la.ctypes.data, float(scale), int(bool(is_causal)), code, y.ctypes.data)
+        None if la is None else la.ctypes.data, mask_kind, float(scale), int(bool(is_causal)), code, y.ctypes.data)
     if rc != 0:
         raise ValueError("oracle_forward rejected its arguments")
     return y.reshape(xa.shape)

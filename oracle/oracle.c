@@ -26,6 +26,11 @@
  *     dot  = sum_j dy_j * y_j
  *     dx_j = (dy_j - dot) * y_j * scale           (the mask gets no gradient)
  *
+ * Boolean mask (mask_kind 1): one byte per element; a nonzero byte masks its
+ * key, s_j = -inf, and a zero byte leaves s_j = x_j * scale.  [P2 §2.2] names
+ * this form: the kernel overrides the true positions with -inf.  Same
+ * broadcast as the additive mask.
+ *
  * Key lengths (optional): row r of batch b keeps only the keys j < L_b,
  * L_b = lengths[b] clamped to [0, cols]; s_j = -inf for j >= L_b.  This is the
  * key-padding mask of [P3 §2.1] written as lengths; [P2 §2.2] makes a padded
@@ -139,15 +144,16 @@ void oracle_set_num_threads(int n)
  *   row_index logical row id of each of those rows in the [rows, cols] view
  *             (fixes q, b, h); NULL means 0..n_rows-1
  *   mask      NULL for no mask, else additive mask values of `dtype`
+ *             (mask_kind 0) or one byte per element, nonzero = masked (mask_kind 1)
  *   lengths   NULL, or the per-batch key lengths (int32, one per batch b)
  *   y         n_rows x cols fp64 output
  * Returns 0, or -1 for an argument it cannot interpret.
  */
 int oracle_forward(const void *x_rows, int64_t n_rows, const int64_t *row_index, int64_t cols,
                    const void *mask, int64_t mask_stride_b, int64_t mask_stride_h, int64_t heads,
-                   const int32_t *lengths, double scale, int is_causal, int dtype, double *y)
+                   const int32_t *lengths, int mask_kind, double scale, int is_causal, int dtype, double *y)
 {
-    if (!x_rows || !y || n_rows < 0 || cols <= 0 || heads <= 0 || !dtype_ok(dtype))
+    if (!x_rows || !y || n_rows < 0 || cols <= 0 || heads <= 0 || !dtype_ok(dtype) || mask_kind < 0 || mask_kind > 1)
         return -1;
     int64_t i;
 #pragma omp parallel for schedule(dynamic, 16)
@@ -169,8 +175,15 @@ int oracle_forward(const void *x_rows, int64_t n_rows, const int64_t *row_index,
 
         for (j = 0; j < cols; j++) {
             double v = load_elem(x_rows, i * cols + j, dtype) * scale;
-            if (mask)
-                v += load_elem(mask, b * mask_stride_b + h * mask_stride_h + q * cols + j, dtype);
+            if (mask) {
+                int64_t mi = b * mask_stride_b + h * mask_stride_h + q * cols + j;
+                if (mask_kind == 1) {
+                    if (((const uint8_t *)mask)[mi] != 0)
+                        v = -INFINITY;
+                } else {
+                    v += load_elem(mask, mi, dtype);
+                }
+            }
             if (is_causal && j > q)
                 v = -INFINITY;
             if (j >= kept)

@@ -42,6 +42,8 @@ def test_forward_closed_forms(case):
         dt = DT[dn]
         x = _arr(case["x"], dt)
         mask = _arr(case["mask"], dt) if "mask" in case else None
+        if "bool_mask" in case:
+            mask = torch.tensor(case["bool_mask"], dtype=torch.bool)
         scale = float(np.float32(_val(case["scale"])))
         y = oracle.forward(x, case["cols"], scale, case["is_causal"], mask,
                            case.get("mask_stride_b", 0), case.get("mask_stride_h", 0), case.get("heads", 1),
@@ -330,3 +332,42 @@ def test_key_lengths_with_row_index_and_clamping():
     assert np.array_equal(part, full[idx])
     assert np.all(full[: H * S] == 0.0)  # L = -5 -> 0: every key of batch 0 masked
     np.testing.assert_array_equal(full[2 * H * S:], oracle.forward(x[2 * H * S:], S, 1.0, True))  # L = 100 -> S
+
+
+# ----------------------------------------------------------- boolean masks ---
+
+@pytest.mark.parametrize("dt", [torch.float64, torch.float32, torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("kind", ["SS", "B1SS", "BHSS"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bool_mask_equals_additive_minus_inf_mask(dt, kind, causal):
+    """The boolean-mask path and the additive-mask path of the oracle are two
+    mechanisms; a boolean mask and the additive mask holding -inf where it is
+    true (0 elsewhere) must give the same result bit for bit, on every
+    broadcast layout."""
+    g = torch.Generator().manual_seed(61)
+    B, H, S = 2, 3, 29
+    x = (torch.randn(B * H * S, S, generator=g, dtype=torch.float64) * 8).to(dt)
+    shape = {"SS": (S, S), "B1SS": (B, 1, S, S), "BHSS": (B, H, S, S)}[kind]
+    sb, sh = {"SS": (0, 0), "B1SS": (S * S, 0), "BHSS": (H * S * S, S * S)}[kind]
+    bm = torch.rand(shape, generator=g) < 0.3
+    bm[..., 0] = False
+    bm.view(-1, S)[3] = True  # one fully masked mask row
+    add = torch.zeros(shape, dtype=torch.float64).masked_fill(bm, -math.inf).to(dt)
+    y_bool = oracle.forward(x, S, 0.125, causal, bm, sb, sh, H)
+    y_add = oracle.forward(x, S, 0.125, causal, add, sb, sh, H)
+    assert np.array_equal(y_bool, y_add)
+
+
+def test_bool_mask_matches_library_softmax():
+    """torch.softmax of the scores with the true positions filled with -inf
+    (rows with at least one kept key), uint8 and bool masks alike."""
+    g = torch.Generator().manual_seed(67)
+    S = 40
+    x = torch.randn(S, S, generator=g, dtype=torch.float64) * 8
+    bm = torch.rand(S, S, generator=g) < 0.5
+    bm[:, 7] = False
+    ref = torch.softmax((x * float(np.float32(0.125))).masked_fill(bm, -math.inf), -1).numpy()
+    for m in (bm, bm.to(torch.uint8) * 3):  # any nonzero byte masks
+        y = oracle.forward(x, S, 0.125, False, m)
+        np.testing.assert_allclose(y, ref, rtol=0, atol=1e-14)
+        assert np.all(y[bm.numpy()] == 0.0)
