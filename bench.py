@@ -86,11 +86,13 @@ def _kept_elems(w, inp) -> float:
     return float(lim.sum())
 
 
-def fwd_bytes(w, inp, lengths=False) -> int:
+def fwd_bytes(w, inp, lengths=False, mask_eb=None) -> int:
     """Algorithmic bytes of one forward: x read (only j <= q under causal),
-    unique mask bytes read (same causal rule), y written in full.  With key
-    lengths: x read only below min(L_b, q + 1), the lengths array, no mask."""
+    unique mask bytes read (same causal rule; mask_eb bytes per mask element,
+    1 for a boolean mask, else x's), y written in full.  With key lengths: x
+    read only below min(L_b, q + 1), the lengths array, no mask."""
     eb = w.elem_bytes
+    meb = eb if mask_eb is None else mask_eb
     rows, S = w.rows, w.cols
     if lengths:
         return int(_kept_elems(w, inp) * eb + inp["key_lengths"].numel() * 4 + rows * S * eb)
@@ -105,11 +107,11 @@ def fwd_bytes(w, inp, lengths=False) -> int:
         if w.mask == "B1SS":
             nb = math.ceil(rows / (w.H * S))
             per_q = (torch.arange(S, dtype=torch.float64) + 1).sum() if w.is_causal else S * S
-            mask_read = float(nb * per_q) * eb
+            mask_read = float(nb * per_q) * meb
         else:  # [S,S] (or full): rows touch min(rows, S) distinct mask rows per mask head
             nq = min(rows, S)
             per_q = float((torch.arange(nq, dtype=torch.float64) + 1).sum()) if w.is_causal else nq * S
-            mask_read = per_q * eb
+            mask_read = per_q * meb
     return int(x_read + mask_read + rows * S * eb)
 
 
@@ -242,9 +244,18 @@ def run_ours(args, rank, world, device):
     if use_len and inp["key_lengths"] is None:
         raise RuntimeError(f"--lengths: workload {w.name} has no key-padding mask")
     lptr = inp["key_lengths"].data_ptr() if use_len else None
+    use_bool = bool(getattr(args, "bool_mask", False))
+    if use_bool:
+        if mask is None or use_len:
+            raise RuntimeError(f"--bool-mask: workload {w.name} has no mask tensor (or --lengths is set)")
+        mbool = (mask != 0).contiguous()  # the workloads' masks hold 0 (kept) or -inf / -10000 (masked)
+        mptr = mbool.data_ptr()
 
     def fwd():
-        if use_len:
+        if use_bool:
+            rc = L.sms_forward_bool(x.data_ptr(), mptr, mnum, inp["mask_stride_b"], inp["mask_stride_h"],
+                                    inp["heads"], y.data_ptr(), w.rows, w.cols, w.scale, int(w.is_causal), dt, st)
+        elif use_len:
             rc = L.sms_forward_lengths(x.data_ptr(), lptr, w.H, y.data_ptr(), w.rows, w.cols, w.scale,
                                        int(w.is_causal), dt, st)
         else:
@@ -263,7 +274,7 @@ def run_ours(args, rank, world, device):
         if rc:
             raise RuntimeError(sms.sms_last_error())
 
-    fb, bb = fwd_bytes(w, inp, use_len), bwd_bytes(w, inp, use_len)
+    fb, bb = fwd_bytes(w, inp, use_len, 1 if use_bool else None), bwd_bytes(w, inp, use_len)
     step_bytes = fb + bb
     working_set = (x.numel() * 4 * x.element_size()) + (0 if mask is None else mask.numel() * mask.element_size())
     flush = working_set < 2 * L2_BYTES
@@ -368,7 +379,8 @@ def run_ours(args, rank, world, device):
         "vs_baseline": None, "dtype": DTYPE_NAME[x.dtype], "data": "synthetic (seeded, see workloads.py)",
         "config": {"workload": w.name, "shape": [w.B, w.H, w.S, w.S] if w.rows_override is None else [w.rows, w.S],
                    "rows": w.rows, "cols": w.cols,
-                   "mask": ("key lengths int32 [B] (sms_forward_lengths)" if use_len else w.mask),
+                   "mask": ("key lengths int32 [B] (sms_forward_lengths)" if use_len else
+                            f"{w.mask} as bytes (sms_forward_bool)" if use_bool else w.mask),
                    "is_causal": w.is_causal,
                    "step": "forward + backward (dy ~ N(0,1))", "scale": w.scale,
                    "l2": ("flushed between steps (2x L2 write), step = kernel time" if flush
@@ -552,6 +564,8 @@ def main():
                     help="also time the step replayed from a CUDA graph of N steps (launch-bound shapes)")
     ap.add_argument("--lengths", action="store_true",
                     help="key-padding workloads through the key-length entry points instead of the [B,1,S,S] mask")
+    ap.add_argument("--bool-mask", action="store_true",
+                    help="masked workloads with the mask as one byte per element (sms_forward_bool)")
     args = ap.parse_args()
 
     world, rank, local = dist_env()

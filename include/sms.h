@@ -115,6 +115,31 @@ SMS_API int sms_forward(const void *x, const void *mask, int64_t mask_numel, int
                 int is_causal, int dtype, void *stream);
 
 /*
+ * Forward with a boolean mask.  The page "用CUDA自定义融合Softmax算子并封装进PyTorch"
+ * §2.2 starts from a boolean mask (true = the key is masked) and turns it into
+ * the additive one as mask * (-inf) before the kernel; here the kernel reads
+ * the boolean mask itself, one byte per element:
+ *       s_j = -inf if mask_row(r)[j] != 0, else x_j * scale
+ *       s_j = -inf if is_causal and j > q;  y as in sms_forward
+ * which is bit for bit sms_forward with the additive mask holding -inf where
+ * the byte is nonzero and 0 elsewhere, at a quarter (fp32) or half (fp16,
+ * bf16) of that mask's bytes.  A row with every key masked gives y = 0.
+ *   mask      device array of mask_numel bytes (torch.bool / uint8 storage),
+ *             16-byte aligned, not NULL; any nonzero byte masks its key
+ *   mask_stride_b, mask_stride_h, heads
+ *             as in sms_forward, in elements (= bytes) of the mask
+ *   other arguments as sms_forward; y may equal x and must not overlap the mask.
+ * The backward is sms_backward (the mask only shapes y).
+ * Errors as sms_forward, plus SMS_ERR_INVALID_ARG for a NULL mask (rows > 0)
+ * and SMS_ERR_UNSUPPORTED when SMS_PATH_CTA is forced: every kernel family
+ * but the staged CTA one reads the boolean mask, and the rows the dispatcher
+ * would give that family go to SMS_PATH_ONLINE.
+ */
+SMS_API int sms_forward_bool(const void *x, const uint8_t *mask, int64_t mask_numel, int64_t mask_stride_b,
+                             int64_t mask_stride_h, int64_t heads, void *y, int64_t rows, int64_t cols, float scale,
+                             int is_causal, int dtype, void *stream);
+
+/*
  * Backward.  dx[r, j] = (dy[r, j] - sum_k dy[r, k] * y[r, k]) * y[r, j] * scale.
  *   y              forward output [rows, cols] (device, `dtype`)
  *   dy             upstream gradient [rows, cols] (device, `dtype`)

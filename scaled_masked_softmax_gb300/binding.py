@@ -23,6 +23,7 @@ PATH_NAMES = {SMS_PATH_AUTO: "auto", SMS_PATH_WARP: "warp", SMS_PATH_CTA: "cta",
 _i64, _i32, _f32, _vp, _cp = ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_char_p
 SIGNATURES = {
     "sms_forward": (_i32, [_vp, _vp, _i64, _i64, _i64, _i64, _vp, _i64, _i64, _f32, _i32, _i32, _vp]),
+    "sms_forward_bool": (_i32, [_vp, _vp, _i64, _i64, _i64, _i64, _vp, _i64, _i64, _f32, _i32, _i32, _vp]),
     "sms_backward": (_i32, [_vp, _vp, _vp, _i64, _i64, _f32, _i32, _i32, _vp]),
     "sms_forward_lengths": (_i32, [_vp, _vp, _i64, _vp, _i64, _i64, _f32, _i32, _i32, _vp]),
     "sms_backward_lengths": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _f32, _i32, _i32, _vp]),
@@ -78,6 +79,13 @@ def sms_forward(x, mask, mask_numel, mask_stride_b, mask_stride_h, heads, y, row
     """Raw pointers in, status checked: see include/sms.h."""
     _check(lib().sms_forward(x, mask, mask_numel, mask_stride_b, mask_stride_h, heads, y, rows, cols, scale,
                              int(bool(is_causal)), dtype, stream))
+
+
+def sms_forward_bool(x, mask, mask_numel, mask_stride_b, mask_stride_h, heads, y, rows, cols, scale, is_causal,
+                     dtype, stream) -> None:
+    """Boolean mask (one byte per element, nonzero = masked): see include/sms.h."""
+    _check(lib().sms_forward_bool(x, mask, mask_numel, mask_stride_b, mask_stride_h, heads, y, rows, cols, scale,
+                                  int(bool(is_causal)), dtype, stream))
 
 
 def sms_backward(y, dy, dx, rows, cols, scale, is_causal_hint, dtype, stream) -> None:

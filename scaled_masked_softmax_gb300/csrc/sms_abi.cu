@@ -188,11 +188,12 @@ int sms_select_path(int64_t rows, int64_t cols, int dtype, int is_backward)
 
 namespace {
 
-// Validation and dispatch shared by sms_forward and sms_forward_lengths
-// (`who` names the entry point in error messages).
+// Validation and dispatch shared by sms_forward, sms_forward_bool and
+// sms_forward_lengths (`who` names the entry point in error messages;
+// mask_bool: the mask holds one byte per element).
 int forward_impl(const char *who, const void *x, const void *mask, int64_t mask_numel, int64_t mask_stride_b,
                  int64_t mask_stride_h, int64_t heads, const int32_t *lengths, void *y, int64_t rows, int64_t cols,
-                 float scale, int is_causal, int dtype, void *stream)
+                 float scale, int is_causal, int dtype, void *stream, bool mask_bool = false)
 {
     t_err[0] = '\0';
     if (dtype < SMS_F32 || dtype > SMS_BF16) return fail(SMS_ERR_INVALID_ARG, "%s: unknown dtype %d", who, dtype);
@@ -233,7 +234,7 @@ int forward_impl(const char *who, const void *x, const void *mask, int64_t mask_
             if (ext > mask_numel)
                 return fail(SMS_ERR_INVALID_ARG, "%s: rows reach mask element %lld but mask_numel is %lld", who,
                             (long long)ext - 1, (long long)mask_numel);
-            if (overlap(mask, mask_numel * eb, y, total * eb))
+            if (overlap(mask, mask_numel * (mask_bool ? 1 : eb), y, total * eb))
                 return fail(SMS_ERR_INVALID_ARG, "%s: y overlaps the mask", who);
         }
     } else if (!lengths && heads <= 0) {
@@ -244,6 +245,19 @@ int forward_impl(const char *who, const void *x, const void *mask, int64_t mask_
         return SMS_OK;
     }
 
+    const int vec = vec_elems(dtype);
+    const bool aligned = cols % vec == 0 && (!mask || (mask_stride_b % vec == 0 && mask_stride_h % vec == 0));
+    int path = pick_path(g_forced.load(), cols, dtype, aligned, false, is_causal != 0);
+    if (mask_bool) {
+        // byte masks are read by every family but the staged CTA path, whose
+        // producer stages additive mask rows; its rows go to the two-pass kernel
+        if (path == SMS_PATH_CTA) {
+            if (g_forced.load() == SMS_PATH_CTA)
+                return fail(SMS_ERR_UNSUPPORTED, "%s: the CTA path does not read a boolean mask", who);
+            path = SMS_PATH_ONLINE;
+        }
+    }
+
     int dev = 0, nsm = 0;
     int *err = nullptr;
     cudaError_t e = device_info(dev, nsm, err);
@@ -252,8 +266,6 @@ int forward_impl(const char *who, const void *x, const void *mask, int64_t mask_
         return fail(SMS_ERR_CUDA, "%s: device query failed: %s", who, cuda_msg(e));
     }
 
-    const int vec = vec_elems(dtype);
-    const bool aligned = cols % vec == 0 && (!mask || (mask_stride_b % vec == 0 && mask_stride_h % vec == 0));
     FwdArgs a;
     a.x = x; a.mask = mask; a.y = y;
     a.rows = rows; a.cols = cols; a.x_total = total;
@@ -263,8 +275,8 @@ int forward_impl(const char *who, const void *x, const void *mask, int64_t mask_
     a.dcols = FastDiv((uint32_t)cols);
     a.dheads = FastDiv((uint32_t)heads);
     a.lengths = lengths;
+    a.mask_bool = (mask && mask_bool) ? 1 : 0;
 
-    const int path = pick_path(g_forced.load(), cols, dtype, aligned, false, a.causal != 0);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (path) {
     case SMS_PATH_WARP:
@@ -386,6 +398,18 @@ int sms_forward(const void *x, const void *mask, int64_t mask_numel, int64_t mas
 {
     return forward_impl("sms_forward", x, mask, mask_numel, mask_stride_b, mask_stride_h, heads, nullptr, y, rows,
                         cols, scale, is_causal, dtype, stream);
+}
+
+int sms_forward_bool(const void *x, const uint8_t *mask, int64_t mask_numel, int64_t mask_stride_b,
+                     int64_t mask_stride_h, int64_t heads, void *y, int64_t rows, int64_t cols, float scale,
+                     int is_causal, int dtype, void *stream)
+{
+    if (!mask && rows != 0) {
+        t_err[0] = '\0';
+        return fail(SMS_ERR_INVALID_ARG, "sms_forward_bool: mask must not be NULL");
+    }
+    return forward_impl("sms_forward_bool", x, mask, mask_numel, mask_stride_b, mask_stride_h, heads, nullptr, y,
+                        rows, cols, scale, is_causal, dtype, stream, true);
 }
 
 int sms_forward_lengths(const void *x, const int32_t *lengths, int64_t heads, void *y, int64_t rows, int64_t cols,

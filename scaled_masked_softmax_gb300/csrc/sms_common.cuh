@@ -127,6 +127,79 @@ template <int VEC> __device__ __forceinline__ uint4 window(const uint4 &lo, cons
 __device__ __forceinline__ uint4 ld_stream(const void *p) { return __ldcs(reinterpret_cast<const uint4 *>(p)); }
 __device__ __forceinline__ uint4 ld_keep(const void *p) { return __ldg(reinterpret_cast<const uint4 *>(p)); }
 __device__ __forceinline__ void st_stream(void *p, const uint4 &v) { __stcs(reinterpret_cast<uint4 *>(p), v); }
+
+// ---------------------------------------------------------- mask elements ---
+// A mask is additive (element type M == T, added to x*scale) or boolean (M ==
+// uint8_t, one byte per element, nonzero = the key is masked and its score is
+// -inf).  MaskIO<T, M> moves the mask elements under one 16-byte x vector
+// (VEC elements): one 16-byte load for an additive mask, VEC bytes in .x (and
+// .y) for a boolean one.  A boolean element becomes the additive value 0 or
+// -inf, so x*scale + m is computed by the same instruction either way and a
+// boolean mask gives bit for bit the result of its additive -inf twin.
+template <typename T, typename M> struct MaskIO;
+
+template <typename T> struct MaskIO<T, T> {
+    static constexpr int VEC = Dt<T>::VEC;
+    static __device__ __forceinline__ uint4 ld(const T *p) { return ld_keep(p); }
+    static __device__ __forceinline__ void unpack_m(const uint4 &v, float *f) { unpack<T>(v, f); }
+    template <int S> static __device__ __forceinline__ uint4 win(const uint4 &lo, const uint4 &hi)
+    {
+        return window_fixed<VEC, S>(lo, hi);
+    }
+    static __device__ __forceinline__ uint4 win_rt(const uint4 &lo, const uint4 &hi, int s)
+    {
+        return window<VEC>(lo, hi, s);
+    }
+    static __device__ __forceinline__ float elem(const T *p) { return to_f32<T>(*p); }
+};
+
+template <typename T> struct MaskIO<T, uint8_t> {
+    static constexpr int VEC = Dt<T>::VEC;
+    static __device__ __forceinline__ uint4 ld(const uint8_t *p)
+    {
+        if constexpr (VEC == 4) {
+            return make_uint4(__ldg(reinterpret_cast<const unsigned int *>(p)), 0u, 0u, 0u);
+        } else {
+            const uint2 v = __ldg(reinterpret_cast<const uint2 *>(p));
+            return make_uint4(v.x, v.y, 0u, 0u);
+        }
+    }
+    static __device__ __forceinline__ void unpack_m(const uint4 &v, float *f)
+    {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            const uint32_t w = e < 4 ? v.x : v.y;
+            f[e] = ((w >> (8 * (e & 3))) & 0xffu) ? neg_inf() : 0.f;
+        }
+    }
+    // Bytes S .. S+VEC-1 of the 2*VEC bytes held by two consecutive VEC-byte
+    // groups (lo, hi).
+    template <int S> static __device__ __forceinline__ uint4 win(const uint4 &lo, const uint4 &hi)
+    {
+        if constexpr (S == 0) return lo;
+        if constexpr (VEC == 4) {
+            return make_uint4(__funnelshift_r(lo.x, hi.x, 8 * S), 0u, 0u, 0u);
+        } else {
+            const uint32_t w[4] = {lo.x, lo.y, hi.x, hi.y};
+            constexpr int q = S / 4, b = 8 * (S % 4);
+            return make_uint4(__funnelshift_r(w[q], w[q + 1], b), __funnelshift_r(w[q + 1], w[q + 2], b), 0u, 0u);
+        }
+    }
+    static __device__ __forceinline__ uint4 win_rt(const uint4 &lo, const uint4 &hi, int s)
+    {
+        switch (s) {
+        case 0: return lo;
+        case 1: return win<1>(lo, hi);
+        case 2: return win<2>(lo, hi);
+        case 3: return win<3>(lo, hi);
+        case 4: return win<4 % VEC>(lo, hi);
+        case 5: return win<5 % VEC>(lo, hi);
+        case 6: return win<6 % VEC>(lo, hi);
+        default: return win<7 % VEC>(lo, hi);
+        }
+    }
+    static __device__ __forceinline__ float elem(const uint8_t *p) { return *p ? neg_inf() : 0.f; }
+};
 // ------------------------------------------------------------ arithmetic ---
 // 2^x on the special-function unit (PTX ex2.approx, subnormal results flushed
 // to zero; 2^-inf = +0).

@@ -27,6 +27,7 @@ struct FwdArgs {
     int *err;              // device error word
     FastDiv dcols, dheads; // division by cols and by heads
     const int32_t *lengths;  // per-batch key lengths (device), nullptr: none
+    int mask_bool;         // 1: the mask holds one byte per element (nonzero = masked), 0: additive, dtype of x
 };
 
 struct BwdArgs {
@@ -46,10 +47,13 @@ struct BwdArgs {
 
 // "aligned" means every row (and every mask row) starts on a 16-byte boundary:
 // cols and both mask strides are multiples of the 16-byte vector width.
+// A boolean mask (FwdArgs::mask_bool) is taken by every forward family but
+// the staged CTA one.
 
 // warp-per-row (or a power-of-two part of a warp per row), rows in registers
 bool warp_fits(int64_t cols, int dtype, bool aligned, bool bwd);
-cudaError_t launch_fwd_warp(const FwdArgs &a, int dtype, bool aligned, cudaStream_t st);
+cudaError_t launch_fwd_warp(const FwdArgs &a, int dtype, bool aligned, cudaStream_t st);  // either mask kind
+cudaError_t launch_fwd_warp_bool(const FwdArgs &a, int dtype, bool aligned, cudaStream_t st);
 cudaError_t launch_bwd_warp(const BwdArgs &a, int dtype, bool aligned, cudaStream_t st);
 
 
@@ -69,7 +73,7 @@ bool cta_fits_bwd(int64_t cols, int dtype, bool aligned);  // backward (y and dy
 cudaError_t launch_fwd_cta(const FwdArgs &a, int dtype, bool aligned, cudaStream_t st);
 cudaError_t launch_bwd_cta(const BwdArgs &a, int dtype, bool aligned, cudaStream_t st);
 
-// streaming two pass, any row length
+// streaming two pass, any row length (either mask kind)
 cudaError_t launch_fwd_online(const FwdArgs &a, int dtype, cudaStream_t st);
 cudaError_t launch_bwd_online(const BwdArgs &a, int dtype, cudaStream_t st);
 

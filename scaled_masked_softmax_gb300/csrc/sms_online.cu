@@ -44,11 +44,12 @@ __device__ __forceinline__ OnlineRow online_geom(int64_t r, int64_t cols, int ca
 }
 
 // Scores of vector vi of the row (-inf outside [0, limit)).
-template <typename T, bool KEEP>
-__device__ __forceinline__ void load_scores(const FwdArgs &a, const OnlineRow &g, const T *xs, const T *ms,
+template <typename T, typename M, bool KEEP>
+__device__ __forceinline__ void load_scores(const FwdArgs &a, const OnlineRow &g, const T *xs, const M *ms,
                                             int64_t m0, bool mvec, int vi, float *s)
 {
     constexpr int VEC = Dt<T>::VEC;
+    using MIO = MaskIO<T, M>;
     const int j0 = vi * VEC - g.xoff;
     float xv[VEC], mv[VEC];
 #pragma unroll
@@ -63,12 +64,12 @@ __device__ __forceinline__ void load_scores(const FwdArgs &a, const OnlineRow &g
     }
     if (ms) {
         if (mvec && m0 + j0 + VEC <= a.mask_total) {
-            unpack<T>(ld_keep(ms + j0), mv);
+            MIO::unpack_m(MIO::ld(ms + j0), mv);
         } else {
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
                 const int j = j0 + e;
-                if (j >= 0 && j < g.limit) mv[e] = to_f32<T>(ms[j]);
+                if (j >= 0 && j < g.limit) mv[e] = MIO::elem(ms + j);
             }
         }
     }
@@ -89,7 +90,7 @@ __device__ __forceinline__ void merge_ml(float &m, float &l, float m2, float l2)
     l = a + b;
 }
 
-template <typename T>
+template <typename T, typename M>
 __global__ void __launch_bounds__(kNT) fwd_online_kernel(const FwdArgs a)
 {
     constexpr int VEC = Dt<T>::VEC;
@@ -101,12 +102,12 @@ __global__ void __launch_bounds__(kNT) fwd_online_kernel(const FwdArgs a)
         split_row(r, a.cols, a.heads, a.dcols, a.dheads, q, hh, bb);
         const OnlineRow g = online_geom<VEC>(r, a.cols, a.causal, q, a.lengths, bb);
         const T *xs = reinterpret_cast<const T *>(a.x) + (g.x0 - g.xoff);
-        const T *ms = nullptr;
+        const M *ms = nullptr;
         int64_t m0 = 0;
         bool mvec = false;
         if (a.mask) {
             m0 = bb * a.msb + hh * a.msh + q * a.cols;
-            ms = reinterpret_cast<const T *>(a.mask) + m0;
+            ms = reinterpret_cast<const M *>(a.mask) + m0;
             mvec = ((m0 - g.xoff) & (VEC - 1)) == 0;
         }
 
@@ -119,7 +120,7 @@ __global__ void __launch_bounds__(kNT) fwd_online_kernel(const FwdArgs a)
             for (int u = 0; u < kU; ++u) {
                 const int vi = base + u * kNT + t;
                 if (vi < g.nv_read) {
-                    load_scores<T, true>(a, g, xs, ms, m0, mvec, vi, s[u]);
+                    load_scores<T, M, true>(a, g, xs, ms, m0, mvec, vi, s[u]);
                 } else {
 #pragma unroll
                     for (int e = 0; e < VEC; ++e) s[u][e] = neg_inf();
@@ -162,7 +163,7 @@ __global__ void __launch_bounds__(kNT) fwd_online_kernel(const FwdArgs a)
                 if (vi >= g.nv_row) continue;
                 float s[VEC];
                 if (vi < g.nv_read) {
-                    load_scores<T, false>(a, g, xs, ms, m0, mvec, vi, s);
+                    load_scores<T, M, false>(a, g, xs, ms, m0, mvec, vi, s);
                 } else {
 #pragma unroll
                     for (int e = 0; e < VEC; ++e) s[e] = neg_inf();
@@ -294,9 +295,15 @@ cudaError_t launch_persistent(K kern, const Args &a, cudaStream_t st)
 cudaError_t launch_fwd_online(const FwdArgs &a, int dtype, cudaStream_t st)
 {
     switch (dtype) {
-    case kF32: return launch_persistent(fwd_online_kernel<float>, a, st);
-    case kF16: return launch_persistent(fwd_online_kernel<__half>, a, st);
-    case kBF16: return launch_persistent(fwd_online_kernel<__nv_bfloat16>, a, st);
+    case kF32:
+        return a.mask_bool ? launch_persistent(fwd_online_kernel<float, uint8_t>, a, st)
+                           : launch_persistent(fwd_online_kernel<float, float>, a, st);
+    case kF16:
+        return a.mask_bool ? launch_persistent(fwd_online_kernel<__half, uint8_t>, a, st)
+                           : launch_persistent(fwd_online_kernel<__half, __half>, a, st);
+    case kBF16:
+        return a.mask_bool ? launch_persistent(fwd_online_kernel<__nv_bfloat16, uint8_t>, a, st)
+                           : launch_persistent(fwd_online_kernel<__nv_bfloat16, __nv_bfloat16>, a, st);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -22,6 +22,8 @@
 // copies it still has in flight and leaves.
 #include <atomic>
 
+#include <type_traits>
+
 #include "sms_rowmath.cuh"
 
 namespace sms {
@@ -126,10 +128,12 @@ __device__ __forceinline__ void ring_issue(const FwdArgs &fa, const BwdArgs &ba,
 }
 
 // One row per group of G = 32*WG lanes.  MB: the stages carry the mask (or
-// dy); a forward without MB reads its mask, if any, from global memory.
-template <typename T, int G, int NV, int K, bool MB, bool ALIGNED, bool BWD>
+// dy); a forward without MB reads its mask, if any, from global memory, with
+// M its element type (T: additive, uint8_t: boolean; staged masks are additive).
+template <typename T, int G, int NV, int K, bool MB, bool ALIGNED, bool BWD, typename M>
 __global__ void __launch_bounds__(ring_groups<G, NV, K, MB>() * G, 1) ring_kernel(const FwdArgs fa, const BwdArgs ba)
 {
+    static_assert(!MB || BWD || std::is_same<M, T>::value, "a staged mask is additive");
     constexpr int VEC = Dt<T>::VEC;
     constexpr int GPC = ring_groups<G, NV, K, MB>();
     constexpr int W = G / 32;
@@ -222,7 +226,7 @@ __global__ void __launch_bounds__(ring_groups<G, NV, K, MB>() * G, 1) ring_kerne
             if (ok && p.fast && p.limit > 0) {
                 const uint4 *A4 = reinterpret_cast<const uint4 *>(st);
                 const uint4 *M4 = reinterpret_cast<const uint4 *>(st + Geo::B_OFF);
-                const T *mk = reinterpret_cast<const T *>(fa.mask) + p.mA;
+                const M *mk = reinterpret_cast<const M *>(fa.mask) + p.mA;
 #pragma unroll
                 for (int k = 0; k < NV; ++k) {
                     const int vi = k * G + gl;
@@ -237,15 +241,15 @@ __global__ void __launch_bounds__(ring_groups<G, NV, K, MB>() * G, 1) ring_kerne
                                 if (p.msh) B.m2[k] = M4[vi + 1];
                             }
                         } else if (fa.mask) {  // a mask shared by many rows: read through L2 by the lanes
-                            B.m[k] = ld_keep(mk + vi * VEC);
+                            B.m[k] = MaskIO<T, M>::ld(mk + vi * VEC);
                             if constexpr (!ALIGNED) {
-                                if (p.msh) B.m2[k] = ld_keep(mk + vi * VEC + VEC);
+                                if (p.msh) B.m2[k] = MaskIO<T, M>::ld(mk + vi * VEC + VEC);
                             }
                         }
                     }
                 }
             } else {
-                fwd_issue<T, G, NV, ALIGNED>(fa, p, gl, B);
+                fwd_issue<T, G, NV, ALIGNED, M>(fa, p, gl, B);
             }
             fence_proxy_async_smem();
             if constexpr (W == 1) {
@@ -254,7 +258,7 @@ __global__ void __launch_bounds__(ring_groups<G, NV, K, MB>() * G, 1) ring_kerne
                     ring_issue<T, G, NV, MB, ALIGNED, BWD>(fa, ba, rn, st, &bars[s], polA, polB);
             }
             float sc[NV][VEC];
-            const float fac = fwd_reduce<T, G, NV, ALIGNED>(fa, p, gl, gi, B, sc, reinterpret_cast<float(*)[W]>(h.red_m[rp]),
+            const float fac = fwd_reduce<T, G, NV, ALIGNED, M>(fa, p, gl, gi, B, sc, reinterpret_cast<float(*)[W]>(h.red_m[rp]),
                                                             reinterpret_cast<float(*)[W]>(h.red_l[rp]), bar_id);
             if (W == 1 ? !ok : *abort_flag != 0) { failed = true; break; }  // group-uniform: after the barrier
             if constexpr (W > 1) {
@@ -280,12 +284,12 @@ __global__ void __launch_bounds__(ring_groups<G, NV, K, MB>() * G, 1) ring_kerne
     }
 }
 
-template <typename T, int G, int NV, int K, bool MB, bool ALIGNED, bool BWD>
+template <typename T, int G, int NV, int K, bool MB, bool ALIGNED, bool BWD, typename M>
 cudaError_t launch_ring(const FwdArgs &fa, const BwdArgs &ba, cudaStream_t st)
 {
     constexpr int smem = ring_smem<G, NV, K, MB>();
     constexpr int GPC = ring_groups<G, NV, K, MB>();
-    auto kern = ring_kernel<T, G, NV, K, MB, ALIGNED, BWD>;
+    auto kern = ring_kernel<T, G, NV, K, MB, ALIGNED, BWD, M>;
     static std::atomic<int> attr_done[64];  // per device: the shared-memory limit has been raised
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -309,14 +313,14 @@ constexpr int kStages = 3;
 // Rows of up to 2048 vectors: one warp with 1, 2, 4 or 8 vectors per lane,
 // then groups of 2 to 8 warps with 6 or 8 (the 6-vector groups keep rows
 // just past a power of two, 4099 say, from doubling their stage and group).
-template <typename T, bool MB, bool ALIGNED, bool BWD>
+template <typename T, bool MB, bool ALIGNED, bool BWD, typename M = T>
 cudaError_t launch_t(const FwdArgs &fa, const BwdArgs &ba, cudaStream_t st)
 {
     constexpr int VEC = Dt<T>::VEC;
     const int64_t cols = BWD ? ba.cols : fa.cols;
     const int64_t need = (cols + VEC - 1) / VEC + (ALIGNED ? 0 : 1);
 #define SMS_RING(G, NV) \
-    if (need <= (G) * (NV)) return launch_ring<T, G, NV, kStages, MB, ALIGNED, BWD>(fa, ba, st);
+    if (need <= (G) * (NV)) return launch_ring<T, G, NV, kStages, MB, ALIGNED, BWD, M>(fa, ba, st);
     SMS_RING(32, 1) SMS_RING(32, 2) SMS_RING(32, 4) SMS_RING(32, 8) SMS_RING(64, 8) SMS_RING(96, 6)
     SMS_RING(128, 8) SMS_RING(192, 6) SMS_RING(256, 8)
 #undef SMS_RING
@@ -327,7 +331,9 @@ cudaError_t launch_t(const FwdArgs &fa, const BwdArgs &ba, cudaStream_t st)
 // of different heads or batches do not share it): it travels through the
 // stages with x.  A smaller mask is shared by many rows and is served by L2;
 // the lanes read it directly and the stages hold x alone (twice the groups).
-inline bool stage_mask(const FwdArgs &fa) { return fa.mask && fa.mask_total * 4 >= fa.x_total; }
+// A boolean mask (a quarter or half of x's bytes per element) is always read
+// by the lanes.
+inline bool stage_mask(const FwdArgs &fa) { return fa.mask && !fa.mask_bool && fa.mask_total * 4 >= fa.x_total; }
 
 template <typename T, bool BWD>
 cudaError_t launch_dt(const FwdArgs &fa, const BwdArgs &ba, bool aligned, cudaStream_t st)
@@ -335,6 +341,9 @@ cudaError_t launch_dt(const FwdArgs &fa, const BwdArgs &ba, bool aligned, cudaSt
     if constexpr (BWD) {
         return aligned ? launch_t<T, true, true, true>(fa, ba, st) : launch_t<T, true, false, true>(fa, ba, st);
     } else {
+        if (fa.mask_bool)
+            return aligned ? launch_t<T, false, true, false, uint8_t>(fa, ba, st)
+                           : launch_t<T, false, false, false, uint8_t>(fa, ba, st);
         if (stage_mask(fa))
             return aligned ? launch_t<T, true, true, false>(fa, ba, st) : launch_t<T, true, false, false>(fa, ba, st);
         return aligned ? launch_t<T, false, true, false>(fa, ba, st) : launch_t<T, false, false, false>(fa, ba, st);

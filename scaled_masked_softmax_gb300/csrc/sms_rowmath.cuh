@@ -122,12 +122,13 @@ template <int NV, bool ALIGNED> struct FwdBuf {
 // vectors per x vector when the mask row is misaligned relative to x).  The
 // per-vector bounds tests of rows at the ends of the buffers live in their
 // own loop: one warp-uniform branch per row keeps them out of the common path.
-template <typename T, int G, int NV, bool ALIGNED>
+template <typename T, int G, int NV, bool ALIGNED, typename M = T>
 __device__ __forceinline__ void fwd_issue(const FwdArgs &a, const RowPos &p, int gl, FwdBuf<NV, ALIGNED> &B)
 {
     constexpr int VEC = Dt<T>::VEC;
+    using MIO = MaskIO<T, M>;
     const T *xs = reinterpret_cast<const T *>(a.x) + p.xb;
-    const T *mk = reinterpret_cast<const T *>(a.mask) + p.mA;
+    const M *mk = reinterpret_cast<const M *>(a.mask) + p.mA;
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
         B.x[k] = make_uint4(0, 0, 0, 0);
@@ -141,9 +142,9 @@ __device__ __forceinline__ void fwd_issue(const FwdArgs &a, const RowPos &p, int
             if (vi * VEC - p.xoff < p.limit) {
                 B.x[k] = ld_stream(xs + vi * VEC);
                 if (a.mask) {
-                    B.m[k] = ld_keep(mk + vi * VEC);
+                    B.m[k] = MIO::ld(mk + vi * VEC);
                     if constexpr (!ALIGNED) {
-                        if (p.msh) B.m2[k] = ld_keep(mk + vi * VEC + VEC);
+                        if (p.msh) B.m2[k] = MIO::ld(mk + vi * VEC + VEC);
                     }
                 }
             }
@@ -157,8 +158,8 @@ __device__ __forceinline__ void fwd_issue(const FwdArgs &a, const RowPos &p, int
                 if (a.mask) {
                     const int64_t mb = p.mA + (int64_t)vi * VEC;
                     if (mb >= 0 && mb + (p.msh ? 2 : 1) * VEC <= a.mask_total) {
-                        B.m[k] = ld_keep(mk + vi * VEC);
-                        if (p.msh) B.m2[k] = ld_keep(mk + vi * VEC + VEC);
+                        B.m[k] = MIO::ld(mk + vi * VEC);
+                        if (p.msh) B.m2[k] = MIO::ld(mk + vi * VEC + VEC);
                     }
                 }
             }
@@ -167,24 +168,25 @@ __device__ __forceinline__ void fwd_issue(const FwdArgs &a, const RowPos &p, int
 }
 
 // Realign all NV mask vectors by the row's shift: one switch per row.
-template <int VEC, int NV, int S>
+template <typename MIO, int NV, int S>
 __device__ __forceinline__ void realign_fixed(uint4 (&m)[NV], const uint4 (&m2)[NV])
 {
 #pragma unroll
-    for (int k = 0; k < NV; ++k) m[k] = window_fixed<VEC, S>(m[k], m2[k]);
+    for (int k = 0; k < NV; ++k) m[k] = MIO::template win<S>(m[k], m2[k]);
 }
-template <int VEC, int NV>
+template <typename MIO, int NV>
 __device__ __forceinline__ void realign(uint4 (&m)[NV], const uint4 (&m2)[NV], int s)
 {
+    constexpr int VEC = MIO::VEC;
     switch (s) {
     case 0: break;
-    case 1: realign_fixed<VEC, NV, 1>(m, m2); break;
-    case 2: realign_fixed<VEC, NV, 2>(m, m2); break;
-    case 3: realign_fixed<VEC, NV, 3>(m, m2); break;
-    case 4: realign_fixed<VEC, NV, 4 % VEC>(m, m2); break;
-    case 5: realign_fixed<VEC, NV, 5 % VEC>(m, m2); break;
-    case 6: realign_fixed<VEC, NV, 6 % VEC>(m, m2); break;
-    default: realign_fixed<VEC, NV, 7 % VEC>(m, m2); break;
+    case 1: realign_fixed<MIO, NV, 1>(m, m2); break;
+    case 2: realign_fixed<MIO, NV, 2>(m, m2); break;
+    case 3: realign_fixed<MIO, NV, 3>(m, m2); break;
+    case 4: realign_fixed<MIO, NV, 4 % VEC>(m, m2); break;
+    case 5: realign_fixed<MIO, NV, 5 % VEC>(m, m2); break;
+    case 6: realign_fixed<MIO, NV, 6 % VEC>(m, m2); break;
+    default: realign_fixed<MIO, NV, 7 % VEC>(m, m2); break;
     }
 }
 
@@ -215,7 +217,7 @@ __device__ __forceinline__ void score_vec(const float (&xv)[VEC], const float (&
 
 // Scores of vector slot k on the common path: every vector read lies inside
 // x and the mask, and the mask is already realigned.
-template <typename T, int G, int NV, bool ALIGNED>
+template <typename T, int G, int NV, bool ALIGNED, typename M = T>
 __device__ __forceinline__ void fwd_scores(const FwdArgs &a, const RowPos &p, int gl, int k,
                                            const FwdBuf<NV, ALIGNED> &B, float (&s)[Dt<T>::VEC], float &mx)
 {
@@ -223,7 +225,7 @@ __device__ __forceinline__ void fwd_scores(const FwdArgs &a, const RowPos &p, in
     float xv[VEC], mv[VEC];
     unpack<T>(B.x[k], xv);
     if (a.mask) {
-        unpack<T>(B.m[k], mv);
+        MaskIO<T, M>::unpack_m(B.m[k], mv);
     } else {
 #pragma unroll
         for (int e = 0; e < VEC; ++e) mv[e] = 0.f;
@@ -233,11 +235,12 @@ __device__ __forceinline__ void fwd_scores(const FwdArgs &a, const RowPos &p, in
 
 // Scores of vector slot k of a row at an end of x or of the mask buffer:
 // partial vectors are read element by element.
-template <typename T, int G, int NV>
+template <typename T, int G, int NV, typename M = T>
 __device__ __forceinline__ void fwd_scores_edge(const FwdArgs &a, const RowPos &p, int gl, int k,
                                                 const FwdBuf<NV, false> &B, float (&s)[Dt<T>::VEC], float &mx)
 {
     constexpr int VEC = Dt<T>::VEC;
+    using MIO = MaskIO<T, M>;
     const int vi = k * G + gl;
     const int j0 = vi * VEC - p.xoff;
     float xv[VEC], mv[VEC];
@@ -245,7 +248,7 @@ __device__ __forceinline__ void fwd_scores_edge(const FwdArgs &a, const RowPos &
 #pragma unroll
     for (int e = 0; e < VEC; ++e) mv[e] = 0.f;
     const T *xs = reinterpret_cast<const T *>(a.x) + p.xb;
-    const T *ms = reinterpret_cast<const T *>(a.mask) + p.mA + p.msh;  // ms[vi*VEC + e]: element j0 + e
+    const M *ms = reinterpret_cast<const M *>(a.mask) + p.mA + p.msh;  // ms[vi*VEC + e]: element j0 + e
     if (j0 < p.limit) {
         if (p.xb + (int64_t)(vi + 1) * VEC > a.x_total) {  // last partial vector of the tensor
 #pragma unroll
@@ -255,12 +258,12 @@ __device__ __forceinline__ void fwd_scores_edge(const FwdArgs &a, const RowPos &
         if (a.mask) {
             const int64_t mb = p.mA + (int64_t)vi * VEC;
             if (mb >= 0 && mb + (p.msh ? 2 : 1) * VEC <= a.mask_total) {
-                unpack<T>(window<VEC>(B.m[k], B.m2[k], p.msh), mv);
+                MIO::unpack_m(MIO::win_rt(B.m[k], B.m2[k], p.msh), mv);
             } else {  // mask vectors at the ends of the mask buffer: element loads
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) {
                     const int j = j0 + e;
-                    mv[e] = (j >= 0 && j < p.limit) ? to_f32<T>(ms[vi * VEC + e]) : 0.f;
+                    mv[e] = (j >= 0 && j < p.limit) ? MIO::elem(ms + vi * VEC + e) : 0.f;
                 }
             }
         }
@@ -302,7 +305,7 @@ template <int G> __device__ __forceinline__ void group_barrier(int bar)
 // Scores, exponentials and the row's normalisation factor: s holds the
 // exponentials on return.  red_m / red_l: this call's shared slots
 // [group][warp] (multi-warp groups only).
-template <typename T, int G, int NV, bool ALIGNED>
+template <typename T, int G, int NV, bool ALIGNED, typename M = T>
 __device__ __forceinline__ float fwd_reduce(const FwdArgs &a, const RowPos &p, int gl, int gi,
                                             FwdBuf<NV, ALIGNED> &B, float (&s)[NV][Dt<T>::VEC],
                                             float (*red_m)[G > 32 ? G / 32 : 1], float (*red_l)[G > 32 ? G / 32 : 1],
@@ -313,13 +316,13 @@ __device__ __forceinline__ float fwd_reduce(const FwdArgs &a, const RowPos &p, i
     float mx = neg_inf();
     if (ALIGNED || p.fast) {
         if constexpr (!ALIGNED) {
-            if (a.mask) realign<VEC, NV>(B.m, B.m2, p.msh);
+            if (a.mask) realign<MaskIO<T, M>, NV>(B.m, B.m2, p.msh);
         }
 #pragma unroll
-        for (int k = 0; k < NV; ++k) fwd_scores<T, G, NV, ALIGNED>(a, p, gl, k, B, s[k], mx);
+        for (int k = 0; k < NV; ++k) fwd_scores<T, G, NV, ALIGNED, M>(a, p, gl, k, B, s[k], mx);
     } else if constexpr (!ALIGNED) {
 #pragma unroll
-        for (int k = 0; k < NV; ++k) fwd_scores_edge<T, G, NV>(a, p, gl, k, B, s[k], mx);
+        for (int k = 0; k < NV; ++k) fwd_scores_edge<T, G, NV, M>(a, p, gl, k, B, s[k], mx);
     }
 
     if constexpr (G <= 32) {
@@ -392,13 +395,13 @@ __device__ __forceinline__ void fwd_store(const FwdArgs &a, const RowPos &p, int
 
 // Reduce, normalise and store row p from its loaded buffer (every thread of
 // the CTA calls this equally often when G > 32 and bar == 0).
-template <typename T, int G, int NV, bool ALIGNED>
+template <typename T, int G, int NV, bool ALIGNED, typename M = T>
 __device__ __forceinline__ void fwd_finish(const FwdArgs &a, const RowPos &p, int gl, int gi,
                                            FwdBuf<NV, ALIGNED> &B, float (*red_m)[G > 32 ? G / 32 : 1],
                                            float (*red_l)[G > 32 ? G / 32 : 1], int bar = 0)
 {
     float s[NV][Dt<T>::VEC];
-    const float fac = fwd_reduce<T, G, NV, ALIGNED>(a, p, gl, gi, B, s, red_m, red_l, bar);
+    const float fac = fwd_reduce<T, G, NV, ALIGNED, M>(a, p, gl, gi, B, s, red_m, red_l, bar);
     fwd_store<T, G, NV, ALIGNED>(a, p, gl, s, fac);
 }
 

@@ -17,6 +17,8 @@
 // by the CTA's first row), so the multi-warp groups' __syncthreads are
 // reached uniformly; the shared reduction slots alternate between two halves
 // so a fast warp never overwrites slots another warp is still reading.
+#include <type_traits>
+
 #include "sms_rowmath.cuh"
 
 namespace sms {
@@ -26,7 +28,7 @@ constexpr int kThreads = 256;
 
 using namespace rowmath;
 
-template <typename T, int G, int NV, bool ALIGNED>
+template <typename T, int G, int NV, bool ALIGNED, typename M>
 __global__ void __launch_bounds__(kThreads, 2) fwd_stream_kernel(const FwdArgs a)
 {
     constexpr int VEC = Dt<T>::VEC;
@@ -39,22 +41,22 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_stream_kernel(const FwdArgs a
     int64_t base = (int64_t)blockIdx.x * GPC;  // the CTA's first row: drives the (CTA-uniform) loop
     FwdBuf<NV, ALIGNED> A, B;
     RowPos pa = fwd_pos<VEC, ALIGNED>(a, base + gi), pb;
-    fwd_issue<T, G, NV, ALIGNED>(a, pa, gl, A);
+    fwd_issue<T, G, NV, ALIGNED, M>(a, pa, gl, A);
     while (true) {
         const bool more1 = base + stride < a.rows;
         if (more1) {
             pb = fwd_pos<VEC, ALIGNED>(a, base + stride + gi);
-            fwd_issue<T, G, NV, ALIGNED>(a, pb, gl, B);
+            fwd_issue<T, G, NV, ALIGNED, M>(a, pb, gl, B);
         }
-        fwd_finish<T, G, NV, ALIGNED>(a, pa, gl, gi, A, red_m[0], red_l[0]);
+        fwd_finish<T, G, NV, ALIGNED, M>(a, pa, gl, gi, A, red_m[0], red_l[0]);
         if (!more1) break;
         base += stride;
         const bool more2 = base + stride < a.rows;
         if (more2) {
             pa = fwd_pos<VEC, ALIGNED>(a, base + stride + gi);
-            fwd_issue<T, G, NV, ALIGNED>(a, pa, gl, A);
+            fwd_issue<T, G, NV, ALIGNED, M>(a, pa, gl, A);
         }
-        fwd_finish<T, G, NV, ALIGNED>(a, pb, gl, gi, B, red_m[1], red_l[1]);
+        fwd_finish<T, G, NV, ALIGNED, M>(a, pb, gl, gi, B, red_m[1], red_l[1]);
         if (!more2) break;
         base += stride;
     }
@@ -109,7 +111,7 @@ int resident_ctas(K kern)
     return per_sm;
 }
 
-template <typename T, int G, int NV, bool ALIGNED, bool BWD, typename Args>
+template <typename T, int G, int NV, bool ALIGNED, bool BWD, typename M, typename Args>
 cudaError_t launch_one(const Args &a, cudaStream_t st)
 {
     constexpr int GPC = kThreads / G;
@@ -122,15 +124,15 @@ cudaError_t launch_one(const Args &a, cudaStream_t st)
         cfg.gridDim = dim3((unsigned)persistent_grid(per_sm, useful));
         return cudaLaunchKernelEx(&cfg, bwd_stream_kernel<T, G, NV, ALIGNED>, a);
     } else {
-        static const int per_sm = resident_ctas(fwd_stream_kernel<T, G, NV, ALIGNED>);
+        static const int per_sm = resident_ctas(fwd_stream_kernel<T, G, NV, ALIGNED, M>);
         cfg.gridDim = dim3((unsigned)persistent_grid(per_sm, useful));
-        return cudaLaunchKernelEx(&cfg, fwd_stream_kernel<T, G, NV, ALIGNED>, a);
+        return cudaLaunchKernelEx(&cfg, fwd_stream_kernel<T, G, NV, ALIGNED, M>, a);
     }
 }
 
 // (lanes per row, vectors per lane), smallest capacity first; one row per
 // group, two row buffers per lane.
-template <typename T, bool ALIGNED, bool BWD, typename Args>
+template <typename T, bool ALIGNED, bool BWD, typename M, typename Args>
 cudaError_t launch_t(const Args &a, cudaStream_t st)
 {
     constexpr int VEC = Dt<T>::VEC;
@@ -141,23 +143,30 @@ cudaError_t launch_t(const Args &a, cudaStream_t st)
     } else {
         const int64_t need = (a.cols + VEC - 1) / VEC + (ALIGNED ? 0 : 1);
 #define SMS_TRY(G, NV) \
-    if (need <= (G) * (NV)) return launch_one<T, G, NV, ALIGNED, BWD>(a, st);
+    if (need <= (G) * (NV)) return launch_one<T, G, NV, ALIGNED, BWD, M>(a, st);
         SMS_TRY(4, 4) SMS_TRY(8, 4) SMS_TRY(16, 4) SMS_TRY(32, 4) SMS_TRY(64, 4) SMS_TRY(128, 4) SMS_TRY(256, 4)
 #undef SMS_TRY
         return cudaErrorNotSupported;
     }
 }
 
-template <bool BWD, typename Args>
+// MASKB: the forward's mask is boolean (one byte per element), else additive.
+template <bool BWD, bool MASKB, typename Args>
 cudaError_t dispatch(const Args &a, int dtype, bool aligned, cudaStream_t st)
 {
     switch (dtype) {
-    case kF32:
-        return aligned ? launch_t<float, true, BWD>(a, st) : launch_t<float, false, BWD>(a, st);
-    case kF16:
-        return aligned ? launch_t<__half, true, BWD>(a, st) : launch_t<__half, false, BWD>(a, st);
-    case kBF16:
-        return aligned ? launch_t<__nv_bfloat16, true, BWD>(a, st) : launch_t<__nv_bfloat16, false, BWD>(a, st);
+    case kF32: {
+        using M = std::conditional_t<MASKB, uint8_t, float>;
+        return aligned ? launch_t<float, true, BWD, M>(a, st) : launch_t<float, false, BWD, M>(a, st);
+    }
+    case kF16: {
+        using M = std::conditional_t<MASKB, uint8_t, __half>;
+        return aligned ? launch_t<__half, true, BWD, M>(a, st) : launch_t<__half, false, BWD, M>(a, st);
+    }
+    case kBF16: {
+        using M = std::conditional_t<MASKB, uint8_t, __nv_bfloat16>;
+        return aligned ? launch_t<__nv_bfloat16, true, BWD, M>(a, st) : launch_t<__nv_bfloat16, false, BWD, M>(a, st);
+    }
     default:
         return cudaErrorInvalidValue;
     }
@@ -173,12 +182,12 @@ bool stream_fits(int64_t cols, int dtype, bool aligned, bool bwd)
 
 cudaError_t launch_fwd_stream(const FwdArgs &a, int dtype, bool aligned, cudaStream_t st)
 {
-    return dispatch<false>(a, dtype, aligned, st);
+    return a.mask_bool ? dispatch<false, true>(a, dtype, aligned, st) : dispatch<false, false>(a, dtype, aligned, st);
 }
 
 cudaError_t launch_bwd_stream(const BwdArgs &a, int dtype, bool aligned, cudaStream_t st)
 {
-    return dispatch<true>(a, dtype, aligned, st);
+    return dispatch<true, false>(a, dtype, aligned, st);
 }
 
 }  // namespace sms

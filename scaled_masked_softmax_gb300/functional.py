@@ -4,9 +4,11 @@ The shape conventions follow the page "用CUDA自定义融合Softmax算子并封
 x is an attention-score tensor [B, H, S, S] (any leading dims; rows = numel /
 size(-1), §4.2), the mask is additive, of x's dtype, and may be omitted (§2.2);
 ``ScaledMaskSoftmaxFunction`` keeps only the output y for the backward and
-returns no gradient for mask, scale or is_causal (§4.3).  Boolean masks must be
-converted by the caller, e.g. ``mask.to(x.dtype) * -inf`` with 0 where kept
-(§2.2 and §5.1 warn that adding a bool mask as 1.0 is wrong).  A key-padding
+returns no gradient for mask, scale or is_causal (§4.3).  A torch.bool (or
+uint8) mask is a boolean mask, true = masked key: §2.2 converts it to the
+additive ``mask * -inf`` before the kernel (and §5.1 warns that adding it as
+1.0 is wrong); here the kernel reads the bytes itself, with the result of
+that additive mask bit for bit and a quarter / half of its bytes.  A key-padding
 mask can instead be given as ``key_lengths`` (int32 [B], the valid keys of
 each batch): the same result as the additive mask with -inf beyond L_b, with
 no mask tensor read and the padded scores never read.
@@ -83,7 +85,8 @@ def _key_lengths(key_lengths: torch.Tensor, x_shape, device) -> tuple:
 def forward(x: torch.Tensor, mask: Optional[torch.Tensor] = None, scale: float = 1.0, is_causal: bool = False,
             out: Optional[torch.Tensor] = None, key_lengths: Optional[torch.Tensor] = None) -> torch.Tensor:
     """y = softmax(x * scale + mask) over the last dim, j > q masked if is_causal,
-    keys j >= key_lengths[b] masked when key_lengths is given."""
+    keys j >= key_lengths[b] masked when key_lengths is given.  A torch.bool
+    mask masks the keys where it is true (score -inf)."""
     if not x.is_cuda:
         raise ValueError("x must be a CUDA tensor (there is no CPU path)")
     if x.dtype not in _DTYPE_CODE:
@@ -101,6 +104,7 @@ def forward(x: torch.Tensor, mask: Optional[torch.Tensor] = None, scale: float =
             (y.numel() and y.data_ptr() % 16):
         raise ValueError("out must be a contiguous, 16-byte aligned tensor like x")
     mptr, mnum, sb, sh, heads = None, 0, 0, 0, (x.shape[-3] if x.dim() >= 3 else 1)
+    mask_bool = False
     if key_lengths is not None:
         if mask is not None:
             raise ValueError("give either an additive mask or key_lengths, not both")
@@ -113,9 +117,9 @@ def forward(x: torch.Tensor, mask: Optional[torch.Tensor] = None, scale: float =
                                         float(scale), bool(is_causal), dt, stream)
         return y
     if mask is not None:
-        if mask.dtype != x.dtype:
-            raise TypeError(f"mask dtype {mask.dtype} must equal x dtype {x.dtype} (convert a bool mask "
-                            "to an additive one first)")
+        mask_bool = mask.dtype in (torch.bool, torch.uint8)
+        if not mask_bool and mask.dtype != x.dtype:
+            raise TypeError(f"mask dtype {mask.dtype} must equal x dtype {x.dtype}, or be torch.bool")
         if mask.device != x.device:
             raise ValueError("mask must be on x's device")
         sb, sh, heads = mask_layout(x.shape, mask.shape)
@@ -125,6 +129,10 @@ def forward(x: torch.Tensor, mask: Optional[torch.Tensor] = None, scale: float =
         return y
     with torch.cuda.device(x.device):
         stream = torch.cuda.current_stream(x.device).cuda_stream
+        if mask_bool:  # torch.bool stores one byte per element, 0 or 1
+            binding.sms_forward_bool(x.data_ptr(), mptr, mnum, sb, sh, heads, y.data_ptr(), rows, cols, float(scale),
+                                     bool(is_causal), dt, stream)
+            return y
         binding.sms_forward(x.data_ptr(), mptr, mnum, sb, sh, heads, y.data_ptr(), rows, cols, float(scale),
                             bool(is_causal), dt, stream)
     return y

@@ -145,3 +145,13 @@ def check_backward(dx_gpu: np.ndarray, y: np.ndarray, dy: np.ndarray, scale: flo
 
 def make(w, device="cuda"):
     return workloads.make_inputs(w, device=device)
+
+
+def raw_forward_bool(x, mask, sb, sh, heads, w, y=None):
+    """sms_forward_bool through the C ABI: ``mask`` is a bool / uint8 device
+    tensor read one byte per element (nonzero = masked)."""
+    y = torch.empty_like(x) if y is None else y
+    dt = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}[x.dtype]
+    sms.sms_forward_bool(x.data_ptr(), mask.data_ptr(), mask.numel(), sb, sh, heads, y.data_ptr(), w.rows, w.cols,
+                         w.scale, w.is_causal, dt, torch.cuda.current_stream().cuda_stream)
+    return y

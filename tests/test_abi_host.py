@@ -209,3 +209,48 @@ def test_lengths_entry_points_pass_validation():
     assert _bwd_len(heads=2, causal=1) == binding.SMS_ERR_CUDA
     assert _fwd_len(rows=0) == binding.SMS_OK
     assert _bwd_len(rows=0) == binding.SMS_OK
+
+
+def _fwd_bool(**kw):
+    a = dict(x=0x10000, mask=0x40000, mask_numel=64, sb=0, sh=0, heads=1, y=0x20000, rows=8, cols=8, scale=1.0,
+             causal=0, dtype=0, stream=None)
+    a.update(kw)
+    return binding.lib().sms_forward_bool(a["x"], a["mask"], a["mask_numel"], a["sb"], a["sh"], a["heads"], a["y"],
+                                          a["rows"], a["cols"], a["scale"], a["causal"], a["dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("kw", [
+    dict(mask=None), dict(x=None), dict(dtype=4), dict(cols=0), dict(scale=float("nan")), dict(heads=0),
+    dict(mask=0x40008),  # misaligned mask
+    dict(mask_numel=63),  # [S,S] byte mask one element short
+    dict(mask_numel=64, rows=16, sb=64),  # 2 batches reach byte 127
+    dict(mask=0x1fff0, mask_numel=64),  # y (bytes 0x20000..) overlaps the last 48 mask bytes
+])
+def test_forward_bool_rejects_bad_arguments(kw):
+    assert _fwd_bool(**kw) == INVALID
+    assert binding.sms_last_error().startswith("sms_forward_bool")
+
+
+def test_forward_bool_mask_extent_is_counted_in_bytes():
+    # a byte mask of 64 elements ends 64 bytes after its start: y may begin
+    # right there even for fp32 x, where an additive mask would be 256 bytes
+    if torch.cuda.is_available():
+        pytest.skip("host-only check")
+    assert _fwd_bool(mask=0x20000 - 64, dtype=0) == binding.SMS_ERR_CUDA
+    assert _fwd(mask=0x20000 - 64, mask_numel=64, rows=8, cols=8) == INVALID
+
+
+def test_forward_bool_paths():
+    # the byte mask is read by every family but the staged CTA one, which is
+    # refused before any device access; a no-op stays a no-op
+    if torch.cuda.is_available():
+        pytest.skip("host-only check")
+    for path, want in [(sms.SMS_PATH_RING, binding.SMS_ERR_CUDA), (sms.SMS_PATH_CTA, UNSUPPORTED),
+                       (sms.SMS_PATH_STREAM, binding.SMS_ERR_CUDA), (sms.SMS_PATH_WARP, binding.SMS_ERR_CUDA),
+                       (sms.SMS_PATH_ONLINE, binding.SMS_ERR_CUDA), (sms.SMS_PATH_AUTO, binding.SMS_ERR_CUDA)]:
+        prev = sms.sms_set_forced_path(path)
+        try:
+            assert _fwd_bool() == want, path
+        finally:
+            sms.sms_set_forced_path(prev)
+    assert _fwd_bool(rows=0, mask=None, x=None, y=None) == binding.SMS_OK
