@@ -154,7 +154,7 @@ def _sample_rows(rows, cols, n, seed):
 
 
 @pytest.mark.parametrize("name", ["keypad_causal_bf16_s4096", "sweep_f16_s4099", "sweep_f32_s1024",
-                                  "sweep_f32_s16384"])
+                                  "sweep_f32_s4099", "sweep_f32_s16384"])
 def test_full_size_bool_mask(name):
     """Full-size workloads whose masks are 0 / -inf, with the mask given as
     bytes: sampled rows against the oracle, and bit-equal on those rows to the
