@@ -1,0 +1,52 @@
+"""The algorithmic bytes bench.py divides by (the roofline's numerator),
+checked on small workloads by enumerating what each row reads and writes:
+x at the kept positions (j <= q under causal), every distinct mask element
+the rows touch (at the mask's element size: x's for an additive mask, one
+byte for a boolean one), y / dx in full; y and dy at the kept positions in
+the backward."""
+import dataclasses
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from scaled_masked_softmax_gb300 import workloads  # noqa: E402
+
+
+def _enumerate(w, inp, mask_eb):
+    S, rows, eb = w.cols, w.rows, w.elem_bytes
+    msb, msh, H = inp["mask_stride_b"], inp["mask_stride_h"], inp["heads"]
+    x_read, mask_idx = 0, set()
+    for r in range(rows):
+        q, h, b = r % S, (r // S) % H, r // (S * H)
+        kept = q + 1 if w.is_causal else S
+        x_read += kept
+        if inp["mask"] is not None:
+            base = b * msb + h * msh + q * S
+            mask_idx.update(range(base, base + kept))
+    fwd = x_read * eb + len(mask_idx) * mask_eb + rows * S * eb
+    bwd = 2 * x_read * eb + rows * S * eb
+    return fwd, bwd
+
+
+@pytest.mark.parametrize("name", ["tiny_causal_f32", "keypad_f32_s1024", "keypad_causal_bf16_s4096",
+                                  "sweep_f16_s1000", "sweep_f32_s4099"])
+@pytest.mark.parametrize("boolean", [False, True])
+def test_algorithmic_bytes_match_enumeration(name, boolean):
+    w = workloads.WORKLOADS[name]
+    if w.rows_override is not None:  # [S,S] sweep: fewer rows than S, and more rows than S
+        small = [dataclasses.replace(w, S=24, rows_override=17), dataclasses.replace(w, S=24, rows_override=61)]
+    else:
+        small = [workloads.scaled(w, B=2, H=3, S=20)]
+    for ws in small:
+        inp = workloads.make_inputs(ws, device="cpu", with_dy=False)
+        if boolean and inp["mask"] is None:
+            continue
+        meb = 1 if boolean else None
+        want_f, want_b = _enumerate(ws, inp, 1 if boolean else ws.elem_bytes)
+        assert bench.fwd_bytes(ws, inp, False, meb) == want_f, ws
+        assert bench.bwd_bytes(ws, inp) == want_b, ws
