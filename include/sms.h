@@ -117,8 +117,10 @@ SMS_API int sms_forward(const void *x, const void *mask, int64_t mask_numel, int
 /*
  * Forward with a boolean mask.  The page "用CUDA自定义融合Softmax算子并封装进PyTorch"
  * §2.2 starts from a boolean mask (true = the key is masked) and turns it into
- * the additive one as mask * (-inf) before the kernel; here the kernel reads
- * the boolean mask itself, one byte per element:
+ * the additive one as mask * (-inf) before the kernel; the second article
+ * (pnsm.cn/news/1983787, §2.3) has the operator read a 0/1 mask itself and
+ * use -inf where it is 1.  Here the kernel reads the boolean mask, one byte
+ * per element:
  *       s_j = -inf if mask_row(r)[j] != 0, else x_j * scale
  *       s_j = -inf if is_causal and j > q;  y as in sms_forward
  * which is bit for bit sms_forward with the additive mask holding -inf where
