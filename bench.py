@@ -499,9 +499,54 @@ def run_cpu_baseline(w, inp_cpu, seconds):
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    return {"value": round(done_bytes / el / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{n_rows} rows of {w.name} (fwd+bwd, fp64, {chunk}-row chunks spread over the tensor), "
-                      f"{el:.1f} s", "rows_per_s": round(n_rows / el, 1)}
+    res = {"value": round(done_bytes / el / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+           "sample": f"{n_rows} rows of {w.name} (fwd+bwd, fp64, {chunk}-row chunks spread over the tensor), "
+                     f"{el:.1f} s", "rows_per_s": round(n_rows / el, 1), "cpu": _cpu_model()}
+    # the same oracle on one thread, over a shorter sample of the same rows
+    prev = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        c1 = max(16, chunk // 8)
+        t0 = time.perf_counter()
+        b1, r1, start = 0, 0, 0
+        while True:
+            idx = _oracle_sample(w, inp_cpu, c1, start)
+            b1 += _sample_bytes(w, idx, inp_cpu)
+            r1 += c1
+            start += c1 * 97
+            el1 = time.perf_counter() - t0
+            if el1 >= max(1.0, seconds / 4):
+                break
+    finally:
+        oracle.set_num_threads(prev)
+    res["single_thread"] = {"value": round(b1 / el1 / 1e9, 4), "unit": "GB/s", "rows_per_s": round(r1 / el1, 1),
+                            "sample": f"{r1} rows, {el1:.1f} s"}
+    return res
+
+
+def _cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (x86: model name; Arm: implementer and part codes)."""
+    import platform
+
+    name, impl, part = None, None, None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                k, v = k.strip(), v.strip()
+                if k == "model name" and name is None:
+                    name = v
+                elif k == "CPU implementer" and impl is None:
+                    impl = v
+                elif k == "CPU part" and part is None:
+                    part = v
+    except OSError:
+        pass
+    if name:
+        return name
+    if impl or part:
+        return f"{platform.machine()} implementer {impl} part {part}"
+    return platform.machine()
 
 
 def run_reference(args, rank, world):
@@ -538,7 +583,7 @@ def run_reference(args, rank, world):
         "config": {"workload": w.name, "rows": w.rows, "cols": w.cols, "mask": w.mask, "is_causal": w.is_causal,
                    "step": "forward + backward on a bounded row sample"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "cpu": _cpu_model()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

@@ -50,3 +50,16 @@ def test_algorithmic_bytes_match_enumeration(name, boolean):
         want_f, want_b = _enumerate(ws, inp, 1 if boolean else ws.elem_bytes)
         assert bench.fwd_bytes(ws, inp, False, meb) == want_f, ws
         assert bench.bwd_bytes(ws, inp) == want_b, ws
+
+
+def test_cpu_baseline_reports_all_cores_and_one_thread():
+    import oracle
+
+    w = workloads.scaled(workloads.WORKLOADS["keypad_f32_s1024"], B=2, H=2, S=64)
+    inp = workloads.make_inputs(w, device="cpu", with_dy=True)
+    before = oracle.num_threads()
+    r = bench.run_cpu_baseline(w, inp, 0.2)
+    assert oracle.num_threads() == before  # the one-thread leg restores the thread count
+    assert r["kind"] == "oracle" and r["cores"] == before and r["value"] > 0 and r["rows_per_s"] > 0
+    assert r["single_thread"]["value"] > 0 and r["single_thread"]["rows_per_s"] > 0
+    assert isinstance(r["cpu"], str) and r["cpu"]
