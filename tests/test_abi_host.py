@@ -254,3 +254,12 @@ def test_forward_bool_paths():
         finally:
             sms.sms_set_forced_path(prev)
     assert _fwd_bool(rows=0, mask=None, x=None, y=None) == binding.SMS_OK
+
+
+def test_build_compiles_every_kernel_source():
+    # a translation unit left out of the build list would drop its kernels
+    # (and, for the boolean-mask warp kernels, an entry point's launches)
+    from scaled_masked_softmax_gb300 import build
+
+    cu = sorted(f for f in os.listdir(build.CSRC) if f.endswith(".cu"))
+    assert sorted(build.SOURCES) == cu
