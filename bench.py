@@ -4,8 +4,9 @@
 One step = one pass of the whole hot path over one batch: the forward
 (load + scale + mask + causal, row max, exp + sum, normalise + store) and the
 backward (row dot, gradient) through the C ABI, on inputs already resident in
-HBM.  Default workload: [8,32,1024,1024] fp32 scores with an [8,1,1024,1024]
-key-padding mask (-10000 fill), forward then backward with dy ~ N(0,1).
+HBM.  Default workload: [4,32,4096,4096] bf16 scores (d_k = 128, scale
+1/sqrt(128)) with a [4,1,4096,4096] key-padding mask (-inf fill) and the causal
+flag, forward then backward (with the causal hint) with dy ~ N(0,1).
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
 instead, on bounded samples of the same workload.  ``--all`` additionally
@@ -21,6 +22,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -30,9 +32,10 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 METRIC = "fused masked-softmax fwd/bwd achieved HBM GB/s and % of GB300 peak; rows/s"
-DEFAULT_WORKLOAD = "keypad_f32_s1024"
+DEFAULT_WORKLOAD = "keypad_causal_bf16_s4096"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal
 DTYPE_NAME = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}
 
 
@@ -145,12 +148,12 @@ class ClockSampler:
         except Exception:
             self.sel = []
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = None
 
     def start(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.f = open(self.path, "w")
+            fd, self.path = tempfile.mkstemp(prefix="sms_clocks_", suffix=".csv")
+            self.f = os.fdopen(fd, "w")
             self.proc = subprocess.Popen(["nvidia-smi"] + self.sel + [f"--query-gpu={self.Q}",
                                           "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
@@ -170,20 +173,25 @@ class ClockSampler:
         self.f.close()
         sm, mx, reasons = [], None, set()
         with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    s, m = float(parts[1]), float(parts[2])
-                except ValueError:
-                    continue
-                sm.append(s)
-                mx = m
-                for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
-                                   parts[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(name)
+            lines = f.readlines()
+        try:
+            os.unlink(self.path)
+        except OSError:
+            pass
+        for line in lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                s, m = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            sm.append(s)
+            mx = m
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                               parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
@@ -223,11 +231,24 @@ def aggregate_gbs(step_bytes, world, step_ms):
 
 # ------------------------------------------------------------------ ours ---
 
+def _workload(args):
+    """The named workload, or (``--bh B,H``) the same distributions at another
+    batch and head count (small profiling captures of the same kernels)."""
+    from scaled_masked_softmax_gb300 import workloads
+
+    w = workloads.WORKLOADS[args.workload]
+    bh = getattr(args, "bh", None)
+    if bh:
+        b, h = (int(v) for v in bh.split(","))
+        w = workloads.scaled(w, B=b, H=h)
+    return w
+
+
 def run_ours(args, rank, world, device):
     import scaled_masked_softmax_gb300 as sms
     from scaled_masked_softmax_gb300 import workloads
 
-    w = workloads.WORKLOADS[args.workload]
+    w = _workload(args)
     torch.cuda.set_device(device)
     inp = workloads.make_inputs(w, device=device, with_dy=True)
     x, mask, dy = inp["x"], inp["mask"], inp["dy"]
@@ -336,9 +357,17 @@ def run_ours(args, rank, world, device):
 
     kernels = {"forward": _kernel(fwd_path, fwd_ms, fb), "backward": _kernel(bwd_path, bwd_ms, bb)}
     dom = "backward" if b_ms * K >= f_ms * K else "forward"
-    traffic = _traffic_record(w.name, dom)
+    wkey = w.name + ("+lengths" if use_len else "+bool" if use_bool else "")
+    traffic = _traffic_record(wkey, dom)
     roof = {"kernel": dom, "bound": "hbm", "achieved": kernels[dom]["gbs"], "peak": peak, "unit": "GB/s",
-            "frac": round(kernels[dom]["gbs"] / peak, 4), "traffic": traffic, "peak_source": peak_kind}
+            "frac": round(kernels[dom]["gbs"] / peak, 4), "traffic": traffic, "peak_source": peak_kind,
+            "frac_of_nominal": round(kernels[dom]["gbs"] / NOMINAL_HBM_GBS, 4),
+            # DRAM bytes the profiler counted per launch over the same event-timed launch duration
+            "traffic_gbs": None if traffic is None else round(traffic / kernels[dom]["ms"] / 1e6, 1)}
+    for name, k in kernels.items():
+        t = _traffic_record(wkey, name)
+        k["ncu_dram_bytes"] = t
+        k["ncu_dram_gbs"] = None if t is None else round(t / k["ms"] / 1e6, 1)
 
     graph = None
     if getattr(args, "graph", 0) and args.graph > 0:
@@ -388,6 +417,8 @@ def run_ours(args, rank, world, device):
                           else "inputs larger than L2, no flush"),
                    "parallelism": f"replicas x{world} (independent rows per GPU)"},
         "pct_of_peak": round(100 * value / world / peak, 2),
+        "pct_of_peak_basis": f"{peak_kind} copy bandwidth {peak} GB/s",
+        "pct_of_nominal": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "rows_per_s": round(w.rows * world / (step_ms / 1e3), 1),
         "kernels": kernels, "roofline": roof, "gpu_launches": int(n_launch), "graph": graph,
         "clocks": clk,
@@ -395,58 +426,147 @@ def run_ours(args, rank, world, device):
     return res, (w, inp, y, dx)
 
 
+def e2e_chunks(w, msb, msh, has_mask, n_target=8):
+    """Row blocks of the pipelined end-to-end leg: (first row, rows, mask
+    element offset).  A block starts where the kernels' row rule (q = r mod S,
+    h, b from r) still holds for its block-relative rows: at a batch boundary
+    when the mask varies by batch or head (the mask pointer then moves to that
+    batch), else at a multiple of S rows (a shared or absent mask)."""
+    per_batch = has_mask and (msb != 0 or msh != 0)
+    unit = w.H * w.cols if per_batch else w.cols
+    n_units = -(-w.rows // unit)
+    per = max(1, -(-n_units // n_target))
+    out = []
+    for u0 in range(0, n_units, per):
+        r0 = u0 * unit
+        n = min(w.rows, (u0 + per) * unit) - r0
+        moff = (r0 // (w.H * w.cols)) * msb if per_batch else 0
+        out.append((r0, n, moff))
+    return out
+
+
 def run_e2e(args, w, inp, device, steps):
-    """Same metric through the C ABI with host buffers: per step, H2D of x
-    (+mask) and dy from pinned memory, forward + backward, D2H of y and dx."""
+    """Same metric through the C ABI with host buffers.  Every step copies x,
+    dy (and the mask) in from pinned host memory, runs the forward and the
+    backward, and copies y and dx back out.  The rows are cut into blocks
+    (``e2e_chunks``) on three streams: the copy-in of block i+1, the kernels
+    of block i and the copy-out of block i-1 overlap, and the two copy
+    directions run at once."""
     import scaled_masked_softmax_gb300 as sms
 
     L = sms.binding.lib()
+    mask = inp["mask"]
     hx = inp["x"].cpu().pin_memory()
-    hm = inp["mask"].cpu().pin_memory() if inp["mask"] is not None else None
+    hm = mask.cpu().pin_memory() if mask is not None else None
     hdy = inp["dy"].cpu().pin_memory()
     hy = torch.empty_like(hx).pin_memory()
     hdx = torch.empty_like(hx).pin_memory()
     d_x = torch.empty_like(inp["x"])
-    d_m = torch.empty_like(inp["mask"]) if hm is not None else None
+    d_m = torch.empty_like(mask) if hm is not None else None
     d_dy = torch.empty_like(inp["dy"])
     d_y = torch.empty_like(inp["x"])
     d_dx = torch.empty_like(inp["x"])
-    stream = torch.cuda.current_stream(device)
-    st = stream.cuda_stream
+    hmf = hm.view(-1) if hm is not None else None
+    dmf = d_m.view(-1) if d_m is not None else None
     dt = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}[hx.dtype]
+    eb = hx.element_size()
+    msb, msh = inp["mask_stride_b"], inp["mask_stride_h"]
+    chunks = e2e_chunks(w, msb, msh, mask is not None)
+    shared_mask = hm is not None and msb == 0  # one mask for every batch: copied in once per step
+    s_in, s_k, s_out = (torch.cuda.Stream(device) for _ in range(3))
+    ev_in = [torch.cuda.Event() for _ in chunks]
+    ev_k = [torch.cuda.Event() for _ in chunks]
+    ev_out = [torch.cuda.Event() for _ in chunks]
+    ev_mask = torch.cuda.Event()
 
     def step():
-        d_x.copy_(hx, non_blocking=True)
-        if hm is not None:
-            d_m.copy_(hm, non_blocking=True)
-        d_dy.copy_(hdy, non_blocking=True)
-        rc = L.sms_forward(d_x.data_ptr(), None if d_m is None else d_m.data_ptr(), 0 if d_m is None else d_m.numel(),
-                           inp["mask_stride_b"], inp["mask_stride_h"], inp["heads"], d_y.data_ptr(), w.rows, w.cols,
-                           w.scale, int(w.is_causal), dt, st)
-        rc = rc or L.sms_backward(d_y.data_ptr(), d_dy.data_ptr(), d_dx.data_ptr(), w.rows, w.cols, w.scale,
-                                  int(w.is_causal), dt, st)
-        if rc:
-            raise RuntimeError(sms.sms_last_error())
-        hy.copy_(d_y, non_blocking=True)
-        hdx.copy_(d_dx, non_blocking=True)
+        if shared_mask:
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(ev_k[-1])  # the last block of the previous step has read it
+                d_m.copy_(hm, non_blocking=True)
+                ev_mask.record(s_in)
+        for c, (r0, n, moff) in enumerate(chunks):
+            r1 = r0 + n
+            mlen = 0
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(ev_k[c])  # the previous step's kernels are done with this block's inputs
+                d_x[r0:r1].copy_(hx[r0:r1], non_blocking=True)
+                d_dy[r0:r1].copy_(hdy[r0:r1], non_blocking=True)
+                if hm is not None and not shared_mask:
+                    nb = -(-n // (w.H * w.cols))
+                    mlen = min(nb * msb, hmf.numel() - moff)
+                    dmf[moff:moff + mlen].copy_(hmf[moff:moff + mlen], non_blocking=True)
+                ev_in[c].record(s_in)
+            s_k.wait_event(ev_in[c])
+            s_k.wait_event(ev_out[c])  # the previous step's copy-out of this block has read y and dx
+            if shared_mask:
+                s_k.wait_event(ev_mask)
+            st = s_k.cuda_stream
+            mptr = None if d_m is None else d_m.data_ptr() + moff * d_m.element_size()
+            mnum = 0 if d_m is None else (dmf.numel() - moff)
+            rc = L.sms_forward(d_x.data_ptr() + r0 * w.cols * eb, mptr, mnum, msb, msh, inp["heads"],
+                               d_y.data_ptr() + r0 * w.cols * eb, n, w.cols, w.scale, int(w.is_causal), dt, st)
+            rc = rc or L.sms_backward(d_y.data_ptr() + r0 * w.cols * eb, d_dy.data_ptr() + r0 * w.cols * eb,
+                                      d_dx.data_ptr() + r0 * w.cols * eb, n, w.cols, w.scale, int(w.is_causal),
+                                      dt, st)
+            if rc:
+                raise RuntimeError(sms.sms_last_error())
+            ev_k[c].record(s_k)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_k[c])
+                hy[r0:r1].copy_(d_y[r0:r1], non_blocking=True)
+                hdx[r0:r1].copy_(d_dx[r0:r1], non_blocking=True)
+                ev_out[c].record(s_out)
 
     for _ in range(2):
         step()
     torch.cuda.synchronize(device)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
+    a.record(s_in)
     for _ in range(steps):
         step()
-    b.record(stream)
+    for s in (s_in, s_k):
+        s_out.wait_stream(s)
+    b.record(s_out)
     torch.cuda.synchronize(device)
     ms = a.elapsed_time(b) / steps
-    h2d = hx.numel() * hx.element_size() + hdy.numel() * hdy.element_size() + \
-        (0 if hm is None else hm.numel() * hm.element_size())
+    # the same step with no overlap, for comparison: copies in, kernels, copies out
+    a2, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    st0 = torch.cuda.current_stream(device)
+
+    def serial_step():
+        d_x.copy_(hx, non_blocking=True)
+        if hm is not None:
+            d_m.copy_(hm, non_blocking=True)
+        d_dy.copy_(hdy, non_blocking=True)
+        rc = L.sms_forward(d_x.data_ptr(), None if d_m is None else d_m.data_ptr(), 0 if d_m is None else d_m.numel(),
+                           msb, msh, inp["heads"], d_y.data_ptr(), w.rows, w.cols, w.scale, int(w.is_causal), dt,
+                           st0.cuda_stream)
+        rc = rc or L.sms_backward(d_y.data_ptr(), d_dy.data_ptr(), d_dx.data_ptr(), w.rows, w.cols, w.scale,
+                                  int(w.is_causal), dt, st0.cuda_stream)
+        if rc:
+            raise RuntimeError(sms.sms_last_error())
+        hy.copy_(d_y, non_blocking=True)
+        hdx.copy_(d_dx, non_blocking=True)
+
+    serial_step()
+    torch.cuda.synchronize(device)
+    n2 = max(1, min(steps, 3))
+    a2.record(st0)
+    for _ in range(n2):
+        serial_step()
+    b2.record(st0)
+    torch.cuda.synchronize(device)
+    ms_serial = a2.elapsed_time(b2) / n2
+    h2d = hx.numel() * eb + hdy.numel() * hdy.element_size() + (0 if hm is None else hm.numel() * hm.element_size())
     d2h = hy.numel() * hy.element_size() + hdx.numel() * hdx.element_size()
     alg = fwd_bytes(w, inp) + bwd_bytes(w)
     return {"value": round(alg / (ms * 1e6), 1), "unit": "GB/s", "ms_per_step": round(ms, 3),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "path": "C ABI (sms_forward + sms_backward) on pinned host buffers copied in and out every step"}
+            "host_link_gbs": round((h2d + d2h) / (ms * 1e6), 1),
+            "blocks": len(chunks), "serial_ms_per_step": round(ms_serial, 3),
+            "path": "C ABI (sms_forward + sms_backward per row block) on pinned host buffers copied in and out "
+                    "every step; copy-in, kernels and copy-out of successive blocks overlap on three streams"}
 
 
 # ------------------------------------------------------- oracle on the CPU ---
@@ -556,7 +676,7 @@ def run_reference(args, rank, world):
 
     if rank != 0:
         return None
-    w = workloads.WORKLOADS[args.workload]
+    w = _workload(args)
     inp_cpu = cpu_inputs(w)
     oracle.build()
     cores = oracle.num_threads()
@@ -610,6 +730,8 @@ def main():
                     help="also time the step replayed from a CUDA graph of N steps (launch-bound shapes)")
     ap.add_argument("--lengths", action="store_true",
                     help="key-padding workloads through the key-length entry points instead of the [B,1,S,S] mask")
+    ap.add_argument("--bh", default=None, metavar="B,H",
+                    help="the workload's distributions at batch B and H heads (small profiling captures)")
     ap.add_argument("--bool-mask", action="store_true",
                     help="masked workloads with the mask as one byte per element (sms_forward_bool)")
     args = ap.parse_args()

@@ -227,11 +227,22 @@ SMS_API int sms_last_path(void);
  */
 SMS_API int64_t sms_launch_count(void);
 
+/* Values of the device error word (sms_device_error): which bounded wait of a
+ * kernel fed by bulk (TMA) copies gave up.  The first failure is kept. */
+typedef enum {
+    SMS_DEVERR_NONE = 0,
+    SMS_DEVERR_CTA_CONSUMER_WAIT = 1, /* SMS_PATH_CTA: a consumer group waited for a staged row  */
+    SMS_DEVERR_CTA_PRODUCER_WAIT = 2, /* SMS_PATH_CTA: the producer waited for a free stage      */
+    SMS_DEVERR_RING_WAIT = 3          /* SMS_PATH_RING: a lane group waited for its own copies   */
+} sms_device_error_code;
+
 /*
  * Reads (and clears) the device-side error word of the current device after
- * synchronising `stream`.  Nonzero means a kernel gave up on a bounded wait
- * for its own bulk copies (1 = consumer wait, 2 = producer wait); its output
- * is then incomplete.  Returns -1 if the read itself failed.
+ * synchronising `stream`.  Nonzero (an sms_device_error_code) means a kernel
+ * gave up on a bounded wait (2 s) for its own bulk copies; it then stopped
+ * taking rows, waited (bounded) for the copies it had in flight and left, so
+ * its output is incomplete but the context stays usable.  Returns -1 if the
+ * read itself failed.
  */
 SMS_API int sms_device_error(void *stream);
 

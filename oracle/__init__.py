@@ -188,10 +188,3 @@ def backward(y_rows, dy_rows, cols: int, scale: float, y_dtype_code=None, dy_dty
         raise ValueError("oracle_backward rejected its arguments")
     return dx.reshape(ya.shape)
 
-
-def mask_row_offset(r: int, cols: int, heads: int, mask_stride_b: int, mask_stride_h: int) -> int:
-    """Element offset of the mask row that row r reads (same rule as oracle.c)."""
-    q = r % cols
-    h = (r // cols) % heads
-    b = r // (cols * heads)
-    return b * mask_stride_b + h * mask_stride_h + q * cols

@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "sms.h"
 #include "sms_fastdiv.h"
 
 namespace sms {

@@ -272,14 +272,16 @@ __device__ __forceinline__ void fwd_scores_edge(const FwdArgs &a, const RowPos &
 }
 
 // exp of every score against the offset c = -m*log2e (in place); returns the
-// lane's partial sum.
-template <int NV, int VEC>
-__device__ __forceinline__ float exp_sum(float (&s)[NV][VEC], float c)
+// lane's partial sum.  LIVE: only the first `nslot` vector slots hold scores
+// (nslot is uniform over the lane group; the other slots are left untouched).
+template <int NV, int VEC, bool LIVE = false>
+__device__ __forceinline__ float exp_sum(float (&s)[NV][VEC], float c, int nslot = NV)
 {
     const float2 l2 = make_float2(kLog2e, kLog2e), c2 = make_float2(c, c);
     float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
+        if (LIVE && k >= nslot) break;
 #pragma unroll
         for (int e = 0; e < VEC; e += 2) {
             float2 t = __ffma2_rn(make_float2(s[k][e], s[k][e + 1]), l2, c2);
@@ -302,6 +304,49 @@ template <int G> __device__ __forceinline__ void group_barrier(int bar)
     else named_sync(bar, G);
 }
 
+// From the scores s (the lane's running max mx) to the exponentials (in s)
+// and the row's normalisation factor, merged over the group of G lanes.
+// LIVE: only the first nslot slots hold scores (see exp_sum).
+template <int G, int NV, int VEC, bool LIVE = false>
+__device__ __forceinline__ float fwd_norm(float (&s)[NV][VEC], float mx, int gl, int gi,
+                                          float (*red_m)[G > 32 ? G / 32 : 1], float (*red_l)[G > 32 ? G / 32 : 1],
+                                          int bar, int nslot = NV)
+{
+    constexpr int W = G > 32 ? G / 32 : 1;
+    if constexpr (G <= 32) {
+        mx = group_max<G>(mx);
+        const float c = (mx == neg_inf()) ? 0.f : -mx * kLog2e;  // fully masked row: every term 0
+        const float sum = group_sum<G>(exp_sum<NV, VEC, LIVE>(s, c, nslot));
+        return sum > 0.f ? __frcp_rn(sum) : 0.f;
+    } else {
+        // each lane exponentiates against its own max; warps merge (max, sum)
+        // pairs, the group's warps merge theirs through shared memory
+        const int wg = gl >> 5, lane = threadIdx.x & 31;
+        const float c = (mx == neg_inf()) ? 0.f : -mx * kLog2e;
+        const float lt = exp_sum<NV, VEC, LIVE>(s, c, nslot);
+        const float mw = group_max<32>(mx);
+        const float mwr = (mw == neg_inf()) ? 0.f : mw;
+        const float lw = group_sum<32>(mx == neg_inf() ? 0.f : lt * ex2((mx - mwr) * kLog2e));
+        if (lane == 0) {
+            red_m[gi][wg] = mw;
+            red_l[gi][wg] = lw;
+        }
+        group_barrier<G>(bar);
+        float mg = neg_inf();
+#pragma unroll
+        for (int w = 0; w < W; ++w) mg = fmaxf(mg, red_m[gi][w]);
+        const float Mr = (mg == neg_inf()) ? 0.f : mg;
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+            const float m2 = red_m[gi][w];
+            tot += (m2 == neg_inf()) ? 0.f : red_l[gi][w] * ex2((m2 - Mr) * kLog2e);
+        }
+        const float inv = tot > 0.f ? __frcp_rn(tot) : 0.f;
+        return (mx == neg_inf()) ? 0.f : ex2((mx - Mr) * kLog2e) * inv;
+    }
+}
+
 // Scores, exponentials and the row's normalisation factor: s holds the
 // exponentials on return.  red_m / red_l: this call's shared slots
 // [group][warp] (multi-warp groups only).
@@ -312,7 +357,6 @@ __device__ __forceinline__ float fwd_reduce(const FwdArgs &a, const RowPos &p, i
                                             int bar)
 {
     constexpr int VEC = Dt<T>::VEC;
-    constexpr int W = G > 32 ? G / 32 : 1;
     float mx = neg_inf();
     if (ALIGNED || p.fast) {
         if constexpr (!ALIGNED) {
@@ -325,38 +369,7 @@ __device__ __forceinline__ float fwd_reduce(const FwdArgs &a, const RowPos &p, i
         for (int k = 0; k < NV; ++k) fwd_scores_edge<T, G, NV, M>(a, p, gl, k, B, s[k], mx);
     }
 
-    if constexpr (G <= 32) {
-        mx = group_max<G>(mx);
-        const float c = (mx == neg_inf()) ? 0.f : -mx * kLog2e;  // fully masked row: every term 0
-        const float sum = group_sum<G>(exp_sum<NV, VEC>(s, c));
-        return sum > 0.f ? __frcp_rn(sum) : 0.f;
-    } else {
-        // each lane exponentiates against its own max; warps merge (max, sum)
-        // pairs, the group's warps merge theirs through shared memory
-        const int wg = gl >> 5, lane = threadIdx.x & 31;
-        const float c = (mx == neg_inf()) ? 0.f : -mx * kLog2e;
-        const float lt = exp_sum<NV, VEC>(s, c);
-        const float mw = group_max<32>(mx);
-        const float mwr = (mw == neg_inf()) ? 0.f : mw;
-        const float lw = group_sum<32>(mx == neg_inf() ? 0.f : lt * ex2((mx - mwr) * kLog2e));
-        if (lane == 0) {
-            red_m[gi][wg] = mw;
-            red_l[gi][wg] = lw;
-        }
-        group_barrier<G>(bar);
-        float M = neg_inf();
-#pragma unroll
-        for (int w = 0; w < W; ++w) M = fmaxf(M, red_m[gi][w]);
-        const float Mr = (M == neg_inf()) ? 0.f : M;
-        float tot = 0.f;
-#pragma unroll
-        for (int w = 0; w < W; ++w) {
-            const float m2 = red_m[gi][w];
-            tot += (m2 == neg_inf()) ? 0.f : red_l[gi][w] * ex2((m2 - Mr) * kLog2e);
-        }
-        const float inv = tot > 0.f ? __frcp_rn(tot) : 0.f;
-        return (mx == neg_inf()) ? 0.f : ex2((mx - Mr) * kLog2e) * inv;
-    }
+    return fwd_norm<G, NV, VEC>(s, mx, gl, gi, red_m, red_l, bar);
 }
 
 // y = e * fac for every element the lane holds.

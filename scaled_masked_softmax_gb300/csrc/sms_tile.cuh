@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(Geo<WG, R, SLOTS, CH>::THREADS, 1)
                     for (int c = 0; c < d.nchunks; ++c) {
                         if (!mbar_wait_bounded(&h.empty[g][stage[g]], ph[g] ^ 1u, abort_flag)) {
                             *abort_flag = 1;
-                            report_error(err, 2);
+                            report_error(err, SMS_DEVERR_CTA_PRODUCER_WAIT);
                             ok = false;
                             break;
                         }
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(Geo<WG, R, SLOTS, CH>::THREADS, 1)
                     if (!mbar_try_wait(&h.full[g][s], p)) {
                         const uint64_t t0 = global_ns();
                         while (!mbar_try_wait(&h.full[g][s], p))
-                            if (global_ns() - t0 > kWaitLimitNs) { report_error(err, 2); break; }
+                            if (global_ns() - t0 > kWaitLimitNs) { report_error(err, SMS_DEVERR_CTA_PRODUCER_WAIT); break; }
                     }
                 }
         return;
@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(Geo<WG, R, SLOTS, CH>::THREADS, 1)
                         if (lane == 0) {
                             *abort_flag = 1;
                             h.cons_abort[g] = 1;
-                            report_error(err, 1);
+                            report_error(err, SMS_DEVERR_CTA_CONSUMER_WAIT);
                         }
                     }
                     st = stages + (size_t)(g * K + stage) * G::STAGE;

@@ -224,10 +224,10 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_warp_kernel(const FwdArgs a)
         __syncthreads();
 #pragma unroll
         for (int i = 0; i < RPG; ++i) {
-            float M = neg_inf();
+            float mg = neg_inf();
 #pragma unroll
-            for (int w = 0; w < W; ++w) M = fmaxf(M, red_m[gi][i][w]);
-            const float Mr = (M == neg_inf()) ? 0.f : M;
+            for (int w = 0; w < W; ++w) mg = fmaxf(mg, red_m[gi][i][w]);
+            const float Mr = (mg == neg_inf()) ? 0.f : mg;
             float tot = 0.f;
 #pragma unroll
             for (int w = 0; w < W; ++w) {

@@ -63,3 +63,31 @@ def test_cpu_baseline_reports_all_cores_and_one_thread():
     assert r["kind"] == "oracle" and r["cores"] == before and r["value"] > 0 and r["rows_per_s"] > 0
     assert r["single_thread"]["value"] > 0 and r["single_thread"]["rows_per_s"] > 0
     assert isinstance(r["cpu"], str) and r["cpu"]
+
+
+@pytest.mark.parametrize("kind", ["none", "SS", "B1SS", "BHSS"])
+@pytest.mark.parametrize("B,Hh,S,rows", [(3, 2, 8, None), (4, 3, 5, None), (1, 1, 7, 40), (2, 5, 4, None)])
+@pytest.mark.parametrize("n_target", [1, 2, 3, 8, 100])
+def test_e2e_blocks_keep_the_row_rule(kind, B, Hh, S, rows, n_target):
+    """The pipelined end-to-end leg calls the kernels once per row block with
+    shifted x / y / mask pointers: every row must land in exactly one block,
+    and the block-relative row must reach the same query position and mask
+    row as the absolute one."""
+    if kind == "SS" and rows is None:
+        rows = B * Hh * S
+    w = workloads.Workload("t", B, Hh, S, "f32", 1.0, 1.0, kind, True, True, 1, rows_override=rows)
+    msb, msh, H = w.mask_strides()
+    blocks = bench.e2e_chunks(w, msb, msh, kind != "none", n_target)
+    seen = []
+    for r0, n, moff in blocks:
+        assert n > 0
+        for rr in range(n):
+            r = r0 + rr
+            seen.append(r)
+            q, h, b = r % S, (r // S) % H, r // (S * H)
+            q2, h2, b2 = rr % S, (rr // S) % H, rr // (S * H)
+            assert q2 == q
+            if kind != "none":
+                assert moff + b2 * msb + h2 * msh + q2 * S == b * msb + h * msh + q * S
+    assert seen == list(range(w.rows))
+    assert len(blocks) <= max(1, n_target) or len(blocks) == -(-w.rows // (S * (H if kind in ("B1SS", "BHSS") else 1)))
