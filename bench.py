@@ -52,9 +52,13 @@ def _peaks():
 
 
 def _kernel_hash() -> str:
+    """Hash of the softmax kernel sources and their dispatcher (the attention
+    kernels, sms_attn*, are not part of it)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "scaled_masked_softmax_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
+        if name.startswith(("sms_attn", "sms_tc")):
+            continue
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())

@@ -155,3 +155,95 @@ def raw_forward_bool(x, mask, sb, sh, heads, w, y=None):
     sms.sms_forward_bool(x.data_ptr(), mask.data_ptr(), mask.numel(), sb, sh, heads, y.data_ptr(), w.rows, w.cols,
                          w.scale, w.is_causal, dt, torch.cuda.current_stream().cuda_stream)
     return y
+
+
+# ------------------------------------------------------- whole-tensor parity ---
+# The full-size workloads are checked on every row: the fp64 oracle runs on the
+# host over chunks of rows (OpenMP over rows), its result is copied to the
+# device, and the comparison (the same bounds as check_forward /
+# check_backward) runs there in fp64.
+
+def _chunk_rows(w, elems=1 << 25):
+    step = max(1, elems // w.cols)
+    return [(r0, min(w.rows, r0 + step)) for r0 in range(0, w.rows, step)]
+
+
+class FullCheck:
+    """Accumulates the whole-tensor bounds over row chunks."""
+
+    def __init__(self, dtype, what):
+        self.dtype, self.what = dtype, what
+        self.fwd_worst = 0.0
+        self.bwd_err = 0.0   # max |dx - ref| (fp32: over the tensor)
+        self.bwd_ref = 0.0   # max |ref| (fp32 per-tensor relative bound)
+        self.rows = 0
+
+    def forward(self, y_dev: torch.Tensor, ref_np: np.ndarray, r0: int):
+        ref = torch.from_numpy(ref_np).to(y_dev.device)
+        y = y_dev.to(torch.float64)
+        assert bool(torch.isfinite(y).all()), f"{self.what}: non-finite output near row {r0}"
+        err = (y - ref).abs()
+        worst = float(err.max()) if err.numel() else 0.0
+        self.fwd_worst = max(self.fwd_worst, worst)
+        assert worst <= FWD_ATOL[self.dtype], \
+            f"{self.what}: max |y - y_ref| = {worst:.3e} > {FWD_ATOL[self.dtype]:.1e} in rows from {r0}"
+        bad = int(((ref == 0) & (y != 0)).sum())
+        assert bad == 0, f"{self.what}: {bad} positions should be exactly 0 in rows from {r0}"
+        if self.dtype == torch.float32:
+            live = ref.sum(-1) > 0.5
+            dev = (1.0 - y.sum(-1))[live].abs()
+            assert dev.numel() == 0 or float(dev.max()) <= 1e-5, \
+                f"{self.what}: |1 - sum y| = {float(dev.max()):.2e} in rows from {r0}"
+        self.rows += y_dev.shape[0]
+
+    def backward(self, dx_dev: torch.Tensor, y_dev: torch.Tensor, dy_dev: torch.Tensor, ref_np: np.ndarray,
+                 scale: float, r0: int):
+        ref = torch.from_numpy(ref_np).to(dx_dev.device)
+        dx = dx_dev.to(torch.float64)
+        assert bool(torch.isfinite(dx).all()), f"{self.what}: non-finite gradient near row {r0}"
+        err = (dx - ref).abs()
+        if self.dtype == torch.float32:
+            self.bwd_err = max(self.bwd_err, float(err.max()))
+            self.bwd_ref = max(self.bwd_ref, float(ref.abs().max()))
+            return
+        y = y_dev.to(torch.float64)
+        dy = dy_dev.to(torch.float64)
+        dot = (y * dy).sum(-1, keepdim=True)
+        bound = 2 * UNIT[self.dtype] * (ref.abs() + abs(scale) * y.abs() * (dy.abs() + dot.abs())) + 1e-7
+        excess = float((err - bound).max())
+        assert excess <= 0, f"{self.what}: backward error exceeds bound by {excess:.3e} in rows from {r0}"
+        self.bwd_err = max(self.bwd_err, float(err.max()))
+
+    def finish_backward(self):
+        if self.dtype == torch.float32:
+            rel = self.bwd_err / max(self.bwd_ref, 1e-30)
+            assert rel <= 1e-5, f"{self.what}: backward relative error {rel:.3e} > 1e-5"
+
+
+def check_all_rows(w, inp, y, dx=None, what="", key_lengths=None, bool_mask=None):
+    """Every row of y (and dx, the backward of y against inp['dy']) against the
+    oracle.  key_lengths: the per-batch lengths the forward used instead of
+    the mask; bool_mask: the byte mask it used instead of the additive one."""
+    chk = FullCheck(w.torch_dtype, what)
+    mask = None
+    if key_lengths is None:
+        mask = bool_mask if bool_mask is not None else inp["mask"]
+        mask = mask.cpu() if mask is not None else None
+    L = key_lengths.cpu() if key_lengths is not None else None
+    for r0, r1 in _chunk_rows(w):
+        xr = inp["x"][r0:r1].cpu()
+        ri = np.arange(r0, r1, dtype=np.int64)
+        if L is not None:
+            ref = oracle.forward(xr, w.cols, w.scale, w.is_causal, heads=w.H, key_lengths=L, row_index=ri)
+        else:
+            ref = oracle.forward(xr, w.cols, w.scale, w.is_causal, mask, inp["mask_stride_b"], inp["mask_stride_h"],
+                                 inp["heads"], row_index=ri)
+        chk.forward(y[r0:r1], ref, r0)
+        if dx is not None:
+            yr, dyr = y[r0:r1], inp["dy"][r0:r1]
+            dref = oracle.backward(yr.cpu(), dyr.cpu(), w.cols, w.scale)
+            chk.backward(dx[r0:r1], yr, dyr, dref, w.scale, r0)
+    if dx is not None:
+        chk.finish_backward()
+    assert chk.rows == w.rows
+    return chk

@@ -10,7 +10,6 @@ layouts cover [S,S], [B,1,S,S] and [B,H,S,S]; fully masked rows give zeros.
 """
 import math
 
-import numpy as np
 import pytest
 import torch
 
@@ -146,19 +145,12 @@ def test_bool_mask_autograd_and_in_place():
         assert torch.equal(xi, y.detach())
 
 
-def _sample_rows(rows, cols, n, seed):
-    rng = np.random.default_rng(seed)
-    idx = set(rng.integers(0, rows, size=n).tolist())
-    idx.update([0, 1, cols - 1, cols, rows - 1])
-    return np.array(sorted(i for i in idx if 0 <= i < rows), dtype=np.int64)
-
-
 @pytest.mark.parametrize("name", ["keypad_causal_bf16_s4096", "sweep_f16_s4099", "sweep_f32_s1024",
                                   "sweep_f32_s4099", "sweep_f32_s16384"])
 def test_full_size_bool_mask(name):
     """Full-size workloads whose masks are 0 / -inf, with the mask given as
-    bytes: sampled rows against the oracle, and bit-equal on those rows to the
-    additive-mask run when both take the same kernel family."""
+    bytes: every row against the oracle's boolean-mask path, and bit-equal to
+    the additive-mask run when both take the same kernel family."""
     w = workloads.WORKLOADS[name]
     inp = workloads.make_inputs(w, device="cuda")
     mb = torch.isinf(inp["mask"])
@@ -166,20 +158,14 @@ def test_full_size_bool_mask(name):
     path_bool = sms.sms_last_path()
     torch.cuda.synchronize()
     assert sms.sms_device_error(torch.cuda.current_stream().cuda_stream) == 0
-    idx = _sample_rows(w.rows, w.cols, 64, w.seed + 11)
-    ti = torch.as_tensor(idx, device=y.device)
-    y_ref = oracle.forward(inp["x"][ti].cpu(), w.cols, w.scale, w.is_causal, mb.cpu(), inp["mask_stride_b"],
-                           inp["mask_stride_h"], inp["heads"], row_index=idx)
-    H.check_forward(H.to_np64(y[ti]), y_ref, w.torch_dtype, name + " bool")
-    ys = y[ti].clone()
-    del y
+    H.check_all_rows(w, inp, y, None, name + " bool", bool_mask=mb)
     y_add = H.raw_forward(inp, w)
     path_add = sms.sms_last_path()
     torch.cuda.synchronize()
     if path_bool == path_add:
-        assert torch.equal(ys, y_add[ti])
+        assert torch.equal(y, y_add)
     else:  # fp32 rows the CTA family takes with an additive mask: the two-pass kernel sums in another order
         assert path_add == sms.SMS_PATH_CTA and path_bool == sms.SMS_PATH_ONLINE
-        H.check_forward(H.to_np64(y_add[ti]), y_ref, w.torch_dtype, name + " additive")
-    del inp, y_add, mb
+        H.check_all_rows(w, inp, y_add, None, name + " additive")
+    del inp, y, y_add, mb
     torch.cuda.empty_cache()
