@@ -193,6 +193,42 @@ SMS_API int sms_backward_lengths(const void *y, const void *dy, void *dx, const 
                                  int64_t rows, int64_t cols, float scale, int is_causal_hint, int dtype,
                                  void *stream);
 
+/*
+ * Fused attention forward on the tensor cores: the step the second article
+ * (pnsm.cn/news/1983787) names as next in §4.4 and the page
+ * "从GEMM到Transformer：手写CUDA算子优化的完整路线与性能调优实践" computes in §2.2
+ * (scores, softmax and the product with V in one kernel, with the streaming
+ * max / sum of that section, so the [S, S] score tensor is never stored):
+ *       O[b,h] = softmax_j(Q[b,h] K[b,h]^T * scale + mask_row, causal) V[b,h]
+ * with the softmax of sms_forward (the mask is not scaled; j > i is masked
+ * under is_causal; a row with every key masked gives O = 0).
+ *   q, k, v, o     dense [batch, heads, seq, head_dim] device buffers of `dtype`
+ *                  (SMS_F16 or SMS_BF16), 16-byte aligned; o must not overlap
+ *                  an input
+ *   mask           NULL, or a mask in the layout of sms_forward: query row i of
+ *                  head (b, h) reads the seq elements from
+ *                  b*mask_stride_b + h*mask_stride_h + i*seq; additive of
+ *                  `dtype` (mask_is_bool = 0) or one byte per element with
+ *                  nonzero = masked (mask_is_bool = 1); mask_numel elements
+ *   lse            NULL, or [batch, heads, seq] fp32: per query row the natural
+ *                  log of the softmax denominator, log sum_j exp(s_j) (-inf for
+ *                  a row with every key masked), which the backward reads
+ *   head_dim       64 or 128
+ *   scale          multiplier of Q K^T (finite), typically 1/sqrt(head_dim)
+ * Arithmetic: Q K^T and P V on tcgen05.mma with fp32 accumulation in tensor
+ * memory; the softmax in fp32; P is rounded to `dtype` before P V; O is
+ * rounded once to `dtype`.  batch * heads * seq == 0 is a valid no-op.
+ * Errors: SMS_ERR_UNSUPPORTED for SMS_F32 or another head_dim;
+ * SMS_ERR_INVALID_ARG for NULL or unaligned pointers, negative sizes or
+ * strides, a mask extent beyond mask_numel, overlapping outputs, a
+ * non-finite scale; SMS_ERR_CUDA when the launch fails.  A bounded wait that
+ * gives up inside the kernel sets SMS_DEVERR_ATTN_WAIT (sms_device_error).
+ */
+SMS_API int sms_attention_forward(const void *q, const void *k, const void *v, const void *mask, int64_t mask_numel,
+                                  int64_t mask_stride_b, int64_t mask_stride_h, int mask_is_bool, void *o,
+                                  float *lse, int64_t batch, int64_t heads, int64_t seq, int64_t head_dim,
+                                  float scale, int is_causal, int dtype, void *stream);
+
 /* Static description of a status code. */
 SMS_API const char *sms_status_string(int status);
 
@@ -233,7 +269,8 @@ typedef enum {
     SMS_DEVERR_NONE = 0,
     SMS_DEVERR_CTA_CONSUMER_WAIT = 1, /* SMS_PATH_CTA: a consumer group waited for a staged row  */
     SMS_DEVERR_CTA_PRODUCER_WAIT = 2, /* SMS_PATH_CTA: the producer waited for a free stage      */
-    SMS_DEVERR_RING_WAIT = 3          /* SMS_PATH_RING: a lane group waited for its own copies   */
+    SMS_DEVERR_RING_WAIT = 3,         /* SMS_PATH_RING: a lane group waited for its own copies   */
+    SMS_DEVERR_ATTN_WAIT = 4          /* fused attention: a role waited for a copy, an MMA or a peer */
 } sms_device_error_code;
 
 /*

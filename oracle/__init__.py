@@ -60,6 +60,8 @@ def _load():
             lib.oracle_backward.restype = i32
             lib.oracle_decode.argtypes = [vp, i64, i32]
             lib.oracle_decode.restype = dbl
+            lib.oracle_decode_array.argtypes = [vp, i64, i32, vp]
+            lib.oracle_decode_array.restype = i32
             lib.oracle_num_threads.restype = i32
             lib.oracle_set_num_threads.argtypes = [i32]
             _lib = lib
@@ -103,13 +105,18 @@ def set_num_threads(n: int) -> None:
 def decode(a, dtype_code=None) -> np.ndarray:
     """Widen every element to fp64 with the oracle's own decoders."""
     arr, code = _raw(a, dtype_code)
-    lib = _load()
-    flat = arr.reshape(-1)
+    flat = np.ascontiguousarray(arr.reshape(-1))
     out = np.empty(flat.size, dtype=np.float64)
-    p = flat.ctypes.data
-    for i in range(flat.size):
-        out[i] = lib.oracle_decode(p, i, code)
+    if _load().oracle_decode_array(flat.ctypes.data, flat.size, code, out.ctypes.data) != 0:
+        raise ValueError("oracle_decode_array rejected its arguments")
     return out.reshape(arr.shape)
+
+
+def decode_one(a, i: int, dtype_code=None) -> float:
+    """Element i of the flattened array widened to fp64 (one decoder call)."""
+    arr, code = _raw(a, dtype_code)
+    flat = np.ascontiguousarray(arr.reshape(-1))
+    return float(_load().oracle_decode(flat.ctypes.data, int(i), code))
 
 
 def forward(x_rows, cols: int, scale: float, is_causal: bool = False, mask=None,

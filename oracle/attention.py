@@ -41,14 +41,15 @@ def _bhsd(a, name):
 
 
 def attention_forward(q, k, v, scale: float, is_causal: bool = False, mask=None, mask_stride_b: int = 0,
-                      mask_stride_h: int = 0, return_probs: bool = False):
+                      mask_stride_h: int = 0, return_probs: bool = False, return_lse: bool = False):
     """O = softmax(Q K^T * scale + mask, causal) V for q [B,H,S,D], k [B,H,S,D], v [B,H,S,Dv].
 
     ``mask`` and its strides follow oracle.forward (additive of q's storage
     dtype, or boolean / uint8 with nonzero = masked; row r of the [B*H*S, S]
     score view reads mask[b*stride_b + h*stride_h + i*S ...]).  ``scale`` is
     used as given (pass the float32 value a kernel sees).  Returns O (fp64),
-    and P as well when ``return_probs``.
+    then P when ``return_probs``, then the per-row log of the softmax
+    denominator when ``return_lse`` (see ``log_sum_exp``).
     """
     Q, K, V = _bhsd(_f64(q), "q"), _bhsd(_f64(k), "k"), _bhsd(_f64(v), "v")
     B, H, S, D = Q.shape
@@ -58,7 +59,60 @@ def attention_forward(q, k, v, scale: float, is_causal: bool = False, mask=None,
     P = _softmax_forward(scores.reshape(-1, S), S, scale, is_causal, mask, mask_stride_b, mask_stride_h, H)
     P = P.reshape(B, H, S, S)
     O = np.matmul(P, V)
-    return (O, P) if return_probs else O
+    out = [O]
+    if return_probs:
+        out.append(P)
+    if return_lse:
+        out.append(log_sum_exp(scores, scale, is_causal, mask, mask_stride_b, mask_stride_h))
+    return tuple(out) if len(out) > 1 else O
+
+
+def log_sum_exp(scores, scale: float, is_causal: bool = False, mask=None, mask_stride_b: int = 0,
+                mask_stride_h: int = 0):
+    """Per query row, log sum_j exp(s_j) of the scores s = scores*scale + mask
+    (j > i masked under causal), the log of the softmax denominator: with
+    M = max_j s_j it is M + log sum_j exp(s_j - M), and -inf for a row whose
+    every score is -inf.  ``scores`` is the fp64 [B, H, S, S] product Q K^T;
+    the mask follows oracle.forward (additive, or boolean / uint8 with
+    nonzero = masked)."""
+    B, H, S, _ = scores.shape
+    s = np.asarray(scores, dtype=np.float64) * float(scale)
+    if mask is not None:
+        m = np.asarray(decode(mask) if not _is_bool(mask) else _bool_np(mask), dtype=np.float64).reshape(-1)
+        for b in range(B):
+            for h in range(H):
+                base = b * mask_stride_b + h * mask_stride_h
+                s[b, h] += m[base:base + S * S].reshape(S, S)
+    if is_causal:
+        s = np.where(np.triu(np.ones((S, S), dtype=bool), 1), -np.inf, s)
+    M = s.max(axis=-1)
+    live = M > -np.inf
+    Mr = np.where(live, M, 0.0)
+    tot = np.exp(s - Mr[..., None]).sum(axis=-1)
+    return np.where(live, Mr + np.log(np.where(live, tot, 1.0)), -np.inf)
+
+
+def _is_bool(mask) -> bool:
+    try:
+        import torch
+
+        if isinstance(mask, torch.Tensor):
+            return mask.dtype in (torch.bool, torch.uint8)
+    except ImportError:  # pragma: no cover
+        pass
+    return np.asarray(mask).dtype in (np.bool_, np.uint8)
+
+
+def _bool_np(mask) -> np.ndarray:
+    """A boolean / byte mask as additive fp64 values: -inf where nonzero, else 0."""
+    try:
+        import torch
+
+        if isinstance(mask, torch.Tensor):
+            mask = mask.detach().to("cpu").numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.where(np.asarray(mask).astype(np.uint8) != 0, -np.inf, 0.0)
 
 
 def attention_backward(q, k, v, d_o, scale: float, is_causal: bool = False, mask=None, mask_stride_b: int = 0,

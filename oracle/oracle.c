@@ -119,6 +119,14 @@ static int dtype_ok(int dtype) { return dtype >= ORC_F32 && dtype <= ORC_F64; }
 /* Exposed so that the tests can pin the decoders over every bit pattern. */
 double oracle_decode(const void *p, int64_t i, int dtype) { return load_elem(p, i, dtype); }
 
+/* Every element of an array widened to binary64 with the decoders above. */
+int oracle_decode_array(const void *p, int64_t n, int dtype, double *out)
+{
+    if (!dtype_ok(dtype) || n < 0 || (n > 0 && (!p || !out))) return 1;
+    for (int64_t i = 0; i < n; ++i) out[i] = load_elem(p, i, dtype);
+    return 0;
+}
+
 int oracle_num_threads(void)
 {
 #ifdef _OPENMP

@@ -27,6 +27,8 @@ SIGNATURES = {
     "sms_backward": (_i32, [_vp, _vp, _vp, _i64, _i64, _f32, _i32, _i32, _vp]),
     "sms_forward_lengths": (_i32, [_vp, _vp, _i64, _vp, _i64, _i64, _f32, _i32, _i32, _vp]),
     "sms_backward_lengths": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _f32, _i32, _i32, _vp]),
+    "sms_attention_forward": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _i64, _i64, _i64, _i64,
+                                     _f32, _i32, _i32, _vp]),
     "sms_status_string": (_cp, [_i32]),
     "sms_last_error": (_cp, []),
     "sms_set_forced_path": (_i32, [_i32]),
@@ -99,6 +101,14 @@ def sms_forward_lengths(x, lengths, heads, y, rows, cols, scale, is_causal, dtyp
 def sms_backward_lengths(y, dy, dx, lengths, heads, rows, cols, scale, is_causal_hint, dtype, stream) -> None:
     _check(lib().sms_backward_lengths(y, dy, dx, lengths, heads, rows, cols, scale, int(bool(is_causal_hint)), dtype,
                                       stream))
+
+
+def sms_attention_forward(q, k, v, mask, mask_numel, mask_stride_b, mask_stride_h, mask_is_bool, o, lse, batch, heads,
+                          seq, head_dim, scale, is_causal, dtype, stream) -> None:
+    """Fused attention forward on the tensor cores: see include/sms.h."""
+    _check(lib().sms_attention_forward(q, k, v, mask, mask_numel, mask_stride_b, mask_stride_h, int(bool(mask_is_bool)),
+                                       o, lse, batch, heads, seq, head_dim, scale, int(bool(is_causal)), dtype,
+                                       stream))
 
 
 def sms_set_forced_path(path: int) -> int:

@@ -122,6 +122,22 @@ int pick_path(int forced, int64_t cols, int dtype, bool aligned, bool bwd, bool 
 
 }  // namespace
 
+int set_last_error(int status, const char *msg)
+{
+    snprintf(t_err, sizeof(t_err), "%s", msg);
+    return status;
+}
+
+void clear_last_error() { t_err[0] = '\0'; }
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+cudaError_t device_error_word(int **err)
+{
+    int dev = 0, n = 0;
+    return device_info(dev, n, *err);
+}
+
 int sm_count()
 {
     int dev = 0, n = 0;

@@ -1,0 +1,43 @@
+// Host-side interface of the fused attention kernels (sms_attn_fwd.cu,
+// sms_attn_bwd.cu) used by the C ABI (sms_attn_abi.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sms {
+
+// Problem description shared by the forward and the backward.  Q, K, V, O
+// (and dO, dQ, dK, dV) are dense [B, H, S, D] tensors of one 16-bit dtype;
+// the mask follows the softmax's rule: query row i of head (b, h) reads the
+// S mask elements from b*msb + h*msh + i*S.
+struct AttnArgs {
+    const void *q, *k, *v;
+    const void *mask;      // nullptr: none
+    int64_t mask_total;    // elements in the mask buffer
+    int64_t msb, msh;
+    int mask_bool;         // 1: one byte per element, nonzero = masked; 0: additive, dtype of q
+    int B, H, S, D;
+    float scale;           // multiplier of Q K^T
+    int causal;
+    int dtype;             // kF16 or kBF16
+    int *err;              // device error word
+    // forward
+    void *o;               // [B, H, S, D]
+    float *lse;            // [B, H, S]: log of each row's softmax denominator (natural log, -inf for a
+                           // fully masked row), or nullptr
+    // backward
+    const void *o_in, *dout;
+    const float *lse_in;
+    void *dq, *dk, *dv;
+    float *dq_acc;         // [B, H, S, D] fp32 scratch (zeroed by the backward before use)
+    float *delta;          // [B, H, S] fp32 scratch: rowsum(dO * O)
+};
+
+// Head dimensions the tensor-core kernels take.
+inline bool attn_head_dim_ok(int d) { return d == 64 || d == 128; }
+
+cudaError_t launch_attn_fwd(const AttnArgs &a, cudaStream_t st);
+cudaError_t launch_attn_bwd(const AttnArgs &a, cudaStream_t st);
+
+}  // namespace sms

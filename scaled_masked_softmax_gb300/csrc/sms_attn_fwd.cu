@@ -1,0 +1,515 @@
+// Fused attention forward on the 5th-generation tensor cores:
+//     O = softmax(Q K^T * scale + mask, causal) V,   lse = log sum exp per row
+// without materialising the [S, S] score tensor (the fusion the second
+// article, pnsm.cn/news/1983787, names in §4.4, with the streaming softmax
+// of "从GEMM到Transformer：手写CUDA算子优化的完整路线与性能调优实践" §2.2).
+//
+// One CTA owns 128 query rows of one (batch, head) and walks the key blocks
+// of 128 keys:
+//   * warp 0, one lane: TMA loads (cp.async.bulk.tensor, 128-byte swizzle)
+//     of the Q tile once and of the K and V tiles into a ring of stages;
+//   * warp 1, one lane: the MMAs, S_j = Q K_j^T into one of two TMEM score
+//     buffers, then O += P_j V_j into the TMEM output accumulator; warp 1
+//     also owns the TMEM allocation;
+//   * warps 2..5 (128 threads, one query row each, row = the warp's TMEM
+//     lane quarter): read S_j from TMEM, apply scale, mask and the causal
+//     rule, keep the running max m and sum l of the online softmax
+//     (m' = max(m, max_j s), l' = l * 2^(m - m') + sum 2^(s - m')), write
+//     P_j = 2^(s - m) as 16-bit values into shared memory in the MMA's
+//     swizzled layout, and rescale O in TMEM when m grows (only when it grows
+//     by more than 2^8, so most blocks skip it: the exponentials stay below
+//     2^8 in between); at the end O / l is stored and lse = (m + log2 l) ln 2.
+// S is double-buffered in TMEM, so the MMA of block j+1 overlaps the softmax
+// of block j, and the P V MMA of block j overlaps the softmax of block j+1.
+//
+// Every mbarrier wait is bounded (2 s).  A role whose wait gives up records
+// an error in the device word and stops; before the CTA leaves, the TMA lane
+// waits (bounded) for every load it issued, the MMA lane for every MMA it
+// issued, and warp 1 frees the TMEM.
+#include <cuda.h>
+
+#include <atomic>
+
+#include "sms_attn.h"
+#include "sms_common.cuh"
+#include "sms_internal.h"
+#include "sms_tc.cuh"
+
+namespace sms {
+namespace {
+
+constexpr int kBM = 128;          // query rows per CTA (the MMA's M)
+constexpr int kBN = 128;          // keys per block
+constexpr int kThreads = 192;     // warps 0 (TMA), 1 (MMA), 2..5 (softmax)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAtom = 16384;  // 128 rows x 128 bytes
+
+template <int D> struct FwdCfg {
+    static constexpr int NST = D == 128 ? 2 : 3;  // K/V stages
+    static constexpr int NP = D == 128 ? 1 : 2;   // P buffers
+    static constexpr uint32_t TILE = (D / 64) * kAtom;  // one 128 x D tile (Q, K or V)
+    static constexpr uint32_t PBUF = (kBN / 64) * kAtom;
+    static constexpr uint32_t OFF_Q = 0;
+    static constexpr uint32_t OFF_K = OFF_Q + TILE;
+    static constexpr uint32_t OFF_V = OFF_K + NST * TILE;
+    static constexpr uint32_t OFF_P = OFF_V + NST * TILE;
+    static constexpr uint32_t OFF_BAR = OFF_P + NP * PBUF;
+    static constexpr uint32_t BAR_BYTES = 512;
+    static constexpr uint32_t SMEM = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
+    static constexpr uint32_t COL_O = 2 * kBN;  // TMEM columns: S0, S1, O
+};
+
+struct FwdBars {
+    uint64_t q_full;
+    uint64_t k_full[3], v_full[3], kv_empty[3];
+    uint64_t s_full[2], s_free[2];
+    uint64_t p_full[2], pv_done[2];
+    uint64_t mma_drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+template <typename T> struct AbFmt;
+template <> struct AbFmt<__half> { static constexpr int v = 0; };
+template <> struct AbFmt<__nv_bfloat16> { static constexpr int v = 1; };
+
+// Bounded wait on phase `parity`; on failure the CTA is flagged and the
+// device word gets the code.
+__device__ __forceinline__ bool wait_or_flag(uint64_t *bar, uint32_t parity, FwdBars &b, int *err)
+{
+    if (mbar_wait_bounded(bar, parity, &b.abort)) return true;
+    *reinterpret_cast<volatile int *>(&b.abort) = 1;
+    report_error(err, SMS_DEVERR_ATTN_WAIT);
+    return false;
+}
+
+// Wait (bounded, whatever the abort flag says) for the copies or MMAs this
+// thread itself issued, before the CTA may leave.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > kWaitLimitNs) return;
+}
+
+// Warp-uniform bounded wait: every lane waits, the warp goes on only if all did.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, FwdBars &b, int *err)
+{
+    const bool w = wait_or_flag(bar, parity, b, err);
+    return __all_sync(0xffffffffu, w);
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, __half *)
+{
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, __nv_bfloat16 *)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// The 32 mask values of columns c0 .. c0+31 of one query row, as additive
+// log2-scaled terms (0 where no mask), in m2[].  MK: 0 none, 1 additive (T),
+// 2 boolean bytes.  Columns at or beyond S read nothing.
+template <typename T, int MK>
+__device__ __forceinline__ void mask_chunk(const AttnArgs &a, int64_t mrow, int c0, bool row_ok, float (&m2)[32])
+{
+#pragma unroll
+    for (int e = 0; e < 32; ++e) m2[e] = 0.f;
+    if constexpr (MK == 0) {
+        return;
+    } else {
+        if (!row_ok) return;
+        const int64_t base = mrow + c0;
+        const int S = a.S;
+        if constexpr (MK == 1) {
+            const T *mp = reinterpret_cast<const T *>(a.mask) + base;
+            const bool vec = (c0 + 32 <= S) && ((reinterpret_cast<uintptr_t>(mp) & 15u) == 0);
+            if (vec) {
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    float f[8];
+                    unpack<T>(ld_keep(mp + 8 * v), f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) m2[8 * v + e] = f[e] * kLog2e;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    if (c0 + e < S) m2[e] = to_f32<T>(mp[e]) * kLog2e;
+            }
+        } else {
+            const uint8_t *mp = reinterpret_cast<const uint8_t *>(a.mask) + base;
+            const bool vec = (c0 + 32 <= S) && ((reinterpret_cast<uintptr_t>(mp) & 15u) == 0);
+            if (vec) {
+#pragma unroll
+                for (int v = 0; v < 2; ++v) {
+                    const uint4 w = ld_keep(mp + 16 * v);
+                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) m2[16 * v + e] = ((ws[e >> 2] >> (8 * (e & 3))) & 0xffu) ? neg_inf() : 0.f;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    if (c0 + e < S) m2[e] = mp[e] ? neg_inf() : 0.f;
+            }
+        }
+    }
+}
+
+template <typename T, int D, int MK>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                const __grid_constant__ CUtensorMap tmv, const AttnArgs a)
+{
+    using C = FwdCfg<D>;
+    constexpr int NST = C::NST, NP = C::NP;
+    constexpr uint32_t IDESC_QK = tc::idesc_f16(AbFmt<T>::v, 0, kBM, kBN);
+    constexpr uint32_t IDESC_PV = tc::idesc_f16(AbFmt<T>::v, 1, kBM, D);
+
+    extern __shared__ unsigned char smem_raw[];
+    // 1024-byte alignment of the shared-memory address (the swizzle atoms)
+    const uint32_t raw = static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw));
+    unsigned char *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    FwdBars &b = *reinterpret_cast<FwdBars *>(smem + C::OFF_BAR);
+    const uint32_t s_base = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nq = (a.S + kBM - 1) / kBM;
+    const int BH = a.B * a.H;
+    const int qb = nq - 1 - (int)(blockIdx.x / (unsigned)BH);  // heaviest causal tiles first, every head
+    const int bh = (int)(blockIdx.x % (unsigned)BH);
+    const int q0 = qb * kBM;
+    const int nkv_all = (a.S + kBN - 1) / kBN;
+    const int nkv = a.causal ? min(nkv_all, (q0 + kBM - 1) / kBN + 1) : nkv_all;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&b.q_full, 1);
+        for (int s = 0; s < 3; ++s) {
+            mbar_init(&b.k_full[s], 1);
+            mbar_init(&b.v_full[s], 1);
+            mbar_init(&b.kv_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&b.s_full[s], 1);
+            mbar_init(&b.s_free[s], kBM);
+            mbar_init(&b.p_full[s], kBM);
+            mbar_init(&b.pv_done[s], 1);
+        }
+        mbar_init(&b.mma_drain, 1);
+        b.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tc::tmem_alloc(&b.tmem_base, kTmemCols);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = b.tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA loads ---
+        if (lane == 0) {
+            tc::prefetch_tmap(&tmq);
+            tc::prefetch_tmap(&tmk);
+            tc::prefetch_tmap(&tmv);
+            mbar_arrive_expect_tx(&b.q_full, C::TILE);
+#pragma unroll
+            for (int at = 0; at < D / 64; ++at) tc::tma_load_3d(smem + C::OFF_Q + at * kAtom, &tmq, at * 64, q0, bh, &b.q_full);
+            int armed = 0;  // blocks whose loads were issued
+            for (int j = 0; j < nkv; ++j) {
+                const int st = j % NST;
+                if (j >= NST && !wait_or_flag(&b.kv_empty[st], (uint32_t)((j / NST - 1) & 1), b, a.err)) break;
+                if (*reinterpret_cast<volatile int *>(&b.abort)) break;
+                mbar_arrive_expect_tx(&b.k_full[st], C::TILE);
+#pragma unroll
+                for (int at = 0; at < D / 64; ++at)
+                    tc::tma_load_3d(smem + C::OFF_K + st * C::TILE + at * kAtom, &tmk, at * 64, j * kBN, bh, &b.k_full[st]);
+                mbar_arrive_expect_tx(&b.v_full[st], C::TILE);
+#pragma unroll
+                for (int at = 0; at < D / 64; ++at)
+                    tc::tma_load_3d(smem + C::OFF_V + st * C::TILE + at * kAtom, &tmv, at * 64, j * kBN, bh, &b.v_full[st]);
+                armed = j + 1;
+            }
+            // leave no load in flight: each stage's last armed phase completes
+            // (bounded), whether or not the MMA lane consumed it
+            drain_wait(&b.q_full, 0);
+            for (int j = (armed > NST ? armed - NST : 0); j < armed; ++j) {
+                const uint32_t par = (uint32_t)((j / NST) & 1);
+                drain_wait(&b.k_full[j % NST], par);
+                drain_wait(&b.v_full[j % NST], par);
+            }
+        }
+    } else if (warp == 1) {
+        // ----------------------------------------------------------- MMAs ---
+        if (lane == 0) {
+            bool ok = wait_or_flag(&b.q_full, 0, b, a.err);
+            const uint32_t q_addr = s_base + C::OFF_Q;
+            auto pv = [&](int m) -> bool {
+                const int pb = m % NP, st = m % NST;
+                if (!wait_or_flag(&b.p_full[pb], (uint32_t)((m / NP) & 1), b, a.err)) return false;
+                if (!wait_or_flag(&b.v_full[st], (uint32_t)((m / NST) & 1), b, a.err)) return false;
+                tc::fence_after_sync();
+                const uint32_t p_addr = s_base + C::OFF_P + pb * C::PBUF;
+                const uint32_t v_addr = s_base + C::OFF_V + st * C::TILE;
+#pragma unroll
+                for (int k = 0; k < kBN / 16; ++k) {
+                    const uint64_t da = tc::desc_sw128(p_addr + (k / 4) * kAtom + (k % 4) * 32, 16, 1024);
+                    const uint64_t db = tc::desc_sw128(v_addr + k * 2048, kAtom, 1024);
+                    tc::mma_f16(tmem + C::COL_O, da, db, IDESC_PV, (m > 0 || k > 0) ? 1u : 0u);
+                }
+                tc::commit(&b.pv_done[pb]);
+                tc::commit(&b.kv_empty[st]);
+                return true;
+            };
+            for (int j = 0; ok && j < nkv; ++j) {
+                const int st = j % NST, sb = j & 1;
+                if (!wait_or_flag(&b.k_full[st], (uint32_t)((j / NST) & 1), b, a.err)) { ok = false; break; }
+                if (j >= 2 && !wait_or_flag(&b.s_free[sb], (uint32_t)(((j - 2) / 2) & 1), b, a.err)) { ok = false; break; }
+                tc::fence_after_sync();
+                const uint32_t k_addr = s_base + C::OFF_K + st * C::TILE;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint64_t da = tc::desc_sw128(q_addr + (k / 4) * kAtom + (k % 4) * 32, 16, 1024);
+                    const uint64_t db = tc::desc_sw128(k_addr + (k / 4) * kAtom + (k % 4) * 32, 16, 1024);
+                    tc::mma_f16(tmem + sb * kBN, da, db, IDESC_QK, k > 0 ? 1u : 0u);
+                }
+                tc::commit(&b.s_full[sb]);
+                if (j >= 1 && !pv(j - 1)) { ok = false; break; }
+            }
+            if (ok) pv(nkv - 1);
+            // leave no MMA in flight
+            tc::commit(&b.mma_drain);
+            drain_wait(&b.mma_drain, 0);
+        }
+    } else {
+        // -------------------------------------------------------- softmax ---
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;  // query row within the tile = TMEM lane
+        const int i = q0 + r;
+        const bool row_ok = i < a.S;
+        const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+        const float sl2 = a.scale * kLog2e;
+        const int bidx = bh / a.H, hidx = bh - bidx * a.H;
+        const int64_t mrow = (int64_t)bidx * a.msb + (int64_t)hidx * a.msh + (int64_t)i * a.S;
+        float m_run = neg_inf(), l = 0.f;
+        bool ok = true;
+        unsigned char *pbase = smem + C::OFF_P;
+        for (int j = 0; j < nkv; ++j) {
+            const int sb = j & 1, pb = j % NP;
+            const int j0 = j * kBN;
+            // per-element rules only where a block crosses the diagonal or the end of the keys
+            const bool pred = (j0 + kBN > a.S) || (a.causal && j0 + kBN - 1 > q0);
+            if (!warp_wait(&b.s_full[sb], (uint32_t)((j / 2) & 1), b, a.err)) { ok = false; break; }
+            tc::fence_after_sync();
+            // pass 1: the block's row max (log2 units)
+            float mx = neg_inf();
+#pragma unroll
+            for (int c = 0; c < kBN / 32; ++c) {
+                uint32_t v[32];
+                float m2[32];
+                mask_chunk<T, MK>(a, mrow, j0 + c * 32, row_ok, m2);
+                tc::tmem_ld32(tl + sb * kBN + c * 32, v);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    float s = fmaf(__uint_as_float(v[e]), sl2, m2[e]);
+                    if (pred) {
+                        const int col = j0 + c * 32 + e;
+                        if (col >= a.S || (a.causal && col > i)) s = neg_inf();
+                    }
+                    mx = fmaxf(mx, s);
+                }
+            }
+            const float m_new = fmaxf(m_run, mx);
+            const bool resc = m_new > m_run + 8.f;  // false while both are -inf
+            const float m_use = resc ? m_new : m_run;
+            const float alpha = resc ? ex2(m_run - m_new) : 1.f;  // 0 when m_run is -inf
+            l *= alpha;
+            // the P buffer of this block is free once the P V MMA of block j - NP is done
+            if (j >= NP && !warp_wait(&b.pv_done[pb], (uint32_t)(((j - NP) / NP) & 1), b, a.err)) { ok = false; break; }
+            if (j >= 1 && __any_sync(0xffffffffu, resc)) {
+                // O holds the blocks before j: rescale it once their P V MMA is done
+                const int m = j - 1;
+                if (!warp_wait(&b.pv_done[m % NP], (uint32_t)((m / NP) & 1), b, a.err)) { ok = false; break; }
+                tc::fence_after_sync();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tc::tmem_ld32(tl + C::COL_O + c * 32, o);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tc::tmem_st32(tl + C::COL_O + c * 32, o);
+                }
+                tc::tmem_wait_st();
+            }
+            // pass 2: P = 2^(s - m) into shared memory, row sums
+            const float moff = (m_use == neg_inf()) ? 0.f : m_use;
+            unsigned char *pbuf = pbase + pb * C::PBUF;
+#pragma unroll
+            for (int c = 0; c < kBN / 32; ++c) {
+                uint32_t v[32];
+                float m2[32];
+                mask_chunk<T, MK>(a, mrow, j0 + c * 32, row_ok, m2);
+                tc::tmem_ld32(tl + sb * kBN + c * 32, v);
+                tc::tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float s0 = fmaf(__uint_as_float(v[e]), sl2, m2[e]);
+                    float s1 = fmaf(__uint_as_float(v[e + 1]), sl2, m2[e + 1]);
+                    if (pred) {
+                        const int col = j0 + c * 32 + e;
+                        if (col >= a.S || (a.causal && col > i)) s0 = neg_inf();
+                        if (col + 1 >= a.S || (a.causal && col + 1 > i)) s1 = neg_inf();
+                    }
+                    const float p0 = ex2(s0 - moff), p1 = ex2(s1 - moff);
+                    l += p0 + p1;
+                    pk[e / 2] = pack2(p0, p1, static_cast<T *>(nullptr));
+                }
+                unsigned char *atom = pbuf + (c / 2) * kAtom;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t off = tc::sw128_off((uint32_t)r, (uint32_t)((c & 1) * 4 + q));
+                    *reinterpret_cast<uint4 *>(atom + off) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                }
+            }
+            tc::fence_before_sync();
+            mbar_arrive(&b.s_free[sb]);
+            tc::fence_async_smem();
+            mbar_arrive(&b.p_full[pb]);
+            m_run = m_use;
+        }
+        // epilogue: O / l, lse
+        if (ok) {
+            const int m = nkv - 1;
+            ok = warp_wait(&b.pv_done[m % NP], (uint32_t)((m / NP) & 1), b, a.err);
+        }
+        if (ok) {
+            tc::fence_after_sync();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            T *orow = reinterpret_cast<T *>(a.o) + ((int64_t)bh * a.S + i) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tc::tmem_ld32(tl + C::COL_O + c * 32, o);
+                tc::tmem_wait_ld();
+                if (row_ok) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        float f[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[8 * v + e]) * inv;
+                        st_stream(orow + c * 32 + 8 * v, pack<T>(f));
+                    }
+                }
+            }
+            if (row_ok && a.lse)
+                a.lse[(int64_t)bh * a.S + i] = l > 0.f ? (m_run + log2f(l)) * 0.6931471805599453f : neg_inf();
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against libcuda).
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                              const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn()
+{
+    static EncodeFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeFn>(p);
+    }();
+    return fn;
+}
+
+}  // namespace
+
+// [B*H, S, D] 16-bit tensor, boxes of 64 x 128 x 1, 128-byte swizzle; rows
+// beyond S of a head read as zeros.
+cudaError_t attn_tensor_map(CUtensorMap *m, const void *base, int dtype, int BH, int S, int D)
+{
+    EncodeFn fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)BH};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(m, dtype == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                          const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+namespace {
+
+template <typename T, int D, int MK>
+cudaError_t launch_fwd(const AttnArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                       cudaStream_t st)
+{
+    auto kern = attn_fwd_kernel<T, D, MK>;
+    constexpr uint32_t smem = FwdCfg<D>::SMEM;
+    static_assert(sizeof(FwdBars) <= FwdCfg<D>::BAR_BYTES, "barrier area");
+    static std::atomic<int> attr_done[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (!attr_done[dev & 63].load(std::memory_order_acquire)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_done[dev & 63].store(1, std::memory_order_release);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(((a.S + kBM - 1) / kBM) * a.B * a.H));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, a);
+}
+
+template <typename T, int D>
+cudaError_t launch_fwd_mk(const AttnArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                          cudaStream_t st)
+{
+    if (!a.mask) return launch_fwd<T, D, 0>(a, tq, tk, tv, st);
+    if (a.mask_bool) return launch_fwd<T, D, 2>(a, tq, tk, tv, st);
+    return launch_fwd<T, D, 1>(a, tq, tk, tv, st);
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const AttnArgs &a, cudaStream_t st)
+{
+    CUtensorMap tq, tk, tv;
+    cudaError_t e;
+    const int BH = a.B * a.H;
+    if ((e = attn_tensor_map(&tq, a.q, a.dtype, BH, a.S, a.D)) != cudaSuccess) return e;
+    if ((e = attn_tensor_map(&tk, a.k, a.dtype, BH, a.S, a.D)) != cudaSuccess) return e;
+    if ((e = attn_tensor_map(&tv, a.v, a.dtype, BH, a.S, a.D)) != cudaSuccess) return e;
+    if (a.dtype == kBF16) {
+        return a.D == 128 ? launch_fwd_mk<__nv_bfloat16, 128>(a, tq, tk, tv, st)
+                          : launch_fwd_mk<__nv_bfloat16, 64>(a, tq, tk, tv, st);
+    }
+    return a.D == 128 ? launch_fwd_mk<__half, 128>(a, tq, tk, tv, st) : launch_fwd_mk<__half, 64>(a, tq, tk, tv, st);
+}
+
+}  // namespace sms

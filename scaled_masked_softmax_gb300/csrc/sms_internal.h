@@ -80,6 +80,14 @@ cudaError_t launch_bwd_online(const BwdArgs &a, int dtype, cudaStream_t st);
 // multiprocessor count of the current device (cached per device)
 int sm_count();
 
+// Shared with the attention entry points (sms_attn_abi.cu): the calling
+// thread's last-error text, the process-wide launch counter, and the current
+// device's error word.
+int set_last_error(int status, const char *msg);
+void clear_last_error();
+void count_launch();
+cudaError_t device_error_word(int **err);
+
 // CTAs for a persistent kernel: `per_sm` per multiprocessor, at most `useful`,
 // at most the limit set by sms_set_grid_limit
 int64_t persistent_grid(int per_sm, int64_t useful);

@@ -185,3 +185,19 @@ def make_inputs(w: Workload, device="cpu", with_dy: Optional[bool] = None):
     return {"x": x, "mask": mask, "dy": dy, "mask_stride_b": sb, "mask_stride_h": sh, "heads": heads,
             "key_lengths": key_lengths}
 
+
+
+def attention_inputs(B: int, H: int, S: int, D: int, dtype: str, seed: int, device="cpu", sigma: float = 1.0,
+                     with_do: bool = False):
+    """Seeded q, k, v (and dO) of a [B, H, S, D] attention step: entries
+    ~ N(0, sigma^2) for q and k (so q.k ~ N(0, D sigma^4), the score
+    distribution the softmax workloads model with x ~ N(0, d_k)), v and dO
+    ~ N(0, 1), drawn in fp32 on ``device`` and rounded to ``dtype``."""
+    dt = DTYPES[dtype]
+    g = torch.Generator(device=torch.device(device)).manual_seed(seed)
+    shape = (B, H, S, D)
+    q = (torch.randn(shape, generator=g, device=device) * sigma).to(dt)
+    k = (torch.randn(shape, generator=g, device=device) * sigma).to(dt)
+    v = torch.randn(shape, generator=g, device=device).to(dt)
+    d_o = torch.randn(shape, generator=g, device=device).to(dt) if with_do else None
+    return q, k, v, d_o

@@ -263,3 +263,34 @@ def test_build_compiles_every_kernel_source():
 
     cu = sorted(f for f in os.listdir(build.CSRC) if f.endswith(".cu"))
     assert sorted(build.SOURCES) == cu
+
+
+def _attn(**kw):
+    a = dict(q=0x100000, k=0x200000, v=0x300000, mask=None, mask_numel=0, sb=0, sh=0, mbool=0, o=0x400000,
+             lse=0x500000, B=1, H=2, S=16, D=64, scale=0.125, causal=0, dtype=binding.SMS_BF16, stream=None)
+    a.update(kw)
+    return binding.lib().sms_attention_forward(a["q"], a["k"], a["v"], a["mask"], a["mask_numel"], a["sb"], a["sh"],
+                                               a["mbool"], a["o"], a["lse"], a["B"], a["H"], a["S"], a["D"],
+                                               a["scale"], a["causal"], a["dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dtype=binding.SMS_F32), UNSUPPORTED), (dict(D=96), UNSUPPORTED), (dict(D=256), UNSUPPORTED),
+    (dict(dtype=7), INVALID), (dict(q=None), INVALID), (dict(v=None), INVALID), (dict(o=None), INVALID),
+    (dict(k=0x200008), INVALID), (dict(o=0x400004), INVALID), (dict(lse=0x500002), INVALID),
+    (dict(B=-1), INVALID), (dict(scale=float("nan")), INVALID),
+    (dict(o=0x100000), INVALID),  # o aliases q
+    (dict(lse=0x400010), INVALID),  # lse inside o
+    (dict(mask=0x600000, mask_numel=16 * 16 - 1), INVALID),  # [S,S] mask one element short
+    (dict(mask=0x600000, mask_numel=512, sb=-1), INVALID), (dict(mask=0x600008, mask_numel=512), INVALID),
+    (dict(mask=0x600000, mask_numel=256, sh=256), INVALID),  # [1,H,S,S] needs 512
+])
+def test_attention_rejects_bad_arguments(kw, status):
+    assert _attn(**kw) == status
+    assert binding.lib().sms_last_error().decode().startswith("sms_attention_forward")
+
+
+def test_attention_empty_problem_is_a_no_op():
+    for kw in (dict(B=0), dict(H=0), dict(S=0)):
+        assert _attn(q=None, k=None, v=None, o=None, **kw) in (INVALID, binding.SMS_OK)
+    assert _attn(B=0) == binding.SMS_OK

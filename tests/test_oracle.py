@@ -88,6 +88,15 @@ def test_decode_bf16_every_bit_pattern():
     assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
 
 
+def test_decode_one_element_equals_the_array_decoder():
+    bits = np.arange(0, 65536, 97, dtype=np.uint32).astype(np.uint16)
+    for code in (oracle.F16, oracle.BF16):
+        whole = oracle.decode(bits, code)
+        for i in range(0, bits.size, 7):
+            one = oracle.decode_one(bits, i, code)
+            assert (np.isnan(one) and np.isnan(whole[i])) or one == whole[i]
+
+
 def test_decode_f32_random_bit_patterns():
     rng = np.random.default_rng(7)
     bits = rng.integers(0, 2**32, size=4096, dtype=np.uint64).astype(np.uint32)

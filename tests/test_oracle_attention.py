@@ -154,3 +154,52 @@ def test_inputs_are_decoded_exactly():
     b = A.attention_forward(q.double(), k.double(), v.double(), 0.5, True)
     assert np.array_equal(a, b)
     assert np.array_equal(oracle.decode(q).reshape(q.shape), q.double().numpy())
+
+
+# ------------------------------------------------------------- log-sum-exp ---
+
+@pytest.mark.parametrize("layout", ["none", "SS", "B1SS", "BHSS", "bool"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_lse_matches_torch_logsumexp(layout, causal):
+    """The per-row log of the softmax denominator against torch.logsumexp of
+    the same masked scores (fp64, a library routine)."""
+    B, H, S = 2, 3, 13
+    q, k, v = _qkv(B, H, S, 8, 4, 21)
+    g = torch.Generator().manual_seed(22)
+    shape = {"none": None, "SS": (S, S), "B1SS": (B, 1, S, S), "BHSS": (B, H, S, S), "bool": (B, 1, S, S)}[layout]
+    sb, sh = {"none": (0, 0), "SS": (0, 0), "B1SS": (S * S, 0), "BHSS": (H * S * S, S * S),
+              "bool": (S * S, 0)}[layout]
+    mask = None
+    full = torch.zeros(B, H, S, S, dtype=torch.float64)
+    if layout == "bool":
+        mask = torch.rand(shape, generator=g) < 0.3
+        mask[..., 0] = False
+        full = torch.zeros(shape, dtype=torch.float64).masked_fill(mask, -math.inf).expand(B, H, S, S)
+    elif shape is not None:
+        mask = torch.randn(shape, generator=g, dtype=torch.float64) * 2
+        full = mask.expand(B, H, S, S)
+    scale = 0.3
+    O, lse = A.attention_forward(q, k, v, scale, causal, mask, sb, sh, return_lse=True)
+    s = torch.matmul(q, k.transpose(-1, -2)) * scale + full
+    if causal:
+        s = s.masked_fill(torch.ones(S, S, dtype=torch.bool).triu(1), -math.inf)
+    ref = torch.logsumexp(s, -1).numpy()
+    assert np.abs(lse - ref).max() < 1e-12
+
+
+def test_lse_closed_forms():
+    # zero queries: every kept score is 0, so lse = log(number of kept keys):
+    # log S without causal, log(i + 1) for row i under causal; a row with every
+    # key masked is -inf
+    B, H, S = 1, 2, 6
+    _, k, v = _qkv(B, H, S, 4, 3, 23)
+    q = torch.zeros(B, H, S, 4, dtype=torch.float64)
+    _, lse = A.attention_forward(q, k, v, 1.0, False, return_lse=True)
+    assert np.allclose(lse, math.log(S), rtol=0, atol=1e-15)
+    _, lse_c = A.attention_forward(q, k, v, 1.0, True, return_lse=True)
+    assert np.allclose(lse_c, np.log(np.arange(1, S + 1))[None, None, :], rtol=0, atol=1e-15)
+    mask = torch.zeros(S, S, dtype=torch.bool)
+    mask[2, :] = True
+    _, lse_m = A.attention_forward(q, k, v, 1.0, False, mask, return_lse=True)
+    assert np.all(np.isneginf(lse_m[:, :, 2]))
+    assert np.allclose(np.delete(lse_m, 2, axis=2), math.log(S), rtol=0, atol=1e-15)
