@@ -229,6 +229,39 @@ SMS_API int sms_attention_forward(const void *q, const void *k, const void *v, c
                                   float *lse, int64_t batch, int64_t heads, int64_t seq, int64_t head_dim,
                                   float scale, int is_causal, int dtype, void *stream);
 
+/*
+ * Backward of sms_attention_forward: dQ, dK and dV of sum(dO * O), by the
+ * chain rule through the three steps (the softmax Jacobian of the page
+ * "用CUDA自定义融合Softmax算子并封装进PyTorch" §3.3 in the middle):
+ *       P = softmax(...) recomputed from q, k, the mask and lse;
+ *       dV = P^T dO,  dP = dO V^T,  dS = scale * P * (dP - rowsum(dO * O)),
+ *       dQ = dS K,    dK = dS^T Q.
+ *   q, k, v, mask, scale, is_causal, sizes, dtype   as given to the forward
+ *   o, lse          the forward's outputs
+ *   d_o             the upstream gradient [batch, heads, seq, head_dim]
+ *   dq, dk, dv      results, same shape and dtype; none may overlap another
+ *                   buffer
+ *   workspace       caller-owned device scratch of at least
+ *                   sms_attention_backward_workspace() bytes, 16-byte aligned
+ *                   (an fp32 dQ accumulator and an fp32 value per query row);
+ *                   its contents on entry do not matter, and it must not be
+ *                   used by anything else until the call's kernels are done
+ * Three kernels are enqueued on `stream`.  Arithmetic: the five products on
+ * tcgen05.mma with fp32 accumulation; P and dS are rounded to `dtype` as MMA
+ * operands; dQ accumulates in fp32 across key blocks; every gradient is
+ * rounded once to `dtype`.  Errors as sms_attention_forward, plus
+ * SMS_ERR_INVALID_ARG for a missing or small workspace.
+ */
+SMS_API int sms_attention_backward(const void *q, const void *k, const void *v, const void *o, const void *d_o,
+                                   const float *lse, const void *mask, int64_t mask_numel, int64_t mask_stride_b,
+                                   int64_t mask_stride_h, int mask_is_bool, void *dq, void *dk, void *dv,
+                                   void *workspace, int64_t workspace_bytes, int64_t batch, int64_t heads,
+                                   int64_t seq, int64_t head_dim, float scale, int is_causal, int dtype,
+                                   void *stream);
+
+/* Bytes of workspace sms_attention_backward needs (-1 for a negative size). */
+SMS_API int64_t sms_attention_backward_workspace(int64_t batch, int64_t heads, int64_t seq, int64_t head_dim);
+
 /* Static description of a status code. */
 SMS_API const char *sms_status_string(int status);
 

@@ -56,6 +56,8 @@ def attention_forward(q, k, v, scale: float, is_causal: bool = False, mask=None,
     if K.shape != (B, H, S, D) or V.shape[:3] != (B, H, S):
         raise ValueError("q, k, v must share B, H and S (square attention), q and k the head dim")
     scores = np.matmul(Q, np.swapaxes(K, -1, -2))  # [B, H, S, S]
+    if mask is not None and not _is_bool(mask):
+        mask = decode(mask)  # an additive mask of the inputs' storage dtype, widened exactly
     P = _softmax_forward(scores.reshape(-1, S), S, scale, is_causal, mask, mask_stride_b, mask_stride_h, H)
     P = P.reshape(B, H, S, S)
     O = np.matmul(P, V)

@@ -67,3 +67,59 @@ def attention_forward(q, k, v, mask: Optional[torch.Tensor] = None, scale: Optio
                                       st)
     del keep
     return (o, lse) if return_lse else o
+
+
+def attention_backward(q, k, v, o, lse, d_o, mask: Optional[torch.Tensor] = None, scale: Optional[float] = None,
+                       is_causal: bool = False):
+    """(dQ, dK, dV) of sum(dO * O) for the forward that produced o and lse
+    (the same q, k, v, mask, scale and causal flag).  The fp32 scratch the
+    kernels need is taken from PyTorch's allocator for the call."""
+    _check_qkv(q, k, v)
+    B, H, S, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    q, k, v, o, d_o = _aligned(q), _aligned(k), _aligned(v), _aligned(o), _aligned(d_o)
+    if o.shape != q.shape or d_o.shape != q.shape or o.dtype != q.dtype or d_o.dtype != q.dtype:
+        raise ValueError("o and d_o must match q in shape and dtype")
+    lse = _aligned(lse.to(torch.float32))
+    mptr, mnum, sb, sh, is_bool, keep = _mask_args(mask, q)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    nws = binding.sms_attention_backward_workspace(B, H, S, D)
+    ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        st = torch.cuda.current_stream(q.device).cuda_stream
+        binding.sms_attention_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), d_o.data_ptr(),
+                                       lse.data_ptr(), mptr, mnum, sb, sh, is_bool, dq.data_ptr(), dk.data_ptr(),
+                                       dv.data_ptr(), ws.data_ptr(), ws.numel(), B, H, S, D, float(scale), is_causal,
+                                       _DT[q.dtype], st)
+    del keep, ws
+    return dq, dk, dv
+
+
+class FusedAttentionFunction(torch.autograd.Function):
+    """O = fused attention of (q, k, v); the backward reruns the tensor-core
+    backward from q, k, v, O and the saved per-row log-sum-exp.  No gradient
+    flows to the mask, the scale or the causal flag."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, mask, scale, is_causal):
+        o, lse = attention_forward(q, k, v, mask, scale, is_causal, return_lse=True)
+        ctx.save_for_backward(q, k, v, o, lse, mask if mask is not None else torch.empty(0, device=q.device))
+        ctx.has_mask = mask is not None
+        ctx.scale, ctx.is_causal = scale, is_causal
+        return o
+
+    @staticmethod
+    def backward(ctx, d_o):
+        q, k, v, o, lse, mask = ctx.saved_tensors
+        dq, dk, dv = attention_backward(q, k, v, o, lse, d_o.contiguous(), mask if ctx.has_mask else None, ctx.scale,
+                                        ctx.is_causal)
+        return dq, dk, dv, None, None, None
+
+
+def fused_attention(q, k, v, mask: Optional[torch.Tensor] = None, scale: Optional[float] = None,
+                    is_causal: bool = False):
+    """Differentiable O = softmax(Q K^T * scale + mask, causal) V on the tensor cores."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    return FusedAttentionFunction.apply(q, k, v, mask, float(scale), bool(is_causal))

@@ -29,6 +29,9 @@ SIGNATURES = {
     "sms_backward_lengths": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _f32, _i32, _i32, _vp]),
     "sms_attention_forward": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _i64, _i64, _i64, _i64,
                                      _f32, _i32, _i32, _vp]),
+    "sms_attention_backward": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _vp, _vp,
+                                      _i64, _i64, _i64, _i64, _i64, _f32, _i32, _i32, _vp]),
+    "sms_attention_backward_workspace": (_i64, [_i64, _i64, _i64, _i64]),
     "sms_status_string": (_cp, [_i32]),
     "sms_last_error": (_cp, []),
     "sms_set_forced_path": (_i32, [_i32]),
@@ -109,6 +112,19 @@ def sms_attention_forward(q, k, v, mask, mask_numel, mask_stride_b, mask_stride_
     _check(lib().sms_attention_forward(q, k, v, mask, mask_numel, mask_stride_b, mask_stride_h, int(bool(mask_is_bool)),
                                        o, lse, batch, heads, seq, head_dim, scale, int(bool(is_causal)), dtype,
                                        stream))
+
+
+def sms_attention_backward(q, k, v, o, d_o, lse, mask, mask_numel, mask_stride_b, mask_stride_h, mask_is_bool, dq, dk,
+                           dv, workspace, workspace_bytes, batch, heads, seq, head_dim, scale, is_causal, dtype,
+                           stream) -> None:
+    """Fused attention backward on the tensor cores: see include/sms.h."""
+    _check(lib().sms_attention_backward(q, k, v, o, d_o, lse, mask, mask_numel, mask_stride_b, mask_stride_h,
+                                        int(bool(mask_is_bool)), dq, dk, dv, workspace, workspace_bytes, batch, heads,
+                                        seq, head_dim, scale, int(bool(is_causal)), dtype, stream))
+
+
+def sms_attention_backward_workspace(batch, heads, seq, head_dim) -> int:
+    return int(lib().sms_attention_backward_workspace(batch, heads, seq, head_dim))
 
 
 def sms_set_forced_path(path: int) -> int:

@@ -116,4 +116,71 @@ int sms_attention_forward(const void *q, const void *k, const void *v, const voi
     return launch_result(launch_attn_fwd(a, static_cast<cudaStream_t>(stream)), who);
 }
 
+int64_t sms_attention_backward_workspace(int64_t batch, int64_t heads, int64_t seq, int64_t head_dim)
+{
+    if (batch < 0 || heads < 0 || seq < 0 || head_dim < 0) return -1;
+    const int64_t rows = batch * heads * seq;
+    return rows * head_dim * 4 + rows * 4;  // fp32 dQ accumulator, then fp32 delta per query row
+}
+
+int sms_attention_backward(const void *q, const void *k, const void *v, const void *o, const void *d_o,
+                           const float *lse, const void *mask, int64_t mask_numel, int64_t mask_stride_b,
+                           int64_t mask_stride_h, int mask_is_bool, void *dq, void *dk, void *dv, void *workspace,
+                           int64_t workspace_bytes, int64_t batch, int64_t heads, int64_t seq, int64_t head_dim,
+                           float scale, int is_causal, int dtype, void *stream)
+{
+    const char *who = "sms_attention_backward";
+    clear_last_error();
+    bool empty = false;
+    int rc = check_common(who, q, k, v, mask, mask_numel, mask_stride_b, mask_stride_h, mask_is_bool, batch, heads,
+                          seq, head_dim, scale, dtype, empty);
+    if (rc != SMS_OK || empty) return rc;
+    if (!o || !d_o || !al16(o) || !al16(d_o)) return fail(SMS_ERR_INVALID_ARG, who, "o and d_o must be 16-byte aligned, non-NULL");
+    if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u)) return fail(SMS_ERR_INVALID_ARG, who, "lse must be a 4-byte aligned, non-NULL pointer");
+    if (!dq || !dk || !dv || !al16(dq) || !al16(dk) || !al16(dv))
+        return fail(SMS_ERR_INVALID_ARG, who, "dq, dk and dv must be 16-byte aligned, non-NULL");
+    const int64_t need = sms_attention_backward_workspace(batch, heads, seq, head_dim);
+    if (!workspace || !al16(workspace) || workspace_bytes < need)
+        return fail(SMS_ERR_INVALID_ARG, who, "workspace must be 16-byte aligned with at least "
+                                              "sms_attention_backward_workspace() bytes");
+    const int64_t nt = batch * heads * seq * head_dim * 2, nl = batch * heads * seq * 4;
+    const int64_t nm = mask ? mask_numel * (mask_is_bool ? 1 : 2) : 0;
+    const void *ins[] = {q, k, v, o, d_o};
+    void *outs[] = {dq, dk, dv};
+    for (void *w : outs) {
+        for (const void *x : ins)
+            if (overlap(w, nt, x, nt)) return fail(SMS_ERR_INVALID_ARG, who, "a gradient overlaps an input");
+        if (overlap(w, nt, lse, nl) || overlap(w, nt, mask, nm) || overlap(w, nt, workspace, need))
+            return fail(SMS_ERR_INVALID_ARG, who, "a gradient overlaps lse, the mask or the workspace");
+    }
+    if (overlap(dq, nt, dk, nt) || overlap(dq, nt, dv, nt) || overlap(dk, nt, dv, nt))
+        return fail(SMS_ERR_INVALID_ARG, who, "dq, dk and dv overlap");
+    for (const void *x : ins)
+        if (overlap(workspace, need, x, nt)) return fail(SMS_ERR_INVALID_ARG, who, "the workspace overlaps an input");
+    if (overlap(workspace, need, lse, nl) || overlap(workspace, need, mask, nm))
+        return fail(SMS_ERR_INVALID_ARG, who, "the workspace overlaps lse or the mask");
+    int *err = nullptr;
+    cudaError_t e = device_error_word(&err);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SMS_ERR_CUDA, who, "device query failed");
+    }
+    AttnArgs a = {};
+    a.q = q; a.k = k; a.v = v;
+    a.mask = mask; a.mask_total = mask ? mask_numel : 0; a.msb = mask_stride_b; a.msh = mask_stride_h;
+    a.mask_bool = (mask && mask_is_bool) ? 1 : 0;
+    a.B = (int)batch; a.H = (int)heads; a.S = (int)seq; a.D = (int)head_dim;
+    a.scale = scale; a.causal = is_causal ? 1 : 0; a.dtype = dtype; a.err = err;
+    a.o_in = o; a.dout = d_o; a.lse_in = lse;
+    a.dq = dq; a.dk = dk; a.dv = dv;
+    a.dq_acc = static_cast<float *>(workspace);
+    a.delta = reinterpret_cast<float *>(static_cast<char *>(workspace) + batch * heads * seq * head_dim * 4);
+    e = launch_attn_bwd(a, static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) {  // three kernels: delta, the main pass, dQ
+        count_launch();
+        count_launch();
+    }
+    return launch_result(e, who);
+}
+
 }  // extern "C"

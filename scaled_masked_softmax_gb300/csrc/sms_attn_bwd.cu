@@ -1,0 +1,476 @@
+// Fused attention backward on the 5th-generation tensor cores: the gradient
+// of O = softmax(Q K^T * scale + mask, causal) V by the chain rule through
+// the three steps (the forward's §4.4 / §2.2 fusion, differentiated with
+// the softmax Jacobian of "用CUDA自定义融合Softmax算子并封装进PyTorch" §3.3):
+//     P     = exp(Q K^T * scale + mask - lse)     (recomputed, never stored)
+//     dV    = P^T dO,          dP = dO V^T
+//     delta = rowsum(dO * O)   (= rowsum(P * dP))
+//     dS    = scale * P * (dP - delta)
+//     dQ    = dS K,            dK = dS^T Q
+//
+// Three kernels on the caller's stream:
+//   1. attn_bwd_pre: delta per query row into the workspace, and the fp32 dQ
+//      accumulator in the workspace cleared;
+//   2. attn_bwd_kernel: one CTA per (batch, head, block of 128 keys) walks the
+//      query blocks (those at or after its keys under causal).  Per block:
+//        S^T = K Q^T and dP^T = V dO^T on tcgen05 into TMEM (keys in lanes);
+//        128 threads (one key each) form P^T and dS^T as 16-bit values in
+//        shared memory in the MMA's swizzled layout;
+//        dV += P^T dO and dK += dS^T Q accumulate in TMEM; dQ_blk = dS K goes
+//        to TMEM (reusing the S^T columns) and the same threads, now one query
+//        row each, add it to the fp32 accumulator with vector reductions.
+//      At the end dK and dV leave TMEM once, rounded to the 16-bit dtype;
+//   3. attn_bwd_post: dQ = the accumulator rounded to the 16-bit dtype.
+// Roles: warp 0 one lane issues the TMA loads (K and V once, Q and dO per
+// query block), warp 1 one lane the MMAs (and owns TMEM), warps 2..5 the
+// element-wise work.  Every mbarrier wait is bounded (2 s) as in the forward.
+#include <cuda.h>
+
+#include <atomic>
+
+#include "sms_attn.h"
+#include "sms_common.cuh"
+#include "sms_internal.h"
+#include "sms_tc.cuh"
+
+namespace sms {
+
+cudaError_t attn_tensor_map(CUtensorMap *m, const void *base, int dtype, int BH, int S, int D);
+
+namespace {
+
+constexpr int kBM = 128;          // keys per CTA (the MMA's M for S^T, dP^T, dV, dK)
+constexpr int kBN = 128;          // queries per block
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAtom = 16384;
+
+template <int D> struct BwdCfg {
+    static constexpr int NST = D == 128 ? 1 : 2;          // Q / dO stages
+    static constexpr uint32_t TILE = (D / 64) * kAtom;    // 128 x D
+    static constexpr uint32_t SQ = 2 * kAtom;             // 128 x 128 (P^T, dS^T)
+    static constexpr uint32_t OFF_K = 0;
+    static constexpr uint32_t OFF_V = OFF_K + TILE;
+    static constexpr uint32_t OFF_Q = OFF_V + TILE;
+    static constexpr uint32_t OFF_DO = OFF_Q + NST * TILE;
+    static constexpr uint32_t OFF_P = OFF_DO + NST * TILE;
+    static constexpr uint32_t OFF_DS = OFF_P + SQ;
+    static constexpr uint32_t OFF_LSE = OFF_DS + SQ;       // 128 floats: lse * log2e (+inf: fully masked)
+    static constexpr uint32_t OFF_DEL = OFF_LSE + 512;     // 128 floats: delta
+    static constexpr uint32_t OFF_BAR = OFF_DEL + 512;
+    static constexpr uint32_t BAR_BYTES = 512;
+    static constexpr uint32_t SMEM = OFF_BAR + BAR_BYTES + 1024;
+    static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 256 + D, COL_DQ = 0;
+};
+
+struct BwdBars {
+    uint64_t kv_full;
+    uint64_t q_full[2], q_empty[2];
+    uint64_t s_full, ds_full, dq_full, dq_free;
+    uint64_t mma_drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+template <typename T> struct AbFmt;
+template <> struct AbFmt<__half> { static constexpr int v = 0; };
+template <> struct AbFmt<__nv_bfloat16> { static constexpr int v = 1; };
+
+__device__ __forceinline__ bool wait_or_flag(uint64_t *bar, uint32_t parity, BwdBars &b, int *err)
+{
+    if (mbar_wait_bounded(bar, parity, &b.abort)) return true;
+    *reinterpret_cast<volatile int *>(&b.abort) = 1;
+    report_error(err, SMS_DEVERR_ATTN_WAIT);
+    return false;
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, BwdBars &b, int *err)
+{
+    const bool w = wait_or_flag(bar, parity, b, err);
+    return __all_sync(0xffffffffu, w);
+}
+
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > kWaitLimitNs) return;
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, __half *)
+{
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, __nv_bfloat16 *)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Mask terms (log2-scaled) of key j for the 32 queries i0 .. i0+31: element
+// (i, j) sits at mrow0 + i*S + j.  Queries at or beyond S read nothing.
+template <typename T, int MK>
+__device__ __forceinline__ void mask_col(const AttnArgs &a, int64_t mbase, int i0, bool key_ok, float (&m2)[32])
+{
+#pragma unroll
+    for (int e = 0; e < 32; ++e) m2[e] = 0.f;
+    if constexpr (MK != 0) {
+        if (!key_ok) return;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            const int i = i0 + e;
+            if (i < a.S) {
+                const int64_t off = mbase + (int64_t)i * a.S;
+                if constexpr (MK == 1) m2[e] = to_f32<T>(reinterpret_cast<const T *>(a.mask)[off]) * kLog2e;
+                else m2[e] = reinterpret_cast<const uint8_t *>(a.mask)[off] ? neg_inf() : 0.f;
+            }
+        }
+    }
+}
+
+template <typename T, int D, int MK>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo, const AttnArgs a)
+{
+    using C = BwdCfg<D>;
+    constexpr int NST = C::NST;
+    constexpr int FMT = AbFmt<T>::v;
+    constexpr uint32_t IDESC_SQ = tc::idesc_f16(FMT, 0, kBM, kBN);          // S^T, dP^T: K-major A and B
+    constexpr uint32_t IDESC_ACC = tc::idesc_f16(FMT, 1, kBM, D);           // dV, dK: K-major A, MN-major B
+    constexpr uint32_t IDESC_DQ = tc::idesc_f16(FMT, 1, kBN, D, 1);         // dQ: MN-major A and B
+
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw));
+    unsigned char *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    BwdBars &b = *reinterpret_cast<BwdBars *>(smem + C::OFF_BAR);
+    const uint32_t s_base = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    float *s_lse = reinterpret_cast<float *>(smem + C::OFF_LSE);
+    float *s_del = reinterpret_cast<float *>(smem + C::OFF_DEL);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int BH = a.B * a.H;
+    const int nkb = (a.S + kBM - 1) / kBM;
+    const int kb = nkb - 1 - (int)(blockIdx.x / (unsigned)BH);
+    const int bh = (int)(blockIdx.x % (unsigned)BH);
+    const int j0 = kb * kBM;
+    const int nqb = (a.S + kBN - 1) / kBN;
+    const int qb0 = a.causal ? j0 / kBN : 0;  // query blocks before the keys see none of them
+    const int npair = nqb - qb0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&b.kv_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&b.q_full[s], 1);
+            mbar_init(&b.q_empty[s], 1);
+        }
+        mbar_init(&b.s_full, 1);
+        mbar_init(&b.ds_full, kBM);
+        mbar_init(&b.dq_full, 1);
+        mbar_init(&b.dq_free, kBM);
+        mbar_init(&b.mma_drain, 1);
+        b.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tc::tmem_alloc(&b.tmem_base, kTmemCols);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = b.tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA loads ---
+        if (lane == 0) {
+            tc::prefetch_tmap(&tmq);
+            tc::prefetch_tmap(&tmk);
+            tc::prefetch_tmap(&tmv);
+            tc::prefetch_tmap(&tmdo);
+            mbar_arrive_expect_tx(&b.kv_full, 2 * C::TILE);
+#pragma unroll
+            for (int at = 0; at < D / 64; ++at) {
+                tc::tma_load_3d(smem + C::OFF_K + at * kAtom, &tmk, at * 64, j0, bh, &b.kv_full);
+                tc::tma_load_3d(smem + C::OFF_V + at * kAtom, &tmv, at * 64, j0, bh, &b.kv_full);
+            }
+            int armed = 0;
+            for (int n = 0; n < npair; ++n) {
+                const int st = n % NST, i0 = (qb0 + n) * kBN;
+                if (n >= NST && !wait_or_flag(&b.q_empty[st], (uint32_t)((n / NST - 1) & 1), b, a.err)) break;
+                if (*reinterpret_cast<volatile int *>(&b.abort)) break;
+                mbar_arrive_expect_tx(&b.q_full[st], 2 * C::TILE);
+#pragma unroll
+                for (int at = 0; at < D / 64; ++at) {
+                    tc::tma_load_3d(smem + C::OFF_Q + st * C::TILE + at * kAtom, &tmq, at * 64, i0, bh, &b.q_full[st]);
+                    tc::tma_load_3d(smem + C::OFF_DO + st * C::TILE + at * kAtom, &tmdo, at * 64, i0, bh, &b.q_full[st]);
+                }
+                armed = n + 1;
+            }
+            drain_wait(&b.kv_full, 0);
+            for (int n = (armed > NST ? armed - NST : 0); n < armed; ++n) drain_wait(&b.q_full[n % NST], (uint32_t)((n / NST) & 1));
+        }
+    } else if (warp == 1) {
+        // ----------------------------------------------------------- MMAs ---
+        if (lane == 0) {
+            bool ok = wait_or_flag(&b.kv_full, 0, b, a.err);
+            const uint32_t k_addr = s_base + C::OFF_K, v_addr = s_base + C::OFF_V;
+            const uint32_t p_addr = s_base + C::OFF_P, ds_addr = s_base + C::OFF_DS;
+            for (int n = 0; ok && n < npair; ++n) {
+                const int st = n % NST;
+                const uint32_t q_addr = s_base + C::OFF_Q + st * C::TILE, do_addr = s_base + C::OFF_DO + st * C::TILE;
+                if (!wait_or_flag(&b.q_full[st], (uint32_t)((n / NST) & 1), b, a.err)) { ok = false; break; }
+                // S^T shares its columns with the previous block's dQ: drained first
+                if (n >= 1 && !wait_or_flag(&b.dq_free, (uint32_t)((n - 1) & 1), b, a.err)) { ok = false; break; }
+                tc::fence_after_sync();
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t ko = (k / 4) * kAtom + (k % 4) * 32;
+                    tc::mma_f16(tmem + C::COL_S, tc::desc_sw128(k_addr + ko, 16, 1024), tc::desc_sw128(q_addr + ko, 16, 1024),
+                                IDESC_SQ, k > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t ko = (k / 4) * kAtom + (k % 4) * 32;
+                    tc::mma_f16(tmem + C::COL_DP, tc::desc_sw128(v_addr + ko, 16, 1024),
+                                tc::desc_sw128(do_addr + ko, 16, 1024), IDESC_SQ, k > 0 ? 1u : 0u);
+                }
+                tc::commit(&b.s_full);
+                if (!wait_or_flag(&b.ds_full, (uint32_t)(n & 1), b, a.err)) { ok = false; break; }
+                tc::fence_after_sync();
+#pragma unroll
+                for (int k = 0; k < kBN / 16; ++k) {
+                    const uint32_t ka = (k / 4) * kAtom + (k % 4) * 32;  // K-major slice of P^T / dS^T
+                    const uint32_t kb_ = k * 2048;                      // MN-major slice of dO / Q
+                    const uint32_t acc = (n > 0 || k > 0) ? 1u : 0u;
+                    tc::mma_f16(tmem + C::COL_DV, tc::desc_sw128(p_addr + ka, 16, 1024),
+                                tc::desc_sw128(do_addr + kb_, kAtom, 1024), IDESC_ACC, acc);
+                    tc::mma_f16(tmem + C::COL_DK, tc::desc_sw128(ds_addr + ka, 16, 1024),
+                                tc::desc_sw128(q_addr + kb_, kAtom, 1024), IDESC_ACC, acc);
+                }
+#pragma unroll
+                for (int k = 0; k < kBM / 16; ++k) {
+                    // dQ = dS K: A = dS (queries x keys) read MN-major from dS^T, B = K MN-major
+                    tc::mma_f16(tmem + C::COL_DQ, tc::desc_sw128(ds_addr + k * 2048, kAtom, 1024),
+                                tc::desc_sw128(k_addr + k * 2048, kAtom, 1024), IDESC_DQ, k > 0 ? 1u : 0u);
+                }
+                tc::commit(&b.dq_full);
+                tc::commit(&b.q_empty[st]);
+            }
+            tc::commit(&b.mma_drain);
+            drain_wait(&b.mma_drain, 0);
+        }
+    } else {
+        // --------------------------------------------- element-wise work ---
+        const int quarter = warp & 3;
+        const int t = quarter * 32 + lane;  // TMEM lane: key j0 + t (S^T, dP^T, dV, dK) or query i0 + t (dQ)
+        const int j = j0 + t;
+        const bool key_ok = j < a.S;
+        const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+        const float sl2 = a.scale * kLog2e;
+        const int bidx = bh / a.H, hidx = bh - bidx * a.H;
+        const int64_t mbase = (int64_t)bidx * a.msb + (int64_t)hidx * a.msh + j;
+        const int64_t row0 = (int64_t)bh * a.S;
+        bool ok = true;
+        for (int n = 0; n < npair; ++n) {
+            const int i0 = (qb0 + n) * kBN;
+            // this block's lse (log2 units; +inf where the row has no kept key, or beyond S) and delta
+            {
+                const int i = i0 + t;
+                float l2 = __int_as_float(0x7f800000), dl = 0.f;
+                if (i < a.S) {
+                    const float lse = a.lse_in[row0 + i];
+                    l2 = (lse == neg_inf()) ? __int_as_float(0x7f800000) : lse * kLog2e;
+                    dl = a.delta[row0 + i];
+                }
+                s_lse[t] = l2;
+                s_del[t] = dl;
+            }
+            named_sync(1, kBM);
+            const bool pred = !key_ok || (i0 + kBN > a.S) || (a.causal && j0 + kBM - 1 > i0);
+            if (!warp_wait(&b.s_full, (uint32_t)(n & 1), b, a.err)) { ok = false; break; }
+            tc::fence_after_sync();
+#pragma unroll
+            for (int c = 0; c < kBN / 32; ++c) {
+                float m2[32];
+                mask_col<T, MK>(a, mbase, i0 + c * 32, key_ok, m2);
+                uint32_t sv[32], dv[32];
+                tc::tmem_ld32(tl + C::COL_S + c * 32, sv);
+                tc::tmem_ld32(tl + C::COL_DP + c * 32, dv);
+                tc::tmem_wait_ld();
+                uint32_t pk[16], dk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float p[2], ds[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int q = c * 32 + e + u;  // query within the block
+                        float s = fmaf(__uint_as_float(sv[e + u]), sl2, m2[e + u]);
+                        if (pred) {
+                            const int i = i0 + q;
+                            if (!key_ok || i >= a.S || (a.causal && j > i)) s = neg_inf();
+                        }
+                        p[u] = ex2(s - s_lse[q]);
+                        ds[u] = p[u] * (__uint_as_float(dv[e + u]) - s_del[q]) * a.scale;
+                    }
+                    pk[e / 2] = pack2(p[0], p[1], static_cast<T *>(nullptr));
+                    dk[e / 2] = pack2(ds[0], ds[1], static_cast<T *>(nullptr));
+                }
+                unsigned char *pa = smem + C::OFF_P + (c / 2) * kAtom;
+                unsigned char *da = smem + C::OFF_DS + (c / 2) * kAtom;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const uint32_t off = tc::sw128_off((uint32_t)t, (uint32_t)((c & 1) * 4 + q4));
+                    *reinterpret_cast<uint4 *>(pa + off) = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+                    *reinterpret_cast<uint4 *>(da + off) = make_uint4(dk[4 * q4], dk[4 * q4 + 1], dk[4 * q4 + 2], dk[4 * q4 + 3]);
+                }
+            }
+            tc::fence_before_sync();
+            tc::fence_async_smem();
+            mbar_arrive(&b.ds_full);
+            // this block's dQ (lane t = query i0 + t) into the fp32 accumulator
+            if (!warp_wait(&b.dq_full, (uint32_t)(n & 1), b, a.err)) { ok = false; break; }
+            tc::fence_after_sync();
+            const int iq = i0 + t;
+            float *acc = a.dq_acc + (row0 + iq) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                tc::tmem_ld32(tl + C::COL_DQ + c * 32, v);
+                tc::tmem_wait_ld();
+                if (iq < a.S) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        tc::red_add_v4(acc + c * 32 + e, __uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                                       __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+                }
+            }
+            tc::fence_before_sync();
+            mbar_arrive(&b.dq_free);
+        }
+        if (ok) {
+            // dK and dV of this CTA's keys (the last dq_full covered every MMA)
+            tc::fence_after_sync();
+            T *dkr = reinterpret_cast<T *>(a.dk) + (row0 + j) * D;
+            T *dvr = reinterpret_cast<T *>(a.dv) + (row0 + j) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t kv[32], vv[32];
+                tc::tmem_ld32(tl + C::COL_DK + c * 32, kv);
+                tc::tmem_ld32(tl + C::COL_DV + c * 32, vv);
+                tc::tmem_wait_ld();
+                if (key_ok) {
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        float fk[8], fv[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            fk[e] = __uint_as_float(kv[8 * w + e]);
+                            fv[e] = __uint_as_float(vv[8 * w + e]);
+                        }
+                        st_stream(dkr + c * 32 + 8 * w, pack<T>(fk));
+                        st_stream(dvr + c * 32 + 8 * w, pack<T>(fv));
+                    }
+                }
+            }
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// delta[r] = sum_d dO[r, d] * O[r, d] (fp32), and the dQ accumulator row
+// cleared: one warp per query row.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) attn_bwd_pre(const AttnArgs a, int64_t rows)
+{
+    const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r >= rows) return;
+    const T *o = reinterpret_cast<const T *>(a.o_in) + r * D;
+    const T *g = reinterpret_cast<const T *>(a.dout) + r * D;
+    float s = 0.f;
+#pragma unroll
+    for (int e = lane; e < D; e += 32) s = fmaf(to_f32<T>(o[e]), to_f32<T>(g[e]), s);
+    s = group_sum<32>(s);
+    if (lane == 0) a.delta[r] = s;
+    float4 *acc = reinterpret_cast<float4 *>(a.dq_acc + r * D);
+    for (int e = lane; e < D / 4; e += 32) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// dQ = the fp32 accumulator rounded to T, 8 elements per thread.
+template <typename T>
+__global__ void __launch_bounds__(256) attn_bwd_post(const AttnArgs a, int64_t n8)
+{
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n8) return;
+    const float4 *acc = reinterpret_cast<const float4 *>(a.dq_acc) + 2 * i;
+    const float4 u = acc[0], v = acc[1];
+    const float f[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
+    st_stream(reinterpret_cast<T *>(a.dq) + 8 * i, pack<T>(f));
+}
+
+template <typename T, int D, int MK>
+cudaError_t launch_main(const AttnArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                        const CUtensorMap &tdo, cudaStream_t st)
+{
+    auto kern = attn_bwd_kernel<T, D, MK>;
+    constexpr uint32_t smem = BwdCfg<D>::SMEM;
+    static_assert(sizeof(BwdBars) <= BwdCfg<D>::BAR_BYTES, "barrier area");
+    static std::atomic<int> attr_done[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (!attr_done[dev & 63].load(std::memory_order_acquire)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_done[dev & 63].store(1, std::memory_order_release);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(((a.S + kBM - 1) / kBM) * a.B * a.H));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, tdo, a);
+}
+
+template <typename T, int D>
+cudaError_t launch_all(const AttnArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                       const CUtensorMap &tdo, cudaStream_t st)
+{
+    const int64_t rows = (int64_t)a.B * a.H * a.S;
+    attn_bwd_pre<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(a, rows);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (!a.mask) e = launch_main<T, D, 0>(a, tq, tk, tv, tdo, st);
+    else if (a.mask_bool) e = launch_main<T, D, 2>(a, tq, tk, tv, tdo, st);
+    else e = launch_main<T, D, 1>(a, tq, tk, tv, tdo, st);
+    if (e != cudaSuccess) return e;
+    const int64_t n8 = rows * D / 8;
+    attn_bwd_post<T><<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>(a, n8);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd(const AttnArgs &a, cudaStream_t st)
+{
+    CUtensorMap tq, tk, tv, tdo;
+    cudaError_t e;
+    const int BH = a.B * a.H;
+    if ((e = attn_tensor_map(&tq, a.q, a.dtype, BH, a.S, a.D)) != cudaSuccess) return e;
+    if ((e = attn_tensor_map(&tk, a.k, a.dtype, BH, a.S, a.D)) != cudaSuccess) return e;
+    if ((e = attn_tensor_map(&tv, a.v, a.dtype, BH, a.S, a.D)) != cudaSuccess) return e;
+    if ((e = attn_tensor_map(&tdo, a.dout, a.dtype, BH, a.S, a.D)) != cudaSuccess) return e;
+    if (a.dtype == kBF16)
+        return a.D == 128 ? launch_all<__nv_bfloat16, 128>(a, tq, tk, tv, tdo, st)
+                          : launch_all<__nv_bfloat16, 64>(a, tq, tk, tv, tdo, st);
+    return a.D == 128 ? launch_all<__half, 128>(a, tq, tk, tv, tdo, st) : launch_all<__half, 64>(a, tq, tk, tv, tdo, st);
+}
+
+}  // namespace sms

@@ -58,13 +58,14 @@ __device__ __forceinline__ void commit(uint64_t *bar)
 }
 
 // Instruction descriptor of kind::f16: fp32 accumulator, A and B of format
-// `ab` (0 = fp16, 1 = bf16), A K-major, B K-major (b_mn = 0) or MN-major
-// (b_mn = 1), M x N.
-__host__ __device__ constexpr uint32_t idesc_f16(int ab, int b_mn, int M, int N)
+// `ab` (0 = fp16, 1 = bf16), each K-major (0) or MN-major (1: b_mn for B,
+// a_mn for A), M x N.
+__host__ __device__ constexpr uint32_t idesc_f16(int ab, int b_mn, int M, int N, int a_mn = 0)
 {
     return (1u << 4)                       // D format: fp32
            | ((uint32_t)ab << 7)           // A format
            | ((uint32_t)ab << 10)          // B format
+           | ((uint32_t)a_mn << 15)        // A major-ness
            | ((uint32_t)b_mn << 16)        // B major-ness
            | ((uint32_t)(N >> 3) << 17)    // N / 8
            | ((uint32_t)(M >> 4) << 24);   // M / 16
@@ -130,6 +131,13 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int x, 
 __device__ __forceinline__ void prefetch_tmap(const void *tmap)
 {
     asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
+// Four fp32 values added to global memory (one vector reduction; addr 16-byte aligned).
+__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d)
+{
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" :: "l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
 }
 
 // Shared-memory writes by ordinary stores become visible to the tensor-core

@@ -294,3 +294,33 @@ def test_attention_empty_problem_is_a_no_op():
     for kw in (dict(B=0), dict(H=0), dict(S=0)):
         assert _attn(q=None, k=None, v=None, o=None, **kw) in (INVALID, binding.SMS_OK)
     assert _attn(B=0) == binding.SMS_OK
+
+
+def _attn_bwd(**kw):
+    a = dict(q=0x100000, k=0x200000, v=0x300000, o=0x400000, do=0x500000, lse=0x600000, mask=None, mask_numel=0,
+             sb=0, sh=0, mbool=0, dq=0x700000, dk=0x800000, dv=0x900000, ws=0xA00000, wsb=1 << 20, B=1, H=2, S=16,
+             D=64, scale=0.125, causal=0, dtype=binding.SMS_BF16, stream=None)
+    a.update(kw)
+    return binding.lib().sms_attention_backward(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["mask"],
+                                                a["mask_numel"], a["sb"], a["sh"], a["mbool"], a["dq"], a["dk"],
+                                                a["dv"], a["ws"], a["wsb"], a["B"], a["H"], a["S"], a["D"],
+                                                a["scale"], a["causal"], a["dtype"], a["stream"])
+
+
+def test_attention_backward_workspace_size():
+    # an fp32 dQ accumulator plus one fp32 per query row
+    assert binding.lib().sms_attention_backward_workspace(2, 3, 5, 64) == 2 * 3 * 5 * 64 * 4 + 2 * 3 * 5 * 4
+    assert binding.lib().sms_attention_backward_workspace(-1, 3, 5, 64) == -1
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dtype=binding.SMS_F32), UNSUPPORTED), (dict(D=32), UNSUPPORTED), (dict(lse=None), INVALID),
+    (dict(do=None), INVALID), (dict(dk=None), INVALID), (dict(ws=None), INVALID),
+    (dict(wsb=2 * 16 * 64 * 4), INVALID),  # one query row's delta short
+    (dict(ws=0xA00008), INVALID), (dict(dq=0x100000), INVALID), (dict(dv=0x800000), INVALID),
+    (dict(ws=0x700000), INVALID),  # workspace on top of dq
+    (dict(lse=0x600002), INVALID), (dict(mask=0xB00000, mask_numel=255), INVALID),
+])
+def test_attention_backward_rejects_bad_arguments(kw, status):
+    assert _attn_bwd(**kw) == status
+    assert binding.lib().sms_last_error().decode().startswith("sms_attention_backward")

@@ -203,3 +203,21 @@ def test_lse_closed_forms():
     _, lse_m = A.attention_forward(q, k, v, 1.0, False, mask, return_lse=True)
     assert np.all(np.isneginf(lse_m[:, :, 2]))
     assert np.allclose(np.delete(lse_m, 2, axis=2), math.log(S), rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_additive_mask_of_the_storage_dtype(dtype):
+    """An additive mask stored in q's 16-bit dtype (the layout the kernels
+    take) is widened exactly: the result equals torch SDPA with that mask
+    converted to fp64 by torch."""
+    B, H, S = 2, 2, 9
+    q, k, v = _qkv(B, H, S, 8, 3, 31, dtype)
+    g = torch.Generator().manual_seed(32)
+    mask = (torch.randn(B, 1, S, S, generator=g) * 3).to(dtype)
+    mask[0, 0, 3, 5] = -math.inf
+    O, lse = A.attention_forward(q, k, v, 0.4, False, mask, S * S, 0, return_lse=True)
+    full = mask.double().expand(B, H, S, S)
+    ref = F.scaled_dot_product_attention(q.double(), k.double(), v.double(), attn_mask=full, scale=0.4)
+    assert np.abs(O - ref.numpy()).max() < 1e-13
+    s = torch.matmul(q.double(), k.double().transpose(-1, -2)) * 0.4 + full
+    assert np.abs(lse - torch.logsumexp(s, -1).numpy()).max() < 1e-12
