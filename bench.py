@@ -573,6 +573,115 @@ def run_e2e(args, w, inp, device, steps):
                     "every step; copy-in, kernels and copy-out of successive blocks overlap on three streams"}
 
 
+# ------------------------------------------------------ fused attention ---
+
+ATTN_METRIC = "fused attention (QK^T, scaled masked softmax, PV) fwd/bwd achieved TFLOP/s and % of measured bf16 peak"
+
+
+def attn_flops(B, H, S, D, causal):
+    """Algorithmic FLOPs of one forward and one backward: 2 S S D per product
+    per head (2 products forward, 5 backward); under causal only the
+    S (S + 1) / 2 kept (query, key) pairs count."""
+    pairs = S * (S + 1) / 2 if causal else S * S
+    per = 2.0 * pairs * D * B * H
+    return 2 * per, 5 * per
+
+
+def _tc_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured (cuBLAS bf16 burst)"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def run_attention(args, device):
+    """The fused attention step on the tensor cores: forward (O, lse) and
+    backward (dQ, dK, dV) through the C ABI on resident inputs."""
+    import scaled_masked_softmax_gb300 as sms
+    from scaled_masked_softmax_gb300 import workloads
+
+    B, H, S, D = (int(v) for v in args.attn_shape.split(","))
+    causal = not args.attn_no_causal
+    dt = torch.bfloat16
+    q, k, v, d_o = workloads.attention_inputs(B, H, S, D, "bf16", seed=41, device=device, with_do=True)
+    mask, sb = None, 0
+    if args.attn_mask:  # the [B,1,S,S] key padding of the bf16 S=4096 softmax workload, as bytes
+        g = torch.Generator().manual_seed(42)
+        L = torch.randint((S + 3) // 4, S + 1, (B,), generator=g)
+        mask = (torch.arange(S)[None, :] >= L[:, None])[:, None, None, :].expand(B, 1, S, S).contiguous().to(device)
+        sb = S * S
+    L = sms.binding.lib()
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, S, dtype=torch.float32, device=device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    nws = sms.sms_attention_backward_workspace(B, H, S, D)
+    ws = torch.empty(nws, dtype=torch.uint8, device=device)
+    st = torch.cuda.current_stream(device).cuda_stream
+    mptr = None if mask is None else mask.data_ptr()
+    mnum = 0 if mask is None else mask.numel()
+    scale = float(np.float32(1.0 / math.sqrt(D)))
+    code = sms.SMS_BF16
+
+    def fwd():
+        rc = L.sms_attention_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), mptr, mnum, sb, 0, 1, o.data_ptr(),
+                                     lse.data_ptr(), B, H, S, D, scale, int(causal), code, st)
+        if rc:
+            raise RuntimeError(sms.sms_last_error())
+
+    def bwd():
+        rc = L.sms_attention_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), d_o.data_ptr(),
+                                      lse.data_ptr(), mptr, mnum, sb, 0, 1, dq.data_ptr(), dk.data_ptr(),
+                                      dv.data_ptr(), ws.data_ptr(), nws, B, H, S, D, scale, int(causal), code, st)
+        if rc:
+            raise RuntimeError(sms.sms_last_error())
+
+    for _ in range(max(args.warmup, 3)):
+        fwd()
+        bwd()
+    torch.cuda.synchronize(device)
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = ClockSampler(device)
+    clocks.start()
+    n0 = sms.sms_launch_count()
+    for i in range(K):
+        ev[i][0].record()
+        fwd()
+        ev[i][1].record()
+        bwd()
+        ev[i][2].record()
+    torch.cuda.synchronize(device)
+    n_launch = sms.sms_launch_count() - n0
+    clk = clocks.stop()
+    f_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
+    b_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(K))
+    ff, bf = attn_flops(B, H, S, D, causal)
+    peak, peak_kind = _tc_peak()
+    tf = (ff + bf) / ((f_ms + b_ms) * 1e9)
+    kern = {"forward": {"ms": round(f_ms, 4), "tflops": round(ff / (f_ms * 1e9), 1),
+                        "frac_of_peak": round(ff / (f_ms * 1e9) / peak, 4)},
+            "backward": {"ms": round(b_ms, 4), "tflops": round(bf / (b_ms * 1e9), 1),
+                         "frac_of_peak": round(bf / (b_ms * 1e9) / peak, 4), "kernels": 3}}
+    dom = "backward" if b_ms >= f_ms else "forward"
+    res = {"metric": ATTN_METRIC, "value": round(tf, 1), "unit": "TFLOP/s", "n_gpus": 1, "steps": K,
+           "warmup": args.warmup, "ms_per_step": round(f_ms + b_ms, 4), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, workloads.attention_inputs)",
+           "config": {"workload": f"attention_bf16_b{B}_h{H}_s{S}_d{D}" + ("_causal" if causal else "")
+                      + ("_keypad" if mask is not None else ""),
+                      "shape": [B, H, S, D], "is_causal": causal, "scale": scale,
+                      "mask": "[B,1,S,S] key padding as bytes" if mask is not None else "none",
+                      "step": "forward (O, lse) + backward (dQ, dK, dV)", "l2": "inputs larger than L2"
+                      if 5 * q.numel() * 2 > L2_BYTES else "inputs fit in L2 (small shape)"},
+           "kernels": kern,
+           "roofline": {"kernel": dom, "bound": "tensor", "achieved": kern[dom]["tflops"], "peak": peak,
+                        "unit": "TFLOP/s", "frac": kern[dom]["frac_of_peak"], "traffic": None,
+                        "peak_source": peak_kind},
+           "gpu_launches": int(n_launch), "clocks": clk}
+    return res
+
 # ------------------------------------------------------- oracle on the CPU ---
 
 def _oracle_sample(w, inp_cpu, n_rows, start):
@@ -738,6 +847,11 @@ def main():
                     help="the workload's distributions at batch B and H heads (small profiling captures)")
     ap.add_argument("--bool-mask", action="store_true",
                     help="masked workloads with the mask as one byte per element (sms_forward_bool)")
+    ap.add_argument("--attention", action="store_true",
+                    help="bench the fused attention step (tensor cores) instead of the softmax")
+    ap.add_argument("--attn-shape", default="4,32,4096,128", metavar="B,H,S,D")
+    ap.add_argument("--attn-no-causal", action="store_true")
+    ap.add_argument("--attn-mask", action="store_true", help="with --attention: a [B,1,S,S] key-padding byte mask")
     args = ap.parse_args()
 
     world, rank, local = dist_env()
@@ -760,6 +874,10 @@ def main():
     __graft_entry__.build()
     import scaled_masked_softmax_gb300 as sms
 
+    if args.attention:
+        res = run_attention(args, device)
+        print(json.dumps(res), flush=True)
+        return
     path_code = {"auto": 0, "warp": 1, "cta": 2, "online": 3, "stream": 4, "ring": 5}
     sms.sms_set_forced_path(path_code[args.path])
     res, (w, inp, _y, _dx) = run_ours(args, rank, world, device)

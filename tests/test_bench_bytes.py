@@ -91,3 +91,12 @@ def test_e2e_blocks_keep_the_row_rule(kind, B, Hh, S, rows, n_target):
                 assert moff + b2 * msb + h2 * msh + q2 * S == b * msb + h * msh + q * S
     assert seen == list(range(w.rows))
     assert len(blocks) <= max(1, n_target) or len(blocks) == -(-w.rows // (S * (H if kind in ("B1SS", "BHSS") else 1)))
+
+
+def test_attention_flops_count_kept_pairs():
+    # 2 S S D per product per head; causal keeps S (S + 1) / 2 pairs
+    f, b = bench.attn_flops(2, 3, 8, 64, False)
+    assert f == 2 * (2 * 8 * 8 * 64 * 6) and b == 5 * (2 * 8 * 8 * 64 * 6)
+    fc, bc = bench.attn_flops(1, 1, 4, 16, True)
+    pairs = sum(q + 1 for q in range(4))
+    assert fc == 2 * 2 * pairs * 16 and bc == 5 * 2 * pairs * 16
