@@ -41,9 +41,11 @@
  *
  * Graphs.  Every launch goes on `stream`, so calls can be captured into a CUDA
  * graph (the second article's §1.1 and §4.4 on launch overhead).  Make one
- * eager call per shape and kernel family before capturing: it does that
- * kernel's one-time set-up (function attributes, occupancy query, the device
- * error word's address), which must not happen during a capture.
+ * eager call per shape and kernel family before capturing, from the host
+ * thread that captures: it does that kernel's one-time set-up (the shared-
+ * memory limit of the kernel, once per device and host thread; the occupancy
+ * query and the device error word's address, once per device), which must
+ * not happen during a capture.
  *
  * Alignment.  x, y, mask, dy and dx must be 16-byte aligned (every CUDA / PyTorch
  * allocation is); rows may start at any element.

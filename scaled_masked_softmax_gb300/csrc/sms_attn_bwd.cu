@@ -153,7 +153,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int BH = a.B * a.H;
     const int nkb = (a.S + kBM - 1) / kBM;
-    const int kb = nkb - 1 - (int)(blockIdx.x / (unsigned)BH);
+    // causal: key block 0 sees every query block, the last one only its own; heaviest first
+    const int kb = a.causal ? (int)(blockIdx.x / (unsigned)BH) : nkb - 1 - (int)(blockIdx.x / (unsigned)BH);
     const int bh = (int)(blockIdx.x % (unsigned)BH);
     const int j0 = kb * kBM;
     const int nqb = (a.S + kBN - 1) / kBN;
@@ -422,14 +423,14 @@ cudaError_t launch_main(const AttnArgs &a, const CUtensorMap &tq, const CUtensor
     auto kern = attn_bwd_kernel<T, D, MK>;
     constexpr uint32_t smem = BwdCfg<D>::SMEM;
     static_assert(sizeof(BwdBars) <= BwdCfg<D>::BAR_BYTES, "barrier area");
-    static std::atomic<int> attr_done[64];
+    static thread_local bool attr_done[64];  // per device and host thread: the shared-memory limit has been raised
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (!attr_done[dev & 63].load(std::memory_order_acquire)) {
+    if (!attr_done[dev & 63]) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        attr_done[dev & 63].store(1, std::memory_order_release);
+        attr_done[dev & 63] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(((a.S + kBM - 1) / kBM) * a.B * a.H));

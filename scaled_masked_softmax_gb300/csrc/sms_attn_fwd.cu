@@ -265,10 +265,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 tc::commit(&b.kv_empty[st]);
                 return true;
             };
-            for (int j = 0; ok && j < nkv; ++j) {
+            // S_j = Q K_j^T into score buffer j % 2, once that buffer's block j - 2 has been read
+            auto qk = [&](int j) -> bool {
                 const int st = j % NST, sb = j & 1;
-                if (!wait_or_flag(&b.k_full[st], (uint32_t)((j / NST) & 1), b, a.err)) { ok = false; break; }
-                if (j >= 2 && !wait_or_flag(&b.s_free[sb], (uint32_t)(((j - 2) / 2) & 1), b, a.err)) { ok = false; break; }
+                if (!wait_or_flag(&b.k_full[st], (uint32_t)((j / NST) & 1), b, a.err)) return false;
+                if (j >= 2 && !wait_or_flag(&b.s_free[sb], (uint32_t)(((j - 2) / 2) & 1), b, a.err)) return false;
                 tc::fence_after_sync();
                 const uint32_t k_addr = s_base + C::OFF_K + st * C::TILE;
 #pragma unroll
@@ -278,9 +279,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                     tc::mma_f16(tmem + sb * kBN, da, db, IDESC_QK, k > 0 ? 1u : 0u);
                 }
                 tc::commit(&b.s_full[sb]);
-                if (j >= 1 && !pv(j - 1)) { ok = false; break; }
+                return true;
+            };
+            // the scores run one block ahead of P V: S_{j+1} is on the tensor
+            // cores while the softmax of block j works
+            if (ok) ok = qk(0);
+            for (int j = 0; ok && j < nkv; ++j) {
+                if (j + 1 < nkv && !qk(j + 1)) { ok = false; break; }
+                if (!pv(j)) { ok = false; break; }
             }
-            if (ok) pv(nkv - 1);
             // leave no MMA in flight
             tc::commit(&b.mma_drain);
             drain_wait(&b.mma_drain, 0);
@@ -469,14 +476,14 @@ cudaError_t launch_fwd(const AttnArgs &a, const CUtensorMap &tq, const CUtensorM
     auto kern = attn_fwd_kernel<T, D, MK>;
     constexpr uint32_t smem = FwdCfg<D>::SMEM;
     static_assert(sizeof(FwdBars) <= FwdCfg<D>::BAR_BYTES, "barrier area");
-    static std::atomic<int> attr_done[64];
+    static thread_local bool attr_done[64];  // per device and host thread: the shared-memory limit has been raised
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (!attr_done[dev & 63].load(std::memory_order_acquire)) {
+    if (!attr_done[dev & 63]) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        attr_done[dev & 63].store(1, std::memory_order_release);
+        attr_done[dev & 63] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(((a.S + kBM - 1) / kBM) * a.B * a.H));

@@ -464,14 +464,14 @@ cudaError_t launch_tile(const FwdArgs &fa, const BwdArgs &ba, cudaStream_t st)
 {
     constexpr int smem = smem_bytes<WG, R, SLOTS, CH>();
     auto kern = tile_kernel<T, WG, R, SLOTS, CH, BWD>;
-    static std::atomic<int> attr_done[64];  // per device: the shared-memory limit has been raised
+    static thread_local bool attr_done[64];  // per device and host thread: the shared-memory limit has been raised
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (!attr_done[dev & 63].load(std::memory_order_acquire)) {  // idempotent: a race only repeats the call
+    if (!attr_done[dev & 63]) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        attr_done[dev & 63].store(1, std::memory_order_release);
+        attr_done[dev & 63] = true;
     }
     const int64_t rows = BWD ? ba.rows : fa.rows;
     const int64_t grid = persistent_grid(1, rows);
