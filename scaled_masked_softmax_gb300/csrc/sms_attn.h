@@ -37,7 +37,8 @@ struct AttnArgs {
 // Head dimensions the tensor-core kernels take.
 inline bool attn_head_dim_ok(int d) { return d == 64 || d == 128; }
 
-cudaError_t launch_attn_fwd(const AttnArgs &a, cudaStream_t st);
-cudaError_t launch_attn_bwd(const AttnArgs &a, cudaStream_t st);
+// `step` (optional) names the step that failed: a tensor map or a kernel launch.
+cudaError_t launch_attn_fwd(const AttnArgs &a, cudaStream_t st, const char **step = nullptr);
+cudaError_t launch_attn_bwd(const AttnArgs &a, cudaStream_t st, const char **step = nullptr);
 
 }  // namespace sms

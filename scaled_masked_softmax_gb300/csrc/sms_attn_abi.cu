@@ -60,7 +60,7 @@ int check_common(const char *who, const void *q, const void *k, const void *v, c
     return SMS_OK;
 }
 
-int launch_result(cudaError_t e, const char *who)
+int launch_result(cudaError_t e, const char *who, const char *step)
 {
     if (e == cudaSuccess) {
         count_launch();
@@ -68,7 +68,8 @@ int launch_result(cudaError_t e, const char *who)
     }
     cudaGetLastError();
     char buf[200];
-    snprintf(buf, sizeof(buf), "launch failed: %s", cudaGetErrorString(e));
+    snprintf(buf, sizeof(buf), "%s failed: %s (%s)", step ? step : "launch", cudaGetErrorString(e),
+             cudaGetErrorName(e));
     return fail(e == cudaErrorNotSupported ? SMS_ERR_UNSUPPORTED : SMS_ERR_CUDA, who, buf);
 }
 
@@ -113,7 +114,9 @@ int sms_attention_forward(const void *q, const void *k, const void *v, const voi
     a.B = (int)batch; a.H = (int)heads; a.S = (int)seq; a.D = (int)head_dim;
     a.scale = scale; a.causal = is_causal ? 1 : 0; a.dtype = dtype; a.err = err;
     a.o = o; a.lse = lse;
-    return launch_result(launch_attn_fwd(a, static_cast<cudaStream_t>(stream)), who);
+    const char *step = nullptr;
+    const cudaError_t e2 = launch_attn_fwd(a, static_cast<cudaStream_t>(stream), &step);
+    return launch_result(e2, who, step);
 }
 
 int64_t sms_attention_backward_workspace(int64_t batch, int64_t heads, int64_t seq, int64_t head_dim)
@@ -175,12 +178,13 @@ int sms_attention_backward(const void *q, const void *k, const void *v, const vo
     a.dq = dq; a.dk = dk; a.dv = dv;
     a.dq_acc = static_cast<float *>(workspace);
     a.delta = reinterpret_cast<float *>(static_cast<char *>(workspace) + batch * heads * seq * head_dim * 4);
-    e = launch_attn_bwd(a, static_cast<cudaStream_t>(stream));
+    const char *step = nullptr;
+    e = launch_attn_bwd(a, static_cast<cudaStream_t>(stream), &step);
     if (e == cudaSuccess) {  // three kernels: delta, the main pass, dQ
         count_launch();
         count_launch();
     }
-    return launch_result(e, who);
+    return launch_result(e, who, step);
 }
 
 }  // extern "C"

@@ -442,16 +442,19 @@ cudaError_t launch_main(const AttnArgs &a, const CUtensorMap &tq, const CUtensor
 
 template <typename T, int D>
 cudaError_t launch_all(const AttnArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                       const CUtensorMap &tdo, cudaStream_t st)
+                       const CUtensorMap &tdo, cudaStream_t st, const char **step)
 {
     const int64_t rows = (int64_t)a.B * a.H * a.S;
+    *step = "delta kernel";
     attn_bwd_pre<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(a, rows);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    *step = "main backward kernel";
     if (!a.mask) e = launch_main<T, D, 0>(a, tq, tk, tv, tdo, st);
     else if (a.mask_bool) e = launch_main<T, D, 2>(a, tq, tk, tv, tdo, st);
     else e = launch_main<T, D, 1>(a, tq, tk, tv, tdo, st);
     if (e != cudaSuccess) return e;
+    *step = "dQ kernel";
     const int64_t n8 = rows * D / 8;
     attn_bwd_post<T><<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>(a, n8);
     return cudaGetLastError();
@@ -459,19 +462,26 @@ cudaError_t launch_all(const AttnArgs &a, const CUtensorMap &tq, const CUtensorM
 
 }  // namespace
 
-cudaError_t launch_attn_bwd(const AttnArgs &a, cudaStream_t st)
+cudaError_t launch_attn_bwd(const AttnArgs &a, cudaStream_t st, const char **step)
 {
+    const char *dummy = nullptr;
+    if (!step) step = &dummy;
     CUtensorMap tq, tk, tv, tdo;
     cudaError_t e;
     const int BH = a.B * a.H;
+    *step = "tensor map of q";
     if ((e = attn_tensor_map(&tq, a.q, a.dtype, BH, a.S, a.D)) != cudaSuccess) return e;
+    *step = "tensor map of k";
     if ((e = attn_tensor_map(&tk, a.k, a.dtype, BH, a.S, a.D)) != cudaSuccess) return e;
+    *step = "tensor map of v";
     if ((e = attn_tensor_map(&tv, a.v, a.dtype, BH, a.S, a.D)) != cudaSuccess) return e;
+    *step = "tensor map of d_o";
     if ((e = attn_tensor_map(&tdo, a.dout, a.dtype, BH, a.S, a.D)) != cudaSuccess) return e;
     if (a.dtype == kBF16)
-        return a.D == 128 ? launch_all<__nv_bfloat16, 128>(a, tq, tk, tv, tdo, st)
-                          : launch_all<__nv_bfloat16, 64>(a, tq, tk, tv, tdo, st);
-    return a.D == 128 ? launch_all<__half, 128>(a, tq, tk, tv, tdo, st) : launch_all<__half, 64>(a, tq, tk, tv, tdo, st);
+        return a.D == 128 ? launch_all<__nv_bfloat16, 128>(a, tq, tk, tv, tdo, st, step)
+                          : launch_all<__nv_bfloat16, 64>(a, tq, tk, tv, tdo, st, step);
+    return a.D == 128 ? launch_all<__half, 128>(a, tq, tk, tv, tdo, st, step)
+                      : launch_all<__half, 64>(a, tq, tk, tv, tdo, st, step);
 }
 
 }  // namespace sms

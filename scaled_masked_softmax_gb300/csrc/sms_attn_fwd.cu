@@ -504,14 +504,20 @@ cudaError_t launch_fwd_mk(const AttnArgs &a, const CUtensorMap &tq, const CUtens
 
 }  // namespace
 
-cudaError_t launch_attn_fwd(const AttnArgs &a, cudaStream_t st)
+cudaError_t launch_attn_fwd(const AttnArgs &a, cudaStream_t st, const char **step)
 {
+    const char *dummy = nullptr;
+    if (!step) step = &dummy;
     CUtensorMap tq, tk, tv;
     cudaError_t e;
     const int BH = a.B * a.H;
+    *step = "tensor map of q";
     if ((e = attn_tensor_map(&tq, a.q, a.dtype, BH, a.S, a.D)) != cudaSuccess) return e;
+    *step = "tensor map of k";
     if ((e = attn_tensor_map(&tk, a.k, a.dtype, BH, a.S, a.D)) != cudaSuccess) return e;
+    *step = "tensor map of v";
     if ((e = attn_tensor_map(&tv, a.v, a.dtype, BH, a.S, a.D)) != cudaSuccess) return e;
+    *step = "forward kernel";
     if (a.dtype == kBF16) {
         return a.D == 128 ? launch_fwd_mk<__nv_bfloat16, 128>(a, tq, tk, tv, st)
                           : launch_fwd_mk<__nv_bfloat16, 64>(a, tq, tk, tv, st);
