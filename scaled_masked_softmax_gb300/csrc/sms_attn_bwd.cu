@@ -466,7 +466,7 @@ cudaError_t launch_attn_bwd(const AttnArgs &a, cudaStream_t st, const char **ste
 {
     const char *dummy = nullptr;
     if (!step) step = &dummy;
-    CUtensorMap tq, tk, tv, tdo;
+    alignas(64) CUtensorMap tq, tk, tv, tdo;  // the encoder needs 64-byte aligned maps
     cudaError_t e;
     const int BH = a.B * a.H;
     *step = "tensor map of q";

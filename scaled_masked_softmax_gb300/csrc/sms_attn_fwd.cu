@@ -450,12 +450,30 @@ EncodeFn encode_fn()
 
 }  // namespace
 
+// The tensor-map encoder is a driver call: it needs the device's context
+// current in the calling thread, which the runtime only makes current on a
+// thread's first call that needs it (a host thread that has launched nothing
+// yet, such as an autograd worker, has none).  cudaSetDevice makes it current.
+cudaError_t context_current()
+{
+    static thread_local int done = -1;  // the device this thread made current
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (done == dev) return cudaSuccess;
+    e = cudaSetDevice(dev);
+    if (e == cudaSuccess) done = dev;
+    return e;
+}
+
 // [B*H, S, D] 16-bit tensor, boxes of 64 x 128 x 1, 128-byte swizzle; rows
 // beyond S of a head read as zeros.
 cudaError_t attn_tensor_map(CUtensorMap *m, const void *base, int dtype, int BH, int S, int D)
 {
     EncodeFn fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
+    const cudaError_t ce = context_current();
+    if (ce != cudaSuccess) return ce;
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)BH};
     const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2};
     const cuuint32_t box[3] = {64, 128, 1};
@@ -508,7 +526,7 @@ cudaError_t launch_attn_fwd(const AttnArgs &a, cudaStream_t st, const char **ste
 {
     const char *dummy = nullptr;
     if (!step) step = &dummy;
-    CUtensorMap tq, tk, tv;
+    alignas(64) CUtensorMap tq, tk, tv;  // the encoder needs 64-byte aligned maps
     cudaError_t e;
     const int BH = a.B * a.H;
     *step = "tensor map of q";
