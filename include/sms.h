@@ -264,6 +264,37 @@ SMS_API int sms_attention_backward(const void *q, const void *k, const void *v, 
 /* Bytes of workspace sms_attention_backward needs (-1 for a negative size). */
 SMS_API int64_t sms_attention_backward_workspace(int64_t batch, int64_t heads, int64_t seq, int64_t head_dim);
 
+/*
+ * sms_attention_backward for callers that cannot allocate device memory: a
+ * process whose memory is owned by a framework or pool it cannot call into,
+ * code that runs where an allocation could block or fail at the wrong time
+ * (inside a captured region, an interrupt-like callback, a real-time loop), or
+ * a plain C caller with no allocator at hand.  The source pages have no
+ * counterpart: this is an addition of the library.
+ * Same arguments, kernels and results as sms_attention_backward, without the
+ * workspace: the scratch (the fp32 dQ accumulator and one fp32 per query row,
+ * sms_attention_backward_workspace() bytes) lives in one array of
+ * SMS_ATTN_STATIC_SCRATCH_BYTES inside the library's device image, which
+ * every GPU that loads the library holds until the process exits.
+ *   - A problem needing more scratch than that is refused with
+ *     SMS_ERR_INVALID_ARG before anything is launched (use the workspace entry
+ *     point for it).
+ *   - No call allocates: not the library, not the CUDA runtime on its behalf.
+ *   - The first call on a device looks up the array's device address there
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture on that device.
+ *   - Every call uses the same array and leaves its contents behind; the
+ *     kernels clear the accumulator themselves before use.  Calls whose
+ *     kernels overlap on the GPU (other streams, other host threads) race on
+ *     the array: order them on one stream.
+ */
+#define SMS_ATTN_STATIC_SCRATCH_BYTES (32ll << 20)
+SMS_API int sms_attention_backward_static(const void *q, const void *k, const void *v, const void *o,
+                                          const void *d_o, const float *lse, const void *mask, int64_t mask_numel,
+                                          int64_t mask_stride_b, int64_t mask_stride_h, int mask_is_bool, void *dq,
+                                          void *dk, void *dv, int64_t batch, int64_t heads, int64_t seq,
+                                          int64_t head_dim, float scale, int is_causal, int dtype, void *stream);
+
 /* Static description of a status code. */
 SMS_API const char *sms_status_string(int status);
 

@@ -14,6 +14,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libsms.so")
 
 SMS_F32, SMS_F16, SMS_BF16 = 0, 1, 2
+SMS_ATTN_STATIC_SCRATCH_BYTES = 32 << 20  # include/sms.h: the static scratch of sms_attention_backward_static
 SMS_OK, SMS_ERR_INVALID_ARG, SMS_ERR_UNSUPPORTED, SMS_ERR_CUDA = 0, 1, 2, 3
 SMS_PATH_AUTO, SMS_PATH_WARP, SMS_PATH_CTA, SMS_PATH_ONLINE, SMS_PATH_STREAM, SMS_PATH_RING = 0, 1, 2, 3, 4, 5
 PATH_NAMES = {SMS_PATH_AUTO: "auto", SMS_PATH_WARP: "warp", SMS_PATH_CTA: "cta", SMS_PATH_ONLINE: "online",
@@ -32,6 +33,8 @@ SIGNATURES = {
     "sms_attention_backward": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _vp, _vp,
                                       _i64, _i64, _i64, _i64, _i64, _f32, _i32, _i32, _vp]),
     "sms_attention_backward_workspace": (_i64, [_i64, _i64, _i64, _i64]),
+    "sms_attention_backward_static": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _vp,
+                                             _i64, _i64, _i64, _i64, _f32, _i32, _i32, _vp]),
     "sms_status_string": (_cp, [_i32]),
     "sms_last_error": (_cp, []),
     "sms_set_forced_path": (_i32, [_i32]),

@@ -20,7 +20,8 @@ LIB = os.path.join(PKG, "libsms.so")
 
 SOURCES = ["sms_abi.cu", "sms_warp.cu", "sms_warp_bool.cu", "sms_stream.cu", "sms_ring.cu", "sms_ring_fwd_f32.cu",
            "sms_ring_fwd_f16.cu", "sms_ring_fwd_bf16.cu", "sms_ring_bwd.cu", "sms_tile_fwd.cu", "sms_tile_bwd.cu",
-           "sms_online.cu", "sms_attn_abi.cu", "sms_attn_fwd.cu", "sms_attn_bwd.cu"]
+           "sms_online.cu", "sms_attn_abi.cu", "sms_attn_fwd.cu", "sms_attn_bwd.cu",
+           "sms_attn_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr", "-I", INCLUDE]
