@@ -38,32 +38,33 @@
 namespace sms {
 namespace {
 
-constexpr int kBM = 128;          // query rows per CTA (the MMA's M)
+constexpr int kBM = 128;          // query rows per tile (the MMA's M); a CTA owns two tiles
 constexpr int kBN = 128;          // keys per block
-constexpr int kThreads = 192;     // warps 0 (TMA), 1 (MMA), 2..5 (softmax)
+constexpr int kThreads = 320;     // warps 0 (TMA), 1 (MMA), 2..5 (softmax, tile 0), 6..9 (softmax, tile 1)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAtom = 16384;  // 128 rows x 128 bytes
 
 template <int D> struct FwdCfg {
-    static constexpr int NST = D == 128 ? 2 : 3;  // K/V stages
-    static constexpr int NP = D == 128 ? 1 : 2;   // P buffers
+    static constexpr int NK = D == 128 ? 2 : 3;        // K slots
+    static constexpr int NV = D == 128 ? 1 : 3;        // V slots
     static constexpr uint32_t TILE = (D / 64) * kAtom;  // one 128 x D tile (Q, K or V)
     static constexpr uint32_t PBUF = (kBN / 64) * kAtom;
-    static constexpr uint32_t OFF_Q = 0;
-    static constexpr uint32_t OFF_K = OFF_Q + TILE;
-    static constexpr uint32_t OFF_V = OFF_K + NST * TILE;
-    static constexpr uint32_t OFF_P = OFF_V + NST * TILE;
-    static constexpr uint32_t OFF_BAR = OFF_P + NP * PBUF;
+    static constexpr uint32_t OFF_Q = 0;                // two Q tiles
+    static constexpr uint32_t OFF_K = OFF_Q + 2 * TILE;
+    static constexpr uint32_t OFF_V = OFF_K + NK * TILE;
+    static constexpr uint32_t OFF_P = OFF_V + NV * TILE;  // one P buffer per tile
+    static constexpr uint32_t OFF_BAR = OFF_P + 2 * PBUF;
     static constexpr uint32_t BAR_BYTES = 512;
     static constexpr uint32_t SMEM = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
-    static constexpr uint32_t COL_O = 2 * kBN;  // TMEM columns: S0, S1, O
+    // TMEM columns of tile t: scores at t*256, output accumulator at t*256 + 128
+    static constexpr uint32_t COL_S = 0, COL_O = kBN, TILE_COLS = 256;
 };
 
 struct FwdBars {
     uint64_t q_full;
-    uint64_t k_full[3], v_full[3], kv_empty[3];
-    uint64_t s_full[2], s_free[2];
-    uint64_t p_full[2], pv_done[2];
+    uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];
+    uint64_t s_full[2], s_free[2];   // per tile
+    uint64_t p_full[2], pv_done[2];  // per tile
     uint64_t mma_drain;
     uint32_t tmem_base;
     int abort;
@@ -72,6 +73,13 @@ struct FwdBars {
 template <typename T> struct AbFmt;
 template <> struct AbFmt<__half> { static constexpr int v = 0; };
 template <> struct AbFmt<__nv_bfloat16> { static constexpr int v = 1; };
+
+__device__ __forceinline__ float rowmath_max3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
 
 // Bounded wait on phase `parity`; on failure the CTA is flagged and the
 // device word gets the code.
@@ -167,7 +175,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 const __grid_constant__ CUtensorMap tmv, const AttnArgs a)
 {
     using C = FwdCfg<D>;
-    constexpr int NST = C::NST, NP = C::NP;
+    constexpr int NK = C::NK, NV = C::NV;
     constexpr uint32_t IDESC_QK = tc::idesc_f16(AbFmt<T>::v, 0, kBM, kBN);
     constexpr uint32_t IDESC_PV = tc::idesc_f16(AbFmt<T>::v, 1, kBM, D);
 
@@ -179,20 +187,25 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
     const uint32_t s_base = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nq = (a.S + kBM - 1) / kBM;
     const int BH = a.B * a.H;
-    const int qb = nq - 1 - (int)(blockIdx.x / (unsigned)BH);  // heaviest causal tiles first, every head
+    const int npair = (a.S + 2 * kBM - 1) / (2 * kBM);
+    const int pr = npair - 1 - (int)(blockIdx.x / (unsigned)BH);  // heaviest causal pairs first, every head
     const int bh = (int)(blockIdx.x % (unsigned)BH);
-    const int q0 = qb * kBM;
+    const int q0 = pr * 2 * kBM;  // tile t covers query rows q0 + t*128 .. + 127
     const int nkv_all = (a.S + kBN - 1) / kBN;
-    const int nkv = a.causal ? min(nkv_all, (q0 + kBM - 1) / kBN + 1) : nkv_all;
+    int nt[2];  // key blocks tile t reads
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+        nt[t] = a.causal ? min(nkv_all, (q0 + t * kBM + kBM - 1) / kBN + 1) : nkv_all;
+    const int nmax = max(nt[0], nt[1]);
 
     if (threadIdx.x == 0) {
         mbar_init(&b.q_full, 1);
         for (int s = 0; s < 3; ++s) {
             mbar_init(&b.k_full[s], 1);
+            mbar_init(&b.k_empty[s], 1);
             mbar_init(&b.v_full[s], 1);
-            mbar_init(&b.kv_empty[s], 1);
+            mbar_init(&b.v_empty[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&b.s_full[s], 1);
@@ -212,81 +225,93 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA loads ---
+        // lane 0: both Q tiles, then the K blocks; lane 1: the V blocks (their
+        // slots free up later than the K slots, so they get their own lane)
         if (lane == 0) {
             tc::prefetch_tmap(&tmq);
             tc::prefetch_tmap(&tmk);
-            tc::prefetch_tmap(&tmv);
-            mbar_arrive_expect_tx(&b.q_full, C::TILE);
+            mbar_arrive_expect_tx(&b.q_full, 2 * C::TILE);
 #pragma unroll
-            for (int at = 0; at < D / 64; ++at) tc::tma_load_3d(smem + C::OFF_Q + at * kAtom, &tmq, at * 64, q0, bh, &b.q_full);
-            int armed = 0;  // blocks whose loads were issued
-            for (int j = 0; j < nkv; ++j) {
-                const int st = j % NST;
-                if (j >= NST && !wait_or_flag(&b.kv_empty[st], (uint32_t)((j / NST - 1) & 1), b, a.err)) break;
+            for (int t = 0; t < 2; ++t)
+#pragma unroll
+                for (int at = 0; at < D / 64; ++at)
+                    tc::tma_load_3d(smem + C::OFF_Q + t * C::TILE + at * kAtom, &tmq, at * 64, q0 + t * kBM, bh,
+                                    &b.q_full);
+            int armed = 0;
+            for (int j = 0; j < nmax; ++j) {
+                const int st = j % NK;
+                if (j >= NK && !wait_or_flag(&b.k_empty[st], (uint32_t)((j / NK - 1) & 1), b, a.err)) break;
                 if (*reinterpret_cast<volatile int *>(&b.abort)) break;
                 mbar_arrive_expect_tx(&b.k_full[st], C::TILE);
 #pragma unroll
                 for (int at = 0; at < D / 64; ++at)
                     tc::tma_load_3d(smem + C::OFF_K + st * C::TILE + at * kAtom, &tmk, at * 64, j * kBN, bh, &b.k_full[st]);
+                armed = j + 1;
+            }
+            drain_wait(&b.q_full, 0);
+            for (int j = (armed > NK ? armed - NK : 0); j < armed; ++j) drain_wait(&b.k_full[j % NK], (uint32_t)((j / NK) & 1));
+        } else if (lane == 1) {
+            tc::prefetch_tmap(&tmv);
+            int armed = 0;
+            for (int j = 0; j < nmax; ++j) {
+                const int st = j % NV;
+                if (j >= NV && !wait_or_flag(&b.v_empty[st], (uint32_t)((j / NV - 1) & 1), b, a.err)) break;
+                if (*reinterpret_cast<volatile int *>(&b.abort)) break;
                 mbar_arrive_expect_tx(&b.v_full[st], C::TILE);
 #pragma unroll
                 for (int at = 0; at < D / 64; ++at)
                     tc::tma_load_3d(smem + C::OFF_V + st * C::TILE + at * kAtom, &tmv, at * 64, j * kBN, bh, &b.v_full[st]);
                 armed = j + 1;
             }
-            // leave no load in flight: each stage's last armed phase completes
-            // (bounded), whether or not the MMA lane consumed it
-            drain_wait(&b.q_full, 0);
-            for (int j = (armed > NST ? armed - NST : 0); j < armed; ++j) {
-                const uint32_t par = (uint32_t)((j / NST) & 1);
-                drain_wait(&b.k_full[j % NST], par);
-                drain_wait(&b.v_full[j % NST], par);
-            }
+            for (int j = (armed > NV ? armed - NV : 0); j < armed; ++j) drain_wait(&b.v_full[j % NV], (uint32_t)((j / NV) & 1));
         }
     } else if (warp == 1) {
         // ----------------------------------------------------------- MMAs ---
+        // Per key block j and tile t: S_t(j) = Q_t K_j^T into tile t's score
+        // columns, P_t(j) V_j into its output columns.  The scores run one block
+        // ahead: while one tile's softmax works, the tensor cores compute the
+        // other tile's scores and products.
         if (lane == 0) {
             bool ok = wait_or_flag(&b.q_full, 0, b, a.err);
-            const uint32_t q_addr = s_base + C::OFF_Q;
-            auto pv = [&](int m) -> bool {
-                const int pb = m % NP, st = m % NST;
-                if (!wait_or_flag(&b.p_full[pb], (uint32_t)((m / NP) & 1), b, a.err)) return false;
-                if (!wait_or_flag(&b.v_full[st], (uint32_t)((m / NST) & 1), b, a.err)) return false;
+            auto qk = [&](int t, int j) -> bool {
+                const int st = j % NK;
+                if (!wait_or_flag(&b.k_full[st], (uint32_t)((j / NK) & 1), b, a.err)) return false;
+                if (j >= 1 && !wait_or_flag(&b.s_free[t], (uint32_t)((j - 1) & 1), b, a.err)) return false;
                 tc::fence_after_sync();
-                const uint32_t p_addr = s_base + C::OFF_P + pb * C::PBUF;
-                const uint32_t v_addr = s_base + C::OFF_V + st * C::TILE;
+                const uint32_t q_addr = s_base + C::OFF_Q + t * C::TILE, k_addr = s_base + C::OFF_K + st * C::TILE;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t ko = (k / 4) * kAtom + (k % 4) * 32;
+                    tc::mma_f16(tmem + t * C::TILE_COLS + C::COL_S, tc::desc_sw128(q_addr + ko, 16, 1024),
+                                tc::desc_sw128(k_addr + ko, 16, 1024), IDESC_QK, k > 0 ? 1u : 0u);
+                }
+                tc::commit(&b.s_full[t]);
+                if (t == 1 || j >= nt[1]) tc::commit(&b.k_empty[st]);  // the last tile that reads K_j
+                return true;
+            };
+            auto pv = [&](int t, int j) -> bool {
+                const int st = j % NV;
+                if (!wait_or_flag(&b.p_full[t], (uint32_t)(j & 1), b, a.err)) return false;
+                if (!wait_or_flag(&b.v_full[st], (uint32_t)((j / NV) & 1), b, a.err)) return false;
+                tc::fence_after_sync();
+                const uint32_t p_addr = s_base + C::OFF_P + t * C::PBUF, v_addr = s_base + C::OFF_V + st * C::TILE;
 #pragma unroll
                 for (int k = 0; k < kBN / 16; ++k) {
                     const uint64_t da = tc::desc_sw128(p_addr + (k / 4) * kAtom + (k % 4) * 32, 16, 1024);
                     const uint64_t db = tc::desc_sw128(v_addr + k * 2048, kAtom, 1024);
-                    tc::mma_f16(tmem + C::COL_O, da, db, IDESC_PV, (m > 0 || k > 0) ? 1u : 0u);
+                    tc::mma_f16(tmem + t * C::TILE_COLS + C::COL_O, da, db, IDESC_PV, (j > 0 || k > 0) ? 1u : 0u);
                 }
-                tc::commit(&b.pv_done[pb]);
-                tc::commit(&b.kv_empty[st]);
+                tc::commit(&b.pv_done[t]);
+                if (t == 1 || j >= nt[1]) tc::commit(&b.v_empty[st]);  // the last tile that reads V_j
                 return true;
             };
-            // S_j = Q K_j^T into score buffer j % 2, once that buffer's block j - 2 has been read
-            auto qk = [&](int j) -> bool {
-                const int st = j % NST, sb = j & 1;
-                if (!wait_or_flag(&b.k_full[st], (uint32_t)((j / NST) & 1), b, a.err)) return false;
-                if (j >= 2 && !wait_or_flag(&b.s_free[sb], (uint32_t)(((j - 2) / 2) & 1), b, a.err)) return false;
-                tc::fence_after_sync();
-                const uint32_t k_addr = s_base + C::OFF_K + st * C::TILE;
-#pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint64_t da = tc::desc_sw128(q_addr + (k / 4) * kAtom + (k % 4) * 32, 16, 1024);
-                    const uint64_t db = tc::desc_sw128(k_addr + (k / 4) * kAtom + (k % 4) * 32, 16, 1024);
-                    tc::mma_f16(tmem + sb * kBN, da, db, IDESC_QK, k > 0 ? 1u : 0u);
+            for (int t = 0; ok && t < 2; ++t)
+                if (nt[t] > 0 && !qk(t, 0)) ok = false;
+            for (int j = 0; ok && j < nmax; ++j) {
+                for (int t = 0; t < 2; ++t) {
+                    if (j + 1 < nt[t] && !qk(t, j + 1)) { ok = false; break; }
+                    if (j < nt[t] && !pv(t, j)) { ok = false; break; }
                 }
-                tc::commit(&b.s_full[sb]);
-                return true;
-            };
-            // the scores run one block ahead of P V: S_{j+1} is on the tensor
-            // cores while the softmax of block j works
-            if (ok) ok = qk(0);
-            for (int j = 0; ok && j < nkv; ++j) {
-                if (j + 1 < nkv && !qk(j + 1)) { ok = false; break; }
-                if (!pv(j)) { ok = false; break; }
             }
             // leave no MMA in flight
             tc::commit(&b.mma_drain);
@@ -294,55 +319,84 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
         }
     } else {
         // -------------------------------------------------------- softmax ---
+        const int t = (warp - 2) >> 2;       // tile of this warp group
         const int quarter = warp & 3;
-        const int r = quarter * 32 + lane;  // query row within the tile = TMEM lane
-        const int i = q0 + r;
+        const int r = quarter * 32 + lane;   // query row within the tile = TMEM lane
+        const int i = q0 + t * kBM + r;
         const bool row_ok = i < a.S;
-        const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16) + t * C::TILE_COLS;
         const float sl2 = a.scale * kLog2e;
         const int bidx = bh / a.H, hidx = bh - bidx * a.H;
         const int64_t mrow = (int64_t)bidx * a.msb + (int64_t)hidx * a.msh + (int64_t)i * a.S;
+        const int n = nt[t];
+        const int qt0 = q0 + t * kBM;
         float m_run = neg_inf(), l = 0.f;
         bool ok = true;
-        unsigned char *pbase = smem + C::OFF_P;
-        for (int j = 0; j < nkv; ++j) {
-            const int sb = j & 1, pb = j % NP;
+        unsigned char *pbuf = smem + C::OFF_P + t * C::PBUF;
+        for (int j = 0; j < n; ++j) {
             const int j0 = j * kBN;
             // per-element rules only where a block crosses the diagonal or the end of the keys
-            const bool pred = (j0 + kBN > a.S) || (a.causal && j0 + kBN - 1 > q0);
-            if (!warp_wait(&b.s_full[sb], (uint32_t)((j / 2) & 1), b, a.err)) { ok = false; break; }
+            const bool pred = (j0 + kBN > a.S) || (a.causal && j0 + kBN - 1 > qt0);
+            if (!warp_wait(&b.s_full[t], (uint32_t)(j & 1), b, a.err)) { ok = false; break; }
             tc::fence_after_sync();
-            // pass 1: the block's row max (log2 units)
+            // the whole block row in registers, then the score columns go back to the MMA
+            float sv[kBN];
+#pragma unroll
+            for (int c = 0; c < kBN / 32; ++c) tc::tmem_ld32(tl + C::COL_S + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * c));
+            tc::tmem_wait_ld();
+            tc::fence_before_sync();
+            mbar_arrive(&b.s_free[t]);
             float mx = neg_inf();
 #pragma unroll
             for (int c = 0; c < kBN / 32; ++c) {
-                uint32_t v[32];
                 float m2[32];
                 mask_chunk<T, MK>(a, mrow, j0 + c * 32, row_ok, m2);
-                tc::tmem_ld32(tl + sb * kBN + c * 32, v);
-                tc::tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    float s = fmaf(__uint_as_float(v[e]), sl2, m2[e]);
+                for (int e = 0; e < 32; e += 2) {
+                    float s0 = fmaf(sv[32 * c + e], sl2, m2[e]);
+                    float s1 = fmaf(sv[32 * c + e + 1], sl2, m2[e + 1]);
                     if (pred) {
                         const int col = j0 + c * 32 + e;
-                        if (col >= a.S || (a.causal && col > i)) s = neg_inf();
+                        if (col >= a.S || (a.causal && col > i)) s0 = neg_inf();
+                        if (col + 1 >= a.S || (a.causal && col + 1 > i)) s1 = neg_inf();
                     }
-                    mx = fmaxf(mx, s);
+                    sv[32 * c + e] = s0;
+                    sv[32 * c + e + 1] = s1;
+                    mx = rowmath_max3(mx, s0, s1);
                 }
             }
             const float m_new = fmaxf(m_run, mx);
             const bool resc = m_new > m_run + 8.f;  // false while both are -inf
             const float m_use = resc ? m_new : m_run;
             const float alpha = resc ? ex2(m_run - m_new) : 1.f;  // 0 when m_run is -inf
-            l *= alpha;
-            // the P buffer of this block is free once the P V MMA of block j - NP is done
-            if (j >= NP && !warp_wait(&b.pv_done[pb], (uint32_t)(((j - NP) / NP) & 1), b, a.err)) { ok = false; break; }
-            if (j >= 1 && __any_sync(0xffffffffu, resc)) {
-                // O holds the blocks before j: rescale it once their P V MMA is done
-                const int m = j - 1;
-                if (!warp_wait(&b.pv_done[m % NP], (uint32_t)((m / NP) & 1), b, a.err)) { ok = false; break; }
+            const float moff = (m_use == neg_inf()) ? 0.f : m_use;
+            float lsum = 0.f;
+#pragma unroll
+            for (int e = 0; e < kBN; ++e) {
+                sv[e] = ex2(sv[e] - moff);
+                lsum += sv[e];
+            }
+            l = l * alpha + lsum;
+            // P of block j - 1 has been consumed (this tile's P buffer is free)
+            // and O holds every block before j once that P V is done
+            if (j >= 1) {
+                if (!warp_wait(&b.pv_done[t], (uint32_t)((j - 1) & 1), b, a.err)) { ok = false; break; }
                 tc::fence_after_sync();
+            }
+#pragma unroll
+            for (int c = 0; c < kBN / 32; ++c) {
+                unsigned char *atom = pbuf + (c / 2) * kAtom;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        w[u] = pack2(sv[32 * c + 8 * q + 2 * u], sv[32 * c + 8 * q + 2 * u + 1], static_cast<T *>(nullptr));
+                    const uint32_t off = tc::sw128_off((uint32_t)r, (uint32_t)((c & 1) * 4 + q));
+                    *reinterpret_cast<uint4 *>(atom + off) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+            if (j >= 1 && __any_sync(0xffffffffu, resc)) {  // the running max grew: rescale O
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
@@ -354,49 +408,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 }
                 tc::tmem_wait_st();
             }
-            // pass 2: P = 2^(s - m) into shared memory, row sums
-            const float moff = (m_use == neg_inf()) ? 0.f : m_use;
-            unsigned char *pbuf = pbase + pb * C::PBUF;
-#pragma unroll
-            for (int c = 0; c < kBN / 32; ++c) {
-                uint32_t v[32];
-                float m2[32];
-                mask_chunk<T, MK>(a, mrow, j0 + c * 32, row_ok, m2);
-                tc::tmem_ld32(tl + sb * kBN + c * 32, v);
-                tc::tmem_wait_ld();
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float s0 = fmaf(__uint_as_float(v[e]), sl2, m2[e]);
-                    float s1 = fmaf(__uint_as_float(v[e + 1]), sl2, m2[e + 1]);
-                    if (pred) {
-                        const int col = j0 + c * 32 + e;
-                        if (col >= a.S || (a.causal && col > i)) s0 = neg_inf();
-                        if (col + 1 >= a.S || (a.causal && col + 1 > i)) s1 = neg_inf();
-                    }
-                    const float p0 = ex2(s0 - moff), p1 = ex2(s1 - moff);
-                    l += p0 + p1;
-                    pk[e / 2] = pack2(p0, p1, static_cast<T *>(nullptr));
-                }
-                unsigned char *atom = pbuf + (c / 2) * kAtom;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t off = tc::sw128_off((uint32_t)r, (uint32_t)((c & 1) * 4 + q));
-                    *reinterpret_cast<uint4 *>(atom + off) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-                }
-            }
-            tc::fence_before_sync();
-            mbar_arrive(&b.s_free[sb]);
             tc::fence_async_smem();
-            mbar_arrive(&b.p_full[pb]);
+            tc::fence_before_sync();
+            mbar_arrive(&b.p_full[t]);
             m_run = m_use;
         }
         // epilogue: O / l, lse
-        if (ok) {
-            const int m = nkv - 1;
-            ok = warp_wait(&b.pv_done[m % NP], (uint32_t)((m / NP) & 1), b, a.err);
-        }
-        if (ok) {
+        if (ok && n > 0) ok = warp_wait(&b.pv_done[t], (uint32_t)((n - 1) & 1), b, a.err);
+        if (ok && n > 0) {
             tc::fence_after_sync();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             T *orow = reinterpret_cast<T *>(a.o) + ((int64_t)bh * a.S + i) * D;
@@ -504,7 +523,7 @@ cudaError_t launch_fwd(const AttnArgs &a, const CUtensorMap &tq, const CUtensorM
         attr_done[dev & 63] = true;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(((a.S + kBM - 1) / kBM) * a.B * a.H));
+    cfg.gridDim = dim3((unsigned)(((a.S + 2 * kBM - 1) / (2 * kBM)) * a.B * a.H));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
