@@ -134,10 +134,9 @@ SMS_API int sms_forward(const void *x, const void *mask, int64_t mask_numel, int
  *             as in sms_forward, in elements (= bytes) of the mask
  *   other arguments as sms_forward; y may equal x and must not overlap the mask.
  * The backward is sms_backward (the mask only shapes y).
- * Errors as sms_forward, plus SMS_ERR_INVALID_ARG for a NULL mask (rows > 0)
- * and SMS_ERR_UNSUPPORTED when SMS_PATH_CTA is forced: every kernel family
- * but the staged CTA one reads the boolean mask, and the rows the dispatcher
- * would give that family go to SMS_PATH_ONLINE.
+ * Every kernel family reads the boolean mask (the staged CTA family stages
+ * its bytes with the scores), and the dispatcher chooses as for sms_forward.
+ * Errors as sms_forward, plus SMS_ERR_INVALID_ARG for a NULL mask (rows > 0).
  */
 SMS_API int sms_forward_bool(const void *x, const uint8_t *mask, int64_t mask_numel, int64_t mask_stride_b,
                              int64_t mask_stride_h, int64_t heads, void *y, int64_t rows, int64_t cols, float scale,
@@ -316,6 +315,17 @@ SMS_API int sms_set_forced_path(int path);
  * Returns the previous cap, or -1 for a negative argument.  Process-wide.
  */
 SMS_API int sms_set_grid_limit(int ctas);
+
+/*
+ * Test control of the bounded-wait abort path (process-wide; 0 = off, the
+ * default).  With ns > 0, every lane group of the SMS_PATH_RING kernels makes
+ * its first wait one on a barrier that nothing ever arrives at, bounded at ns
+ * nanoseconds instead of 2 s: the wait gives up, the kernel records
+ * SMS_DEVERR_RING_WAIT, waits (bounded at 2 s) for the bulk copies it has in
+ * flight and returns without finishing its rows.  Returns the previous value,
+ * or -1 for ns outside [0, 1e9].
+ */
+SMS_API int64_t sms_set_test_stall(int64_t ns);
 
 /* The family the dispatcher would pick for this forward (or backward) shape of non-causal rows. */
 SMS_API int sms_select_path(int64_t rows, int64_t cols, int dtype, int is_backward);

@@ -42,6 +42,7 @@ SIGNATURES = {
     "sms_select_path": (_i32, [_i64, _i64, _i32, _i32]),
     "sms_last_path": (_i32, []),
     "sms_launch_count": (_i64, []),
+    "sms_set_test_stall": (_i64, [_i64]),
     "sms_device_error": (_i32, [_vp]),
     "sms_version": (_i32, []),
 }
@@ -154,6 +155,13 @@ def sms_last_path() -> int:
 
 def sms_launch_count() -> int:
     return lib().sms_launch_count()
+
+
+def sms_set_test_stall(ns: int) -> int:
+    prev = lib().sms_set_test_stall(int(ns))
+    if prev < 0:
+        raise ValueError(f"bad stall {ns}")
+    return prev
 
 
 def sms_device_error(stream) -> int:

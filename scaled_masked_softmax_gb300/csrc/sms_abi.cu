@@ -24,6 +24,7 @@ thread_local int t_last_path = SMS_PATH_AUTO;
 std::atomic<int> g_forced{SMS_PATH_AUTO};
 std::atomic<int> g_grid_limit{0};
 std::atomic<int64_t> g_launches{0};
+std::atomic<uint32_t> g_stall_ns{0};
 
 constexpr int kMaxDevices = 64;
 std::once_flag g_dev_once[kMaxDevices];
@@ -132,6 +133,8 @@ void clear_last_error() { t_err[0] = '\0'; }
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+uint32_t test_stall_ns() { return g_stall_ns.load(std::memory_order_relaxed); }
+
 cudaError_t device_error_word(int **err)
 {
     int dev = 0, n = 0;
@@ -191,6 +194,12 @@ int sms_set_grid_limit(int ctas)
 }
 
 int64_t sms_launch_count(void) { return g_launches.load(); }
+
+int64_t sms_set_test_stall(int64_t ns)
+{
+    if (ns < 0 || ns > 1000000000ll) return -1;
+    return g_stall_ns.exchange((uint32_t)ns);
+}
 
 int sms_select_path(int64_t rows, int64_t cols, int dtype, int is_backward)
 {
@@ -263,16 +272,7 @@ int forward_impl(const char *who, const void *x, const void *mask, int64_t mask_
 
     const int vec = vec_elems(dtype);
     const bool aligned = cols % vec == 0 && (!mask || (mask_stride_b % vec == 0 && mask_stride_h % vec == 0));
-    int path = pick_path(g_forced.load(), cols, dtype, aligned, false, is_causal != 0);
-    if (mask_bool) {
-        // byte masks are read by every family but the staged CTA path, whose
-        // producer stages additive mask rows; its rows go to the two-pass kernel
-        if (path == SMS_PATH_CTA) {
-            if (g_forced.load() == SMS_PATH_CTA)
-                return fail(SMS_ERR_UNSUPPORTED, "%s: the CTA path does not read a boolean mask", who);
-            path = SMS_PATH_ONLINE;
-        }
-    }
+    const int path = pick_path(g_forced.load(), cols, dtype, aligned, false, is_causal != 0);
 
     int dev = 0, nsm = 0;
     int *err = nullptr;
@@ -292,6 +292,7 @@ int forward_impl(const char *who, const void *x, const void *mask, int64_t mask_
     a.dheads = FastDiv((uint32_t)heads);
     a.lengths = lengths;
     a.mask_bool = (mask && mask_bool) ? 1 : 0;
+    a.stall_ns = test_stall_ns();
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (path) {
@@ -374,6 +375,7 @@ int backward_impl(const char *who, const void *y, const void *dy, void *dx, cons
     a.lengths = lengths;
     a.heads = heads;
     a.dheads = FastDiv((uint32_t)heads);
+    a.stall_ns = test_stall_ns();
 
     const int path = pick_path(g_forced.load(), cols, dtype, aligned, true, a.causal != 0);
     cudaStream_t st = static_cast<cudaStream_t>(stream);

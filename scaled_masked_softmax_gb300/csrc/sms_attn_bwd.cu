@@ -41,7 +41,8 @@ namespace {
 
 constexpr int kBM = 128;          // keys per CTA (the MMA's M for S^T, dP^T, dV, dK)
 constexpr int kBN = 128;          // queries per block
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;     // warps 0 (TMA), 1 (MMA), 2..9 (element-wise: two warps per TMEM lane quarter)
+constexpr int kMath = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAtom = 16384;
 
@@ -168,9 +169,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             mbar_init(&b.q_empty[s], 1);
         }
         mbar_init(&b.s_full, 1);
-        mbar_init(&b.ds_full, kBM);
+        mbar_init(&b.ds_full, kMath);
         mbar_init(&b.dq_full, 1);
-        mbar_init(&b.dq_free, kBM);
+        mbar_init(&b.dq_free, kMath);
         mbar_init(&b.mma_drain, 1);
         b.abort = 0;
         fence_mbar_init();
@@ -262,7 +263,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
         }
     } else {
         // --------------------------------------------- element-wise work ---
+        // two warps per TMEM lane quarter: `half` takes half of the columns
+        // (queries of S^T / dP^T, head-dim columns of dQ, dK, dV)
         const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const int mt = threadIdx.x - 64;   // 0 .. 255
         const int t = quarter * 32 + lane;  // TMEM lane: key j0 + t (S^T, dP^T, dV, dK) or query i0 + t (dQ)
         const int j = j0 + t;
         const bool key_ok = j < a.S;
@@ -275,23 +280,24 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
         for (int n = 0; n < npair; ++n) {
             const int i0 = (qb0 + n) * kBN;
             // this block's lse (log2 units; +inf where the row has no kept key, or beyond S) and delta
-            {
-                const int i = i0 + t;
+            if (mt < kBN) {
+                const int i = i0 + mt;
                 float l2 = __int_as_float(0x7f800000), dl = 0.f;
                 if (i < a.S) {
                     const float lse = a.lse_in[row0 + i];
                     l2 = (lse == neg_inf()) ? __int_as_float(0x7f800000) : lse * kLog2e;
                     dl = a.delta[row0 + i];
                 }
-                s_lse[t] = l2;
-                s_del[t] = dl;
+                s_lse[mt] = l2;
+                s_del[mt] = dl;
             }
-            named_sync(1, kBM);
+            named_sync(1, kMath);
             const bool pred = !key_ok || (i0 + kBN > a.S) || (a.causal && j0 + kBM - 1 > i0);
             if (!warp_wait(&b.s_full, (uint32_t)(n & 1), b, a.err)) { ok = false; break; }
             tc::fence_after_sync();
 #pragma unroll
-            for (int c = 0; c < kBN / 32; ++c) {
+            for (int cc = 0; cc < kBN / 64; ++cc) {
+                const int c = half * (kBN / 64) + cc;  // this warp's 32-query chunks
                 float m2[32];
                 mask_col<T, MK>(a, mbase, i0 + c * 32, key_ok, m2);
                 uint32_t sv[32], dv[32];
@@ -334,7 +340,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             const int iq = i0 + t;
             float *acc = a.dq_acc + (row0 + iq) * D;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int cc = 0; cc < D / 64; ++cc) {
+                const int c = half * (D / 64) + cc;  // this warp's 32-column chunks of dQ
                 uint32_t v[32];
                 tc::tmem_ld32(tl + C::COL_DQ + c * 32, v);
                 tc::tmem_wait_ld();
@@ -354,7 +361,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             T *dkr = reinterpret_cast<T *>(a.dk) + (row0 + j) * D;
             T *dvr = reinterpret_cast<T *>(a.dv) + (row0 + j) * D;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int cc = 0; cc < D / 64; ++cc) {
+                const int c = half * (D / 64) + cc;
                 uint32_t kv[32], vv[32];
                 tc::tmem_ld32(tl + C::COL_DK + c * 32, kv);
                 tc::tmem_ld32(tl + C::COL_DV + c * 32, vv);

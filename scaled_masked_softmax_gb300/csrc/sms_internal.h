@@ -28,6 +28,8 @@ struct FwdArgs {
     FastDiv dcols, dheads; // division by cols and by heads
     const int32_t *lengths;  // per-batch key lengths (device), nullptr: none
     int mask_bool;         // 1: the mask holds one byte per element (nonzero = masked), 0: additive, dtype of x
+    uint32_t stall_ns;     // test control (sms_set_test_stall): >0 makes a ring group's first wait one on a
+                           // barrier nothing arrives at, bounded at this many ns
 };
 
 struct BwdArgs {
@@ -43,6 +45,7 @@ struct BwdArgs {
     const int32_t *lengths;  // key-length hint: y == 0 at j >= lengths[b]; nullptr: none
     int64_t heads;         // heads of the [B,H,S,S] view (locates b for the lengths)
     FastDiv dheads;        // division by heads
+    uint32_t stall_ns;     // test control, as in FwdArgs
 };
 
 // "aligned" means every row (and every mask row) starts on a 16-byte boundary:
@@ -87,6 +90,9 @@ int set_last_error(int status, const char *msg);
 void clear_last_error();
 void count_launch();
 cudaError_t device_error_word(int **err);
+
+// The test control of sms_set_test_stall (0: off).
+uint32_t test_stall_ns();
 
 // CTAs for a persistent kernel: `per_sm` per multiprocessor, at most `useful`,
 // at most the limit set by sms_set_grid_limit

@@ -67,6 +67,7 @@ template <int G, int NV, int K, bool MB> constexpr int ring_smem()
 // reduction slots for multi-warp groups.
 template <int K> struct RingHdr {
     uint64_t full[16][K];
+    uint64_t stall;                    // test control: a barrier nothing ever arrives at
     int abort[16];
     float red_m[2][16], red_l[2][16];  // [row parity][group * W + warp]
 };
@@ -157,11 +158,14 @@ __global__ void __launch_bounds__(ring_groups<G, NV, K, MB>() * G, 1) ring_kerne
     const int64_t ng = (int64_t)gridDim.x * GPC;
     const int64_t r0 = (int64_t)blockIdx.x * GPC + gi;
 
+    const uint32_t stall_ns = BWD ? ba.stall_ns : fa.stall_ns;
     if (issuer) {
         for (int s = 0; s < K; ++s) mbar_init(&bars[s], 1);
         h.abort[gi] = 0;
+        if (gi == 0) mbar_init(&h.stall, 1);
         fence_mbar_init();
     }
+    if (stall_ns) __syncthreads();  // the stall barrier is initialised before any group waits on it
     if constexpr (W > 1) named_sync(bar_id, G);
     else __syncwarp();
     volatile int *abort_flag = &h.abort[gi];
@@ -186,7 +190,10 @@ __global__ void __launch_bounds__(ring_groups<G, NV, K, MB>() * G, 1) ring_kerne
         unsigned char *st = ring + s * Geo::STAGE;
         // a warp whose wait gave up reads nothing, flags the group, and still
         // takes part in the group barrier; the group then leaves together
-        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], par, abort_flag));
+        // (test control: the first wait is one on the stall barrier, which never completes)
+        const bool ok = __all_sync(0xffffffffu, (stall_ns && i == 0)
+                                                    ? mbar_wait_bounded(&h.stall, 0, abort_flag, stall_ns)
+                                                    : mbar_wait_bounded(&bars[s], par, abort_flag));
         if (!ok && lane == 0) {
             *abort_flag = 1;
             report_error(err, SMS_DEVERR_RING_WAIT);

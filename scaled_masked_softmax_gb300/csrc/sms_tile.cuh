@@ -31,6 +31,7 @@
 #pragma once
 
 #include <atomic>
+#include <type_traits>
 
 #include "sms_common.cuh"
 #include "sms_internal.h"
@@ -98,7 +99,10 @@ template <int WG, int R, int SLOTS, int CH> __host__ __device__ constexpr int sm
     return hdr_bytes<WG, R>() + R * ring_k<WG, R, SLOTS, CH>() * Geo<WG, R, SLOTS, CH>::STAGE;
 }
 
-template <typename T, int WG, int R, int SLOTS, int CH, bool BWD>
+// M: the mask element type of the forward (T: additive; uint8_t: one byte per
+// element, nonzero = masked).  Mask rows are staged in 16-byte vectors of
+// their own alignment either way: MEPV elements per vector.
+template <typename T, int WG, int R, int SLOTS, int CH, bool BWD, typename M>
 __global__ void __launch_bounds__(Geo<WG, R, SLOTS, CH>::THREADS, 1)
     tile_kernel(const FwdArgs fa, const BwdArgs ba)
 {
@@ -106,6 +110,8 @@ __global__ void __launch_bounds__(Geo<WG, R, SLOTS, CH>::THREADS, 1)
     constexpr int K = ring_k<WG, R, SLOTS, CH>();
     static_assert(K >= 2, "each group needs at least two stages");
     constexpr int VEC = Dt<T>::VEC;
+    constexpr int MEPV = 16 / (int)sizeof(M);  // mask elements per 16-byte vector
+    constexpr bool MBOOL = !std::is_same<M, T>::value;
     constexpr int GT = G::GT;
     extern __shared__ __align__(128) unsigned char smem[];
     Hdr<WG, R> &h = *reinterpret_cast<Hdr<WG, R> *>(smem);
@@ -192,10 +198,10 @@ __global__ void __launch_bounds__(Geo<WG, R, SLOTS, CH>::THREADS, 1)
                         } else if (srcB) {
                             const int64_t jlo = max(0, vlo * VEC - d.xoff);
                             const int64_t jhi = min((int64_t)d.limit, (int64_t)vhi * VEC - d.xoff);
-                            const int64_t mv_lo = (d.m0 + jlo) / VEC;
-                            const int64_t cm_hi = min((d.m0 + jhi + VEC - 1) / VEC, fa.mask_total / VEC);
-                            d.mrel = (int)(d.m0 - mv_lo * VEC);
-                            d.mcnt = cm_hi > mv_lo ? (int)(cm_hi - mv_lo) * VEC : 0;
+                            const int64_t mv_lo = (d.m0 + jlo) / MEPV;
+                            const int64_t cm_hi = min((d.m0 + jhi + MEPV - 1) / MEPV, fa.mask_total / MEPV);
+                            d.mrel = (int)(d.m0 - mv_lo * MEPV);
+                            d.mcnt = cm_hi > mv_lo ? (int)(cm_hi - mv_lo) * MEPV : 0;
                             bytesB = cm_hi > mv_lo ? (uint32_t)(cm_hi - mv_lo) * 16u : 0u;
                             b_src = mv_lo;
                         }
@@ -326,18 +332,31 @@ __global__ void __launch_bounds__(Geo<WG, R, SLOTS, CH>::THREADS, 1)
 #pragma unroll
                         for (int e = 0; e < VEC; ++e) b[e] = 0.f;
                         if (srcB) {
-                            const T *msm = reinterpret_cast<const T *>(st + G::B_OFF);
+                            using MIO = MaskIO<T, M>;
+                            const M *msm = reinterpret_cast<const M *>(st + G::B_OFF);
                             const int jj = j0 + d.mrel;  // stage index of element j0
                             if (d.mvec && jj >= 0 && jj + VEC <= d.mcnt) {
-                                unpack<T>(*reinterpret_cast<const uint4 *>(msm + jj), b);
+                                if constexpr (MBOOL) {  // VEC bytes: one 4- or 8-byte shared load
+                                    uint4 w = make_uint4(0, 0, 0, 0);
+                                    if constexpr (VEC == 4) {
+                                        w.x = *reinterpret_cast<const uint32_t *>(msm + jj);
+                                    } else {
+                                        const uint2 v = *reinterpret_cast<const uint2 *>(msm + jj);
+                                        w.x = v.x;
+                                        w.y = v.y;
+                                    }
+                                    MIO::unpack_m(w, b);
+                                } else {
+                                    unpack<T>(*reinterpret_cast<const uint4 *>(msm + jj), b);
+                                }
                             } else {
-                                const T *mrow = reinterpret_cast<const T *>(srcB) + d.m0;
+                                const M *mrow = reinterpret_cast<const M *>(srcB) + d.m0;
 #pragma unroll
                                 for (int e = 0; e < VEC; ++e) {
                                     const int j = j0 + e;
                                     if (j >= 0 && j < limit) {
                                         const int idx = j + d.mrel;
-                                        b[e] = idx < d.mcnt ? to_f32<T>(msm[idx]) : to_f32<T>(mrow[j]);
+                                        b[e] = idx < d.mcnt ? MIO::elem(msm + idx) : MIO::elem(mrow + j);
                                     }
                                 }
                             }
@@ -459,11 +478,11 @@ __global__ void __launch_bounds__(Geo<WG, R, SLOTS, CH>::THREADS, 1)
     }
 }
 
-template <typename T, int WG, int R, int SLOTS, int CH, bool BWD>
+template <typename T, int WG, int R, int SLOTS, int CH, bool BWD, typename M>
 cudaError_t launch_tile(const FwdArgs &fa, const BwdArgs &ba, cudaStream_t st)
 {
     constexpr int smem = smem_bytes<WG, R, SLOTS, CH>();
-    auto kern = tile_kernel<T, WG, R, SLOTS, CH, BWD>;
+    auto kern = tile_kernel<T, WG, R, SLOTS, CH, BWD, M>;
     static thread_local bool attr_done[64];  // per device and host thread: the shared-memory limit has been raised
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -498,12 +517,12 @@ inline int64_t row_vectors(int64_t cols, int dtype, bool aligned)
 //   WG=16 R=1 : 4, 8 slots, rows in 2 or 4 chunks
 // SLOTS is capped at 4 for the 16-bit forward (8 fp32 scores per slot) and 8
 // elsewhere, which keeps every thread within 32 fp32 values per slot set.
-template <typename T, bool BWD>
+template <typename T, bool BWD, typename M = T>
 cudaError_t launch_t(const FwdArgs &fa, const BwdArgs &ba, int64_t vecs, cudaStream_t st)
 {
     constexpr bool S8 = BWD || Dt<T>::VEC == 4;  // 8 slots allowed
 #define SMS_TILE(WG, R, SL, CH) \
-    if (vecs <= (int64_t)(WG) * 32 * (SL)) return launch_tile<T, WG, R, SL, CH, BWD>(fa, ba, st);
+    if (vecs <= (int64_t)(WG) * 32 * (SL)) return launch_tile<T, WG, R, SL, CH, BWD, M>(fa, ba, st);
     SMS_TILE(1, 8, 1, 1) SMS_TILE(1, 8, 2, 2) SMS_TILE(1, 8, 4, 4)
     if constexpr (S8) { SMS_TILE(1, 8, 8, 8) }
     SMS_TILE(2, 4, 4, 4)
@@ -524,10 +543,13 @@ template <bool BWD>
 cudaError_t dispatch(const FwdArgs &fa, const BwdArgs &ba, int64_t cols, int dtype, bool aligned, cudaStream_t st)
 {
     const int64_t vecs = row_vectors(cols, dtype, aligned);
+    const bool mb = !BWD && fa.mask && fa.mask_bool;
     switch (dtype) {
-    case kF32: return launch_t<float, BWD>(fa, ba, vecs, st);
-    case kF16: return launch_t<__half, BWD>(fa, ba, vecs, st);
-    case kBF16: return launch_t<__nv_bfloat16, BWD>(fa, ba, vecs, st);
+    case kF32: return mb ? launch_t<float, BWD, uint8_t>(fa, ba, vecs, st) : launch_t<float, BWD>(fa, ba, vecs, st);
+    case kF16: return mb ? launch_t<__half, BWD, uint8_t>(fa, ba, vecs, st) : launch_t<__half, BWD>(fa, ba, vecs, st);
+    case kBF16:
+        return mb ? launch_t<__nv_bfloat16, BWD, uint8_t>(fa, ba, vecs, st)
+                  : launch_t<__nv_bfloat16, BWD>(fa, ba, vecs, st);
     default: return cudaErrorInvalidValue;
     }
 }

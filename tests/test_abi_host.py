@@ -241,11 +241,11 @@ def test_forward_bool_mask_extent_is_counted_in_bytes():
 
 
 def test_forward_bool_paths():
-    # the byte mask is read by every family but the staged CTA one, which is
-    # refused before any device access; a no-op stays a no-op
+    # the byte mask is read by every family (no forced path refuses it on the
+    # host; without a device each reaches the device query); a no-op stays a no-op
     if torch.cuda.is_available():
         pytest.skip("host-only check")
-    for path, want in [(sms.SMS_PATH_RING, binding.SMS_ERR_CUDA), (sms.SMS_PATH_CTA, UNSUPPORTED),
+    for path, want in [(sms.SMS_PATH_RING, binding.SMS_ERR_CUDA), (sms.SMS_PATH_CTA, binding.SMS_ERR_CUDA),
                        (sms.SMS_PATH_STREAM, binding.SMS_ERR_CUDA), (sms.SMS_PATH_WARP, binding.SMS_ERR_CUDA),
                        (sms.SMS_PATH_ONLINE, binding.SMS_ERR_CUDA), (sms.SMS_PATH_AUTO, binding.SMS_ERR_CUDA)]:
         prev = sms.sms_set_forced_path(path)
@@ -324,3 +324,11 @@ def test_attention_backward_workspace_size():
 def test_attention_backward_rejects_bad_arguments(kw, status):
     assert _attn_bwd(**kw) == status
     assert binding.lib().sms_last_error().decode().startswith("sms_attention_backward")
+
+
+def test_test_stall_control_range():
+    L = binding.lib()
+    assert L.sms_set_test_stall(-1) == -1
+    assert L.sms_set_test_stall(2_000_000_000) == -1
+    prev = L.sms_set_test_stall(5000)
+    assert L.sms_set_test_stall(prev) == 5000

@@ -59,7 +59,7 @@ def _run(path, fn):
     return out, taken
 
 
-@pytest.mark.parametrize("path", ["auto", "warp", "stream", "ring", "online"])
+@pytest.mark.parametrize("path", ["auto", "warp", "stream", "ring", "cta", "online"])
 @pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("S", WIDTHS)
 def test_bool_mask_widths(S, dt, path):
@@ -73,7 +73,6 @@ def test_bool_mask_widths(S, dt, path):
     y_bool, taken = _run(path, lambda: H.raw_forward_bool(x, mb, 0, 0, 1, w))
     y_add, taken_add = _run(path, lambda: H.raw_forward(dict(x=x, mask=ma, mask_stride_b=0, mask_stride_h=0,
                                                              heads=1), w))
-    assert taken != sms.SMS_PATH_CTA
     if taken == taken_add:
         assert torch.equal(y_bool, y_add), f"{path} S={S} {dt}: boolean and additive -inf masks differ"
     y_ref = oracle.forward(x.cpu(), S, w.scale, causal, mb.cpu())
@@ -82,7 +81,7 @@ def test_bool_mask_widths(S, dt, path):
         assert torch.all(y_bool[1] == 0), "a fully masked row must be zero"
 
 
-@pytest.mark.parametrize("path", ["auto", "warp", "stream", "ring", "online"])
+@pytest.mark.parametrize("path", ["auto", "warp", "stream", "ring", "cta", "online"])
 @pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("kind", ["SS", "B1SS", "BHSS"])
 @pytest.mark.parametrize("causal", [False, True])
@@ -103,24 +102,22 @@ def test_bool_mask_layouts(S, causal, kind, dt, path):
     H.check_forward(H.to_np64(y), y_ref, DTYPES[dt], f"{path} bool {kind} S={S} {dt} causal={causal}")
 
 
-def test_bool_mask_cta_path_is_refused():
-    """The staged CTA family stages additive mask rows only: forced, it is
-    refused; its rows (fp32, 8193..16384 columns) go to the two-pass kernel."""
-    w = workloads.Workload("b_r", 1, 1, 256, "f16", 8.0, 0.125, "none", True, False, 65)
+def test_bool_mask_on_the_cta_path():
+    """The staged CTA family stages the mask bytes with the scores: its rows
+    (fp32, 8193..16384 columns) take it with a boolean mask too, bit-equal to
+    the additive -inf mask on the same path, with the grid capped so every CTA
+    walks several rows through its stage ring."""
+    w = workloads.Workload("b_c", 1, 1, 12345, "f32", 8.0, 0.125, "none", False, False, 66, rows_override=40)
     x = workloads.make_inputs(w, device="cuda")["x"]
-    mb = _mask((256, 256), 0.1, 66)
-    with H.forced_path("cta"):
-        with pytest.raises(sms.SmsError) as e:
-            H.raw_forward_bool(x, mb, 0, 0, 1, w)
-    assert e.value.status == 2
-    w2 = workloads.Workload("b_o", 1, 1, 12345, "f32", 8.0, 0.125, "none", False, False, 66, rows_override=40)
-    x2 = workloads.make_inputs(w2, device="cuda")["x"]
-    mb2 = _mask((40, 12345), 0.1, 67)
-    y2 = H.raw_forward_bool(x2, mb2, 0, 0, 1, w2)
-    assert sms.sms_last_path() == sms.SMS_PATH_ONLINE
-    torch.cuda.synchronize()
-    H.check_forward(H.to_np64(y2), oracle.forward(x2.cpu(), 12345, w2.scale, False, mb2.cpu()), torch.float32,
-                    "bool fp32 S=12345 auto")
+    mb = _mask((40, 12345), 0.1, 67)
+    with H.grid_limit(3):
+        y, taken = _run("auto", lambda: H.raw_forward_bool(x, mb, 0, 0, 1, w))
+        y_add, taken_add = _run("auto", lambda: H.raw_forward(dict(x=x, mask=_additive(mb, torch.float32),
+                                                                   mask_stride_b=0, mask_stride_h=0, heads=1), w))
+    assert taken == taken_add == sms.SMS_PATH_CTA
+    assert torch.equal(y, y_add)
+    H.check_forward(H.to_np64(y), oracle.forward(x.cpu(), 12345, w.scale, False, mb.cpu()), torch.float32,
+                    "bool fp32 S=12345 cta")
 
 
 def test_bool_mask_autograd_and_in_place():
@@ -164,8 +161,7 @@ def test_full_size_bool_mask(name):
     torch.cuda.synchronize()
     if path_bool == path_add:
         assert torch.equal(y, y_add)
-    else:  # fp32 rows the CTA family takes with an additive mask: the two-pass kernel sums in another order
-        assert path_add == sms.SMS_PATH_CTA and path_bool == sms.SMS_PATH_ONLINE
+    else:
         H.check_all_rows(w, inp, y_add, None, name + " additive")
     del inp, y, y_add, mb
     torch.cuda.empty_cache()

@@ -446,3 +446,42 @@ def test_full_size_workload(name):
     assert chk.rows == w.rows
     del inp, y, dx
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("direction", ["forward", "backward"])
+def test_ring_wait_that_runs_out_reports_and_recovers(direction):
+    """The bounded-wait abort path, run on the GPU without a fault: with the
+    test control on, each ring group's first wait is on a barrier nothing
+    arrives at (bounded at 0.2 ms).  The kernel records SMS_DEVERR_RING_WAIT,
+    drains its own bulk copies and returns; the error word reads once and
+    clears, and the next call (control off) is correct."""
+    w = _wl(2048, "f16", 900, mask="none", causal=True, seed=29)
+    inp = H.make(w)
+    st = torch.cuda.current_stream().cuda_stream
+    y_ok = None
+    if direction == "backward":
+        with H.forced_path("ring"):
+            y_ok = H.raw_forward(inp, w)
+        torch.cuda.synchronize()
+    prev = sms.sms_set_test_stall(200_000)
+    try:
+        with H.forced_path("ring"):
+            if direction == "forward":
+                H.raw_forward(inp, w)
+            else:
+                H.raw_backward(y_ok, inp["dy"], w, causal_hint=True)
+        torch.cuda.synchronize()
+        assert sms.sms_device_error(st) == 3  # SMS_DEVERR_RING_WAIT
+    finally:
+        sms.sms_set_test_stall(prev)
+    assert sms.sms_device_error(st) == 0  # read once, then clear
+    with H.forced_path("ring"):
+        if direction == "forward":
+            y = H.raw_forward(inp, w)
+            torch.cuda.synchronize()
+            H.check_forward(H.to_np64(y), H.oracle_forward(inp, w), torch.float16, "ring after a stall")
+        else:
+            dx = H.raw_backward(y_ok, inp["dy"], w, causal_hint=True)
+            torch.cuda.synchronize()
+            H.check_backward(H.to_np64(dx), y_ok.cpu(), inp["dy"].cpu(), w.scale, torch.float16, "ring bwd after a stall")
+    assert sms.sms_device_error(st) == 0
