@@ -277,21 +277,28 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
         const int64_t mbase = (int64_t)bidx * a.msb + (int64_t)hidx * a.msh + j;
         const int64_t row0 = (int64_t)bh * a.S;
         bool ok = true;
+        // lse and delta of a query block: loaded one block ahead by threads
+        // mt < 128 (one query each), so the global loads are off the block's path
+        float lse_n = 0.f, del_n = 0.f;
+        auto fetch = [&](int n) {
+            const int i = (qb0 + n) * kBN + mt;
+            lse_n = neg_inf();
+            del_n = 0.f;
+            if (mt < kBN && n < npair && i < a.S) {
+                lse_n = a.lse_in[row0 + i];
+                del_n = a.delta[row0 + i];
+            }
+        };
+        fetch(0);
         for (int n = 0; n < npair; ++n) {
             const int i0 = (qb0 + n) * kBN;
             // this block's lse (log2 units; +inf where the row has no kept key, or beyond S) and delta
             if (mt < kBN) {
-                const int i = i0 + mt;
-                float l2 = __int_as_float(0x7f800000), dl = 0.f;
-                if (i < a.S) {
-                    const float lse = a.lse_in[row0 + i];
-                    l2 = (lse == neg_inf()) ? __int_as_float(0x7f800000) : lse * kLog2e;
-                    dl = a.delta[row0 + i];
-                }
-                s_lse[mt] = l2;
-                s_del[mt] = dl;
+                s_lse[mt] = (lse_n == neg_inf()) ? __int_as_float(0x7f800000) : lse_n * kLog2e;
+                s_del[mt] = del_n;
             }
             named_sync(1, kMath);
+            fetch(n + 1);
             const bool pred = !key_ok || (i0 + kBN > a.S) || (a.causal && j0 + kBM - 1 > i0);
             if (!warp_wait(&b.s_full, (uint32_t)(n & 1), b, a.err)) { ok = false; break; }
             tc::fence_after_sync();
