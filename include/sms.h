@@ -244,7 +244,8 @@ SMS_API int sms_attention_forward(const void *q, const void *k, const void *v, c
  *                   buffer
  *   workspace       caller-owned device scratch of at least
  *                   sms_attention_backward_workspace() bytes, 16-byte aligned
- *                   (an fp32 dQ accumulator and an fp32 value per query row);
+ *                   (an fp32 dQ accumulator padded to whole blocks of 128
+ *                   queries, and an fp32 value per query row);
  *                   its contents on entry do not matter, and it must not be
  *                   used by anything else until the call's kernels are done
  * Three kernels are enqueued on `stream`.  Arithmetic: the five products on

@@ -30,9 +30,18 @@ struct AttnArgs {
     const void *o_in, *dout;
     const float *lse_in;
     void *dq, *dk, *dv;
-    float *dq_acc;         // [B, H, S, D] fp32 scratch (zeroed by the backward before use)
+    float *dq_acc;         // fp32 scratch of attn_bwd_acc_rows() x D (zeroed by the backward before use): one
+                           // tile per (batch, head, block of kAttnBwdQueryBlock queries), element (r, c) of a
+                           // tile at float ((c / 4) * kAttnBwdQueryBlock + r) * 4 + c % 4
     float *delta;          // [B, H, S] fp32 scratch: rowsum(dO * O)
 };
+
+// Queries per block of the backward; its dQ accumulator holds whole blocks.
+constexpr int kAttnBwdQueryBlock = 128;
+inline int64_t attn_bwd_acc_rows(int64_t B, int64_t H, int64_t S)
+{
+    return B * H * ((S + kAttnBwdQueryBlock - 1) / kAttnBwdQueryBlock) * kAttnBwdQueryBlock;
+}
 
 // Head dimensions the tensor-core kernels take.
 inline bool attn_head_dim_ok(int d) { return d == 64 || d == 128; }

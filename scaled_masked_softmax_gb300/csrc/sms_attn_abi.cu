@@ -122,8 +122,8 @@ int sms_attention_forward(const void *q, const void *k, const void *v, const voi
 int64_t sms_attention_backward_workspace(int64_t batch, int64_t heads, int64_t seq, int64_t head_dim)
 {
     if (batch < 0 || heads < 0 || seq < 0 || head_dim < 0) return -1;
-    const int64_t rows = batch * heads * seq;
-    return rows * head_dim * 4 + rows * 4;  // fp32 dQ accumulator, then fp32 delta per query row
+    // fp32 dQ accumulator in whole query blocks, then fp32 delta per query row
+    return attn_bwd_acc_rows(batch, heads, seq) * head_dim * 4 + batch * heads * seq * 4;
 }
 
 int sms_attention_backward(const void *q, const void *k, const void *v, const void *o, const void *d_o,
@@ -177,7 +177,7 @@ int sms_attention_backward(const void *q, const void *k, const void *v, const vo
     a.o_in = o; a.dout = d_o; a.lse_in = lse;
     a.dq = dq; a.dk = dk; a.dv = dv;
     a.dq_acc = static_cast<float *>(workspace);
-    a.delta = reinterpret_cast<float *>(static_cast<char *>(workspace) + batch * heads * seq * head_dim * 4);
+    a.delta = reinterpret_cast<float *>(static_cast<char *>(workspace) + attn_bwd_acc_rows(batch, heads, seq) * head_dim * 4);
     const char *step = nullptr;
     e = launch_attn_bwd(a, static_cast<cudaStream_t>(stream), &step);
     if (e == cudaSuccess) {  // three kernels: delta, the main pass, dQ

@@ -14,16 +14,22 @@
 //   2. attn_bwd_kernel: one CTA per (batch, head, block of 128 keys) walks the
 //      query blocks (those at or after its keys under causal).  Per block:
 //        S^T = K Q^T and dP^T = V dO^T on tcgen05 into TMEM (keys in lanes);
-//        128 threads (one key each) form P^T and dS^T as 16-bit values in
+//        256 threads (two per key) form P^T and dS^T as 16-bit values in
 //        shared memory in the MMA's swizzled layout;
 //        dV += P^T dO and dK += dS^T Q accumulate in TMEM; dQ_blk = dS K goes
-//        to TMEM (reusing the S^T columns) and the same threads, now one query
-//        row each, add it to the fp32 accumulator with vector reductions.
+//        to TMEM (reusing the dP^T columns); the same threads, now one query
+//        row each, copy it into shared memory (the P^T / dS^T area, which the
+//        products have finished with), and one thread hands the whole tile to
+//        the TMA unit as a single bulk add into the fp32 accumulator, which
+//        runs while the next block is computed.
 //      At the end dK and dV leave TMEM once, rounded to the 16-bit dtype;
 //   3. attn_bwd_post: dQ = the accumulator rounded to the 16-bit dtype.
-// Roles: warp 0 one lane issues the TMA loads (K and V once, Q and dO per
-// query block), warp 1 one lane the MMAs (and owns TMEM), warps 2..5 the
-// element-wise work.  Every mbarrier wait is bounded (2 s) as in the forward.
+// Roles: warp 0 one lane issues the TMA loads (K and V once; dO and Q of each
+// query block through a ring of tile slots, so that they arrive a block
+// ahead), warp 1 one lane the MMAs (and owns TMEM), warps 2..9 the
+// element-wise work.  The next block's S^T product is issued before this
+// block's dQ has left TMEM (they use different columns), so it overlaps the
+// dQ copy.  Every mbarrier wait is bounded (2 s) as in the forward.
 #include <cuda.h>
 
 #include <atomic>
@@ -40,33 +46,39 @@ cudaError_t attn_tensor_map(CUtensorMap *m, const void *base, int dtype, int BH,
 namespace {
 
 constexpr int kBM = 128;          // keys per CTA (the MMA's M for S^T, dP^T, dV, dK)
-constexpr int kBN = 128;          // queries per block
+constexpr int kBN = kAttnBwdQueryBlock;  // queries per block (128)
 constexpr int kThreads = 320;     // warps 0 (TMA), 1 (MMA), 2..9 (element-wise: two warps per TMEM lane quarter)
 constexpr int kMath = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAtom = 16384;
 
 template <int D> struct BwdCfg {
-    static constexpr int NST = D == 128 ? 1 : 2;          // Q / dO stages
+    // dO and Q tiles of the query blocks in order (dO(n), Q(n), dO(n+1), ...)
+    // through a ring of NSLOT slots
+    static constexpr int NSLOT = D == 128 ? 3 : 4;
     static constexpr uint32_t TILE = (D / 64) * kAtom;    // 128 x D
     static constexpr uint32_t SQ = 2 * kAtom;             // 128 x 128 (P^T, dS^T)
     static constexpr uint32_t OFF_K = 0;
     static constexpr uint32_t OFF_V = OFF_K + TILE;
-    static constexpr uint32_t OFF_Q = OFF_V + TILE;
-    static constexpr uint32_t OFF_DO = OFF_Q + NST * TILE;
-    static constexpr uint32_t OFF_P = OFF_DO + NST * TILE;
+    static constexpr uint32_t OFF_R = OFF_V + TILE;
+    static constexpr uint32_t OFF_P = OFF_R + NSLOT * TILE;
     static constexpr uint32_t OFF_DS = OFF_P + SQ;
     static constexpr uint32_t OFF_LSE = OFF_DS + SQ;       // 128 floats: lse * log2e (+inf: fully masked)
     static constexpr uint32_t OFF_DEL = OFF_LSE + 512;     // 128 floats: delta
     static constexpr uint32_t OFF_BAR = OFF_DEL + 512;
     static constexpr uint32_t BAR_BYTES = 512;
     static constexpr uint32_t SMEM = OFF_BAR + BAR_BYTES + 1024;
-    static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 256 + D, COL_DQ = 0;
+    static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 256 + D, COL_DQ = 128;
+    // one block's dQ in fp32, staged over P^T and dS^T: element (query r, column c)
+    // at byte ((c / 4) * 128 + r) * 16 + (c % 4) * 4, the accumulator's tile layout
+    static constexpr uint32_t DQ_BYTES = kBN * D * 4;
+    static_assert(DQ_BYTES <= 2 * SQ && OFF_DS == OFF_P + SQ, "dQ staging area");
+    static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
 struct BwdBars {
     uint64_t kv_full;
-    uint64_t q_full[2], q_empty[2];
+    uint64_t r_full[4], r_empty[4];
     uint64_t s_full, ds_full, dq_full, dq_free;
     uint64_t mma_drain;
     uint32_t tmem_base;
@@ -137,7 +149,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo, const AttnArgs a)
 {
     using C = BwdCfg<D>;
-    constexpr int NST = C::NST;
+    constexpr int NS = C::NSLOT;
     constexpr int FMT = AbFmt<T>::v;
     constexpr uint32_t IDESC_SQ = tc::idesc_f16(FMT, 0, kBM, kBN);          // S^T, dP^T: K-major A and B
     constexpr uint32_t IDESC_ACC = tc::idesc_f16(FMT, 1, kBM, D);           // dV, dK: K-major A, MN-major B
@@ -164,9 +176,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
 
     if (threadIdx.x == 0) {
         mbar_init(&b.kv_full, 1);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&b.q_full[s], 1);
-            mbar_init(&b.q_empty[s], 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&b.r_full[s], 1);
+            mbar_init(&b.r_empty[s], 1);
         }
         mbar_init(&b.s_full, 1);
         mbar_init(&b.ds_full, kMath);
@@ -195,21 +207,21 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 tc::tma_load_3d(smem + C::OFF_K + at * kAtom, &tmk, at * 64, j0, bh, &b.kv_full);
                 tc::tma_load_3d(smem + C::OFF_V + at * kAtom, &tmv, at * 64, j0, bh, &b.kv_full);
             }
+            // tile u: dO (u even) or Q (u odd) of query block qb0 + u / 2, into slot u % NS
             int armed = 0;
-            for (int n = 0; n < npair; ++n) {
-                const int st = n % NST, i0 = (qb0 + n) * kBN;
-                if (n >= NST && !wait_or_flag(&b.q_empty[st], (uint32_t)((n / NST - 1) & 1), b, a.err)) break;
+            for (int u = 0; u < 2 * npair; ++u) {
+                const int sl = u % NS, i0 = (qb0 + (u >> 1)) * kBN;
+                if (u >= NS && !wait_or_flag(&b.r_empty[sl], (uint32_t)((u / NS - 1) & 1), b, a.err)) break;
                 if (*reinterpret_cast<volatile int *>(&b.abort)) break;
-                mbar_arrive_expect_tx(&b.q_full[st], 2 * C::TILE);
+                const CUtensorMap *m = (u & 1) ? &tmq : &tmdo;
+                mbar_arrive_expect_tx(&b.r_full[sl], C::TILE);
 #pragma unroll
-                for (int at = 0; at < D / 64; ++at) {
-                    tc::tma_load_3d(smem + C::OFF_Q + st * C::TILE + at * kAtom, &tmq, at * 64, i0, bh, &b.q_full[st]);
-                    tc::tma_load_3d(smem + C::OFF_DO + st * C::TILE + at * kAtom, &tmdo, at * 64, i0, bh, &b.q_full[st]);
-                }
-                armed = n + 1;
+                for (int at = 0; at < D / 64; ++at)
+                    tc::tma_load_3d(smem + C::OFF_R + sl * C::TILE + at * kAtom, m, at * 64, i0, bh, &b.r_full[sl]);
+                armed = u + 1;
             }
             drain_wait(&b.kv_full, 0);
-            for (int n = (armed > NST ? armed - NST : 0); n < armed; ++n) drain_wait(&b.q_full[n % NST], (uint32_t)((n / NST) & 1));
+            for (int u = (armed > NS ? armed - NS : 0); u < armed; ++u) drain_wait(&b.r_full[u % NS], (uint32_t)((u / NS) & 1));
         }
     } else if (warp == 1) {
         // ----------------------------------------------------------- MMAs ---
@@ -218,11 +230,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             const uint32_t k_addr = s_base + C::OFF_K, v_addr = s_base + C::OFF_V;
             const uint32_t p_addr = s_base + C::OFF_P, ds_addr = s_base + C::OFF_DS;
             for (int n = 0; ok && n < npair; ++n) {
-                const int st = n % NST;
-                const uint32_t q_addr = s_base + C::OFF_Q + st * C::TILE, do_addr = s_base + C::OFF_DO + st * C::TILE;
-                if (!wait_or_flag(&b.q_full[st], (uint32_t)((n / NST) & 1), b, a.err)) { ok = false; break; }
-                // S^T shares its columns with the previous block's dQ: drained first
-                if (n >= 1 && !wait_or_flag(&b.dq_free, (uint32_t)((n - 1) & 1), b, a.err)) { ok = false; break; }
+                const int ud = 2 * n, uq = 2 * n + 1;  // ring tiles of dO(n) and Q(n)
+                const int sd = ud % NS, sq = uq % NS;
+                const uint32_t q_addr = s_base + C::OFF_R + sq * C::TILE, do_addr = s_base + C::OFF_R + sd * C::TILE;
+                // S^T: its columns were read out before the previous ds_full
+                if (!wait_or_flag(&b.r_full[sq], (uint32_t)((uq / NS) & 1), b, a.err)) { ok = false; break; }
                 tc::fence_after_sync();
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
@@ -230,6 +242,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                     tc::mma_f16(tmem + C::COL_S, tc::desc_sw128(k_addr + ko, 16, 1024), tc::desc_sw128(q_addr + ko, 16, 1024),
                                 IDESC_SQ, k > 0 ? 1u : 0u);
                 }
+                // dP^T shares its columns with the previous block's dQ: drained first
+                if (!wait_or_flag(&b.r_full[sd], (uint32_t)((ud / NS) & 1), b, a.err)) { ok = false; break; }
+                if (n >= 1 && !wait_or_flag(&b.dq_free, (uint32_t)((n - 1) & 1), b, a.err)) { ok = false; break; }
+                tc::fence_after_sync();
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t ko = (k / 4) * kAtom + (k % 4) * 32;
@@ -239,16 +255,17 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 tc::commit(&b.s_full);
                 if (!wait_or_flag(&b.ds_full, (uint32_t)(n & 1), b, a.err)) { ok = false; break; }
                 tc::fence_after_sync();
+                // K-major slice k of P^T / dS^T at (k / 4) * kAtom + (k % 4) * 32; MN-major slice of dO / Q at k * 2048
 #pragma unroll
-                for (int k = 0; k < kBN / 16; ++k) {
-                    const uint32_t ka = (k / 4) * kAtom + (k % 4) * 32;  // K-major slice of P^T / dS^T
-                    const uint32_t kb_ = k * 2048;                      // MN-major slice of dO / Q
-                    const uint32_t acc = (n > 0 || k > 0) ? 1u : 0u;
-                    tc::mma_f16(tmem + C::COL_DV, tc::desc_sw128(p_addr + ka, 16, 1024),
-                                tc::desc_sw128(do_addr + kb_, kAtom, 1024), IDESC_ACC, acc);
-                    tc::mma_f16(tmem + C::COL_DK, tc::desc_sw128(ds_addr + ka, 16, 1024),
-                                tc::desc_sw128(q_addr + kb_, kAtom, 1024), IDESC_ACC, acc);
-                }
+                for (int k = 0; k < kBN / 16; ++k)
+                    tc::mma_f16(tmem + C::COL_DV, tc::desc_sw128(p_addr + (k / 4) * kAtom + (k % 4) * 32, 16, 1024),
+                                tc::desc_sw128(do_addr + k * 2048, kAtom, 1024), IDESC_ACC, (n > 0 || k > 0) ? 1u : 0u);
+                tc::commit(&b.r_empty[sd]);
+#pragma unroll
+                for (int k = 0; k < kBN / 16; ++k)
+                    tc::mma_f16(tmem + C::COL_DK, tc::desc_sw128(ds_addr + (k / 4) * kAtom + (k % 4) * 32, 16, 1024),
+                                tc::desc_sw128(q_addr + k * 2048, kAtom, 1024), IDESC_ACC, (n > 0 || k > 0) ? 1u : 0u);
+                tc::commit(&b.r_empty[sq]);
 #pragma unroll
                 for (int k = 0; k < kBM / 16; ++k) {
                     // dQ = dS K: A = dS (queries x keys) read MN-major from dS^T, B = K MN-major
@@ -256,7 +273,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                                 tc::desc_sw128(k_addr + k * 2048, kAtom, 1024), IDESC_DQ, k > 0 ? 1u : 0u);
                 }
                 tc::commit(&b.dq_full);
-                tc::commit(&b.q_empty[st]);
             }
             tc::commit(&b.mma_drain);
             drain_wait(&b.mma_drain, 0);
@@ -293,14 +309,18 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
         for (int n = 0; n < npair; ++n) {
             const int i0 = (qb0 + n) * kBN;
             // this block's lse (log2 units; +inf where the row has no kept key, or beyond S) and delta
+            // (every thread finished reading the previous block's at the dQ barrier below)
             if (mt < kBN) {
                 s_lse[mt] = (lse_n == neg_inf()) ? __int_as_float(0x7f800000) : lse_n * kLog2e;
                 s_del[mt] = del_n;
             }
-            named_sync(1, kMath);
             fetch(n + 1);
             const bool pred = !key_ok || (i0 + kBN > a.S) || (a.causal && j0 + kBM - 1 > i0);
             if (!warp_wait(&b.s_full, (uint32_t)(n & 1), b, a.err)) { ok = false; break; }
+            // the previous block's dQ has left the P^T / dS^T area before it is overwritten
+            if (mt == 0) tc::bulk_wait_read();
+            __syncwarp();
+            named_sync(1, kMath);
             tc::fence_after_sync();
 #pragma unroll
             for (int cc = 0; cc < kBN / 64; ++cc) {
@@ -341,27 +361,35 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             tc::fence_before_sync();
             tc::fence_async_smem();
             mbar_arrive(&b.ds_full);
-            // this block's dQ (lane t = query i0 + t) into the fp32 accumulator
+            // this block's dQ (lane t = query i0 + t) out of TMEM, staged in shared memory in the
+            // accumulator's tile layout (a warp's 32 queries fill 512 contiguous bytes per 4 columns)
             if (!warp_wait(&b.dq_full, (uint32_t)(n & 1), b, a.err)) { ok = false; break; }
             tc::fence_after_sync();
-            const int iq = i0 + t;
-            float *acc = a.dq_acc + (row0 + iq) * D;
+            uint32_t v[D / 64][32];
+#pragma unroll
+            for (int cc = 0; cc < D / 64; ++cc) tc::tmem_ld32(tl + C::COL_DQ + (half * (D / 64) + cc) * 32, v[cc]);
+            tc::tmem_wait_ld();
+            tc::fence_before_sync();
+            mbar_arrive(&b.dq_free);
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc) {
                 const int c = half * (D / 64) + cc;  // this warp's 32-column chunks of dQ
-                uint32_t v[32];
-                tc::tmem_ld32(tl + C::COL_DQ + c * 32, v);
-                tc::tmem_wait_ld();
-                if (iq < a.S) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        tc::red_add_v4(acc + c * 32 + e, __uint_as_float(v[e]), __uint_as_float(v[e + 1]),
-                                       __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
-                }
+                for (int g = 0; g < 8; ++g)
+                    *reinterpret_cast<uint4 *>(smem + C::OFF_P + ((c * 8 + g) * kBN + t) * 16) =
+                        make_uint4(v[cc][4 * g], v[cc][4 * g + 1], v[cc][4 * g + 2], v[cc][4 * g + 3]);
             }
-            tc::fence_before_sync();
-            mbar_arrive(&b.dq_free);
+            tc::fence_async_smem();
+            named_sync(2, kMath);
+            // one bulk add of the whole tile into the accumulator, by the TMA unit
+            if (mt == 0) {
+                tc::bulk_reduce_add_f32(a.dq_acc + ((int64_t)bh * nqb + qb0 + n) * (kBN * D), s_base + C::OFF_P,
+                                        C::DQ_BYTES);
+                tc::bulk_commit();
+            }
         }
+        // the last bulk adds have finished before the CTA's shared memory is released
+        if (mt == 0) tc::bulk_wait_all();
         if (ok) {
             // dK and dV of this CTA's keys (the last dq_full covered every MMA)
             tc::fence_after_sync();
@@ -400,13 +428,17 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
     }
 }
 
-// delta[r] = sum_d dO[r, d] * O[r, d] (fp32), and the dQ accumulator row
-// cleared: one warp per query row.
+// The dQ accumulator cleared (D floats per warp, acc_rows warps), and
+// delta[r] = sum_d dO[r, d] * O[r, d] (fp32) by warp r for each of the `rows`
+// query rows.
 template <typename T, int D>
-__global__ void __launch_bounds__(256) attn_bwd_pre(const AttnArgs a, int64_t rows)
+__global__ void __launch_bounds__(256) attn_bwd_pre(const AttnArgs a, int64_t rows, int64_t acc_rows)
 {
     const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
+    if (r >= acc_rows) return;
+    float4 *acc = reinterpret_cast<float4 *>(a.dq_acc + r * D);
+    for (int e = lane; e < D / 4; e += 32) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (r >= rows) return;
     const T *o = reinterpret_cast<const T *>(a.o_in) + r * D;
     const T *g = reinterpret_cast<const T *>(a.dout) + r * D;
@@ -415,20 +447,29 @@ __global__ void __launch_bounds__(256) attn_bwd_pre(const AttnArgs a, int64_t ro
     for (int e = lane; e < D; e += 32) s = fmaf(to_f32<T>(o[e]), to_f32<T>(g[e]), s);
     s = group_sum<32>(s);
     if (lane == 0) a.delta[r] = s;
-    float4 *acc = reinterpret_cast<float4 *>(a.dq_acc + r * D);
-    for (int e = lane; e < D / 4; e += 32) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// dQ = the fp32 accumulator rounded to T, 8 elements per thread.
-template <typename T>
-__global__ void __launch_bounds__(256) attn_bwd_post(const AttnArgs a, int64_t n8)
+// dQ = the fp32 accumulator rounded to T: each thread 8 columns of one query
+// row, a warp 4 rows x 8 column groups (64-byte runs read from the tile
+// layout, 128-byte runs written to dQ's rows).
+template <typename T, int D>
+__global__ void __launch_bounds__(256) attn_bwd_post(const AttnArgs a, int64_t units)
 {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n8) return;
-    const float4 *acc = reinterpret_cast<const float4 *>(a.dq_acc) + 2 * i;
-    const float4 u = acc[0], v = acc[1];
+    const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (g >= units) return;
+    constexpr int per_tile = kBN * D / 8;
+    const int64_t tile = g / per_tile;
+    const int w = (int)(g - tile * per_tile), wi = w >> 5, lane = w & 31;
+    const int r = (wi / (D / 64)) * 4 + (lane & 3);       // query within the block
+    const int cg = (wi % (D / 64)) * 8 + (lane >> 2);     // 8-column group
+    const int nqb = (a.S + kBN - 1) / kBN;
+    const int64_t bh = tile / nqb;
+    const int i = (int)(tile - bh * nqb) * kBN + r;
+    if (i >= a.S) return;
+    const float4 *acc = reinterpret_cast<const float4 *>(a.dq_acc) + tile * (kBN * D / 4);
+    const float4 u = acc[(2 * cg) * kBN + r], v = acc[(2 * cg + 1) * kBN + r];
     const float f[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
-    st_stream(reinterpret_cast<T *>(a.dq) + 8 * i, pack<T>(f));
+    st_stream(reinterpret_cast<T *>(a.dq) + (bh * a.S + i) * D + cg * 8, pack<T>(f));
 }
 
 template <typename T, int D, int MK>
@@ -460,8 +501,9 @@ cudaError_t launch_all(const AttnArgs &a, const CUtensorMap &tq, const CUtensorM
                        const CUtensorMap &tdo, cudaStream_t st, const char **step)
 {
     const int64_t rows = (int64_t)a.B * a.H * a.S;
+    const int64_t acc_rows = attn_bwd_acc_rows(a.B, a.H, a.S);
     *step = "delta kernel";
-    attn_bwd_pre<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(a, rows);
+    attn_bwd_pre<T, D><<<(unsigned)((acc_rows + 7) / 8), 256, 0, st>>>(a, rows, acc_rows);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     *step = "main backward kernel";
@@ -470,8 +512,8 @@ cudaError_t launch_all(const AttnArgs &a, const CUtensorMap &tq, const CUtensorM
     else e = launch_main<T, D, 1>(a, tq, tk, tv, tdo, st);
     if (e != cudaSuccess) return e;
     *step = "dQ kernel";
-    const int64_t n8 = rows * D / 8;
-    attn_bwd_post<T><<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>(a, n8);
+    const int64_t units = acc_rows * D / 8;
+    attn_bwd_post<T, D><<<(unsigned)((units + 255) / 256), 256, 0, st>>>(a, units);
     return cudaGetLastError();
 }
 

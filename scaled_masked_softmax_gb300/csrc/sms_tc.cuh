@@ -133,12 +133,20 @@ __device__ __forceinline__ void prefetch_tmap(const void *tmap)
     asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
-// Four fp32 values added to global memory (one vector reduction; addr 16-byte aligned).
-__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d)
+// `bytes` of fp32 in shared memory added element-wise to global memory by the
+// TMA unit (both addresses 16-byte aligned, bytes a multiple of 16), in the
+// issuing thread's current bulk group.  The shared source stays in use until
+// bulk_wait_read() returns.
+__device__ __forceinline__ void bulk_reduce_add_f32(float *gdst, uint32_t s_src, uint32_t bytes)
 {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" :: "l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;"
+                 :: "l"(gdst), "r"(s_src), "r"(bytes) : "memory");
 }
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// every committed bulk group of this thread has finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// every committed bulk group of this thread has finished
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Shared-memory writes by ordinary stores become visible to the tensor-core
 // and TMA (async proxy) reads that follow a barrier.

@@ -308,8 +308,9 @@ def _attn_bwd(**kw):
 
 
 def test_attention_backward_workspace_size():
-    # an fp32 dQ accumulator plus one fp32 per query row
-    assert binding.lib().sms_attention_backward_workspace(2, 3, 5, 64) == 2 * 3 * 5 * 64 * 4 + 2 * 3 * 5 * 4
+    # the fp32 dQ accumulator in whole blocks of 128 queries, then one fp32 per query row
+    assert binding.lib().sms_attention_backward_workspace(2, 3, 5, 64) == 2 * 3 * 128 * 64 * 4 + 2 * 3 * 5 * 4
+    assert binding.lib().sms_attention_backward_workspace(1, 2, 300, 128) == 2 * 384 * 128 * 4 + 2 * 300 * 4
     assert binding.lib().sms_attention_backward_workspace(-1, 3, 5, 64) == -1
 
 
