@@ -49,6 +49,7 @@ constexpr int kBM = 128;          // keys per CTA (the MMA's M for S^T, dP^T, dV
 constexpr int kBN = kAttnBwdQueryBlock;  // queries per block (128)
 constexpr int kThreads = 320;     // warps 0 (TMA), 1 (MMA), 2..9 (element-wise: two warps per TMEM lane quarter)
 constexpr int kMath = 256;
+constexpr int kHeadGroup = 8;     // heads whose CTAs are scheduled together
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAtom = 16384;
 
@@ -79,7 +80,7 @@ template <int D> struct BwdCfg {
 struct BwdBars {
     uint64_t kv_full;
     uint64_t r_full[4], r_empty[4];
-    uint64_t s_full, ds_full, dq_full, dq_free;
+    uint64_t s_full, ds_full, dq_full, dq_free, stage_free;
     uint64_t mma_drain;
     uint32_t tmem_base;
     int abort;
@@ -143,6 +144,44 @@ __device__ __forceinline__ void mask_col(const AttnArgs &a, int64_t mbase, int i
     }
 }
 
+// P^T and dS^T of one 32-query chunk c for this thread's key j (TMEM lane):
+// sv / dv hold S^T and dP^T of queries c*32 .. c*32+31, s_lse their lse in
+// log2 units (+inf: no kept key), s_dsc their delta * scale; pk / dk get the
+// results as 16-bit pairs in query order.  PR: the chunk may hold positions
+// that are masked out by position (causal diagonal, keys or queries past S).
+template <typename T, int MK, bool PR>
+__device__ __forceinline__ void p_ds_chunk(const AttnArgs &a, const uint32_t (&sv)[32], const uint32_t (&dv)[32],
+                                           const float (&m2)[32], const float *s_lse, const float *s_dsc, int c,
+                                           int i0, int j, bool key_ok, float sl2, uint32_t (&pk)[16],
+                                           uint32_t (&dk)[16])
+{
+    const float4 *l4 = reinterpret_cast<const float4 *>(s_lse + c * 32);
+    const float4 *g4 = reinterpret_cast<const float4 *>(s_dsc + c * 32);
+#pragma unroll
+    for (int e4 = 0; e4 < 8; ++e4) {
+        const float4 L = l4[e4], G = g4[e4];
+        const float lq[4] = {L.x, L.y, L.z, L.w}, gq[4] = {G.x, G.y, G.z, G.w};
+        float p[4], ds[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = 4 * e4 + u;
+            // log2 of P: S * scale * log2e + mask - lse (one rounding without a mask)
+            float x = MK == 0 ? fmaf(__uint_as_float(sv[e]), sl2, -lq[u])
+                              : fmaf(__uint_as_float(sv[e]), sl2, m2[e]) - lq[u];
+            if constexpr (PR) {
+                const int i = i0 + c * 32 + e;
+                if (!key_ok || i >= a.S || (a.causal && j > i)) x = neg_inf();
+            }
+            p[u] = ex2(x);
+            ds[u] = p[u] * fmaf(__uint_as_float(dv[e]), a.scale, -gq[u]);  // scale * P * (dP - delta)
+        }
+        pk[2 * e4] = pack2(p[0], p[1], static_cast<T *>(nullptr));
+        pk[2 * e4 + 1] = pack2(p[2], p[3], static_cast<T *>(nullptr));
+        dk[2 * e4] = pack2(ds[0], ds[1], static_cast<T *>(nullptr));
+        dk[2 * e4 + 1] = pack2(ds[2], ds[3], static_cast<T *>(nullptr));
+    }
+}
+
 template <typename T, int D, int MK>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -161,14 +200,20 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
     BwdBars &b = *reinterpret_cast<BwdBars *>(smem + C::OFF_BAR);
     const uint32_t s_base = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
     float *s_lse = reinterpret_cast<float *>(smem + C::OFF_LSE);
-    float *s_del = reinterpret_cast<float *>(smem + C::OFF_DEL);
+    float *s_dsc = reinterpret_cast<float *>(smem + C::OFF_DEL);  // delta * scale per query of the block
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int BH = a.B * a.H;
     const int nkb = (a.S + kBM - 1) / kBM;
-    // causal: key block 0 sees every query block, the last one only its own; heaviest first
-    const int kb = a.causal ? (int)(blockIdx.x / (unsigned)BH) : nkb - 1 - (int)(blockIdx.x / (unsigned)BH);
-    const int bh = (int)(blockIdx.x % (unsigned)BH);
+    // CTAs in groups of kHeadGroup heads, so that the CTAs running at one time
+    // share few heads: the group's fp32 dQ accumulator, Q and dO stay in L2.
+    // Inside a group, key blocks in order (under causal, key block 0 sees every
+    // query block and the last only its own: heaviest first), then heads.
+    const int grp = (int)(blockIdx.x / (unsigned)(kHeadGroup * nkb));
+    const int gsz = min(kHeadGroup, BH - grp * kHeadGroup);
+    const int rk = (int)(blockIdx.x - (unsigned)(grp * kHeadGroup * nkb));
+    const int kb = a.causal ? rk / gsz : nkb - 1 - rk / gsz;
+    const int bh = grp * kHeadGroup + rk % gsz;
     const int j0 = kb * kBM;
     const int nqb = (a.S + kBN - 1) / kBN;
     const int qb0 = a.causal ? j0 / kBN : 0;  // query blocks before the keys see none of them
@@ -181,9 +226,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             mbar_init(&b.r_empty[s], 1);
         }
         mbar_init(&b.s_full, 1);
-        mbar_init(&b.ds_full, kMath);
+        mbar_init(&b.ds_full, kMath / 32);   // one arrival per element-wise warp
         mbar_init(&b.dq_full, 1);
-        mbar_init(&b.dq_free, kMath);
+        mbar_init(&b.dq_free, kMath / 32);
+        mbar_init(&b.stage_free, 1);
         mbar_init(&b.mma_drain, 1);
         b.abort = 0;
         fence_mbar_init();
@@ -312,16 +358,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             // (every thread finished reading the previous block's at the dQ barrier below)
             if (mt < kBN) {
                 s_lse[mt] = (lse_n == neg_inf()) ? __int_as_float(0x7f800000) : lse_n * kLog2e;
-                s_del[mt] = del_n;
+                s_dsc[mt] = del_n * a.scale;
             }
+            named_sync(1, kMath);
             fetch(n + 1);
             const bool pred = !key_ok || (i0 + kBN > a.S) || (a.causal && j0 + kBM - 1 > i0);
             if (!warp_wait(&b.s_full, (uint32_t)(n & 1), b, a.err)) { ok = false; break; }
-            // the previous block's dQ has left the P^T / dS^T area before it is overwritten
-            if (mt == 0) tc::bulk_wait_read();
-            __syncwarp();
-            named_sync(1, kMath);
             tc::fence_after_sync();
+            bool staged = true;
 #pragma unroll
             for (int cc = 0; cc < kBN / 64; ++cc) {
                 const int c = half * (kBN / 64) + cc;  // this warp's 32-query chunks
@@ -332,22 +376,17 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 tc::tmem_ld32(tl + C::COL_DP + c * 32, dv);
                 tc::tmem_wait_ld();
                 uint32_t pk[16], dk[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float p[2], ds[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int q = c * 32 + e + u;  // query within the block
-                        float s = fmaf(__uint_as_float(sv[e + u]), sl2, m2[e + u]);
-                        if (pred) {
-                            const int i = i0 + q;
-                            if (!key_ok || i >= a.S || (a.causal && j > i)) s = neg_inf();
-                        }
-                        p[u] = ex2(s - s_lse[q]);
-                        ds[u] = p[u] * (__uint_as_float(dv[e + u]) - s_del[q]) * a.scale;
+                if (pred) p_ds_chunk<T, MK, true>(a, sv, dv, m2, s_lse, s_dsc, c, i0, j, key_ok, sl2, pk, dk);
+                else p_ds_chunk<T, MK, false>(a, sv, dv, m2, s_lse, s_dsc, c, i0, j, key_ok, sl2, pk, dk);
+                if (cc == 0 && n > 0) {
+                    // the previous block's dQ has left the P^T / dS^T area (its bulk add has read
+                    // it) before the first store here; the wait overlaps the first chunk's arithmetic
+                    if (mt == 0) {
+                        tc::bulk_wait_read();
+                        mbar_arrive(&b.stage_free);
                     }
-                    pk[e / 2] = pack2(p[0], p[1], static_cast<T *>(nullptr));
-                    dk[e / 2] = pack2(ds[0], ds[1], static_cast<T *>(nullptr));
+                    __syncwarp();
+                    if (!warp_wait(&b.stage_free, (uint32_t)((n - 1) & 1), b, a.err)) { staged = false; break; }
                 }
                 unsigned char *pa = smem + C::OFF_P + (c / 2) * kAtom;
                 unsigned char *da = smem + C::OFF_DS + (c / 2) * kAtom;
@@ -358,9 +397,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                     *reinterpret_cast<uint4 *>(da + off) = make_uint4(dk[4 * q4], dk[4 * q4 + 1], dk[4 * q4 + 2], dk[4 * q4 + 3]);
                 }
             }
+            if (!staged) { ok = false; break; }
             tc::fence_before_sync();
             tc::fence_async_smem();
-            mbar_arrive(&b.ds_full);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&b.ds_full);
             // this block's dQ (lane t = query i0 + t) out of TMEM, staged in shared memory in the
             // accumulator's tile layout (a warp's 32 queries fill 512 contiguous bytes per 4 columns)
             if (!warp_wait(&b.dq_full, (uint32_t)(n & 1), b, a.err)) { ok = false; break; }
@@ -370,7 +411,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             for (int cc = 0; cc < D / 64; ++cc) tc::tmem_ld32(tl + C::COL_DQ + (half * (D / 64) + cc) * 32, v[cc]);
             tc::tmem_wait_ld();
             tc::fence_before_sync();
-            mbar_arrive(&b.dq_free);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&b.dq_free);
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc) {
                 const int c = half * (D / 64) + cc;  // this warp's 32-column chunks of dQ
