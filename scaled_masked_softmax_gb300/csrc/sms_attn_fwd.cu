@@ -169,6 +169,29 @@ __device__ __forceinline__ void mask_chunk(const AttnArgs &a, int64_t mrow, int 
     }
 }
 
+// Scores of 32 keys col0 .. col0+31 for query row i, in place, in log2 units:
+// S * scale * log2e + mask; with PR, keys past S or (causal) after i get -inf.
+// Returns the running maximum updated with them.
+template <bool PR>
+__device__ __forceinline__ float score_chunk(const AttnArgs &a, float (&s)[32], const float (&m2)[32], int col0, int i,
+                                             float sl2, float mx)
+{
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+        float s0 = fmaf(s[e], sl2, m2[e]);
+        float s1 = fmaf(s[e + 1], sl2, m2[e + 1]);
+        if constexpr (PR) {
+            const int col = col0 + e;
+            if (col >= a.S || (a.causal && col > i)) s0 = neg_inf();
+            if (col + 1 >= a.S || (a.causal && col + 1 > i)) s1 = neg_inf();
+        }
+        s[e] = s0;
+        s[e + 1] = s1;
+        mx = rowmath_max3(mx, s0, s1);
+    }
+    return mx;
+}
+
 template <typename T, int D, int MK>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -351,19 +374,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             for (int c = 0; c < kBN / 32; ++c) {
                 float m2[32];
                 mask_chunk<T, MK>(a, mrow, j0 + c * 32, row_ok, m2);
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float s0 = fmaf(sv[32 * c + e], sl2, m2[e]);
-                    float s1 = fmaf(sv[32 * c + e + 1], sl2, m2[e + 1]);
-                    if (pred) {
-                        const int col = j0 + c * 32 + e;
-                        if (col >= a.S || (a.causal && col > i)) s0 = neg_inf();
-                        if (col + 1 >= a.S || (a.causal && col + 1 > i)) s1 = neg_inf();
-                    }
-                    sv[32 * c + e] = s0;
-                    sv[32 * c + e + 1] = s1;
-                    mx = rowmath_max3(mx, s0, s1);
-                }
+                float(&sc)[32] = *reinterpret_cast<float(*)[32]>(sv + 32 * c);
+                mx = pred ? score_chunk<true>(a, sc, m2, j0 + c * 32, i, sl2, mx)
+                          : score_chunk<false>(a, sc, m2, j0 + c * 32, i, sl2, mx);
             }
             const float m_new = fmaxf(m_run, mx);
             const bool resc = m_new > m_run + 8.f;  // false while both are -inf
