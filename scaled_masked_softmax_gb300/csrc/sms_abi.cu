@@ -213,6 +213,43 @@ int sms_select_path(int64_t rows, int64_t cols, int dtype, int is_backward)
 
 namespace {
 
+// The mask-reuse order (ReuseOrder) of rows sharing a [cols, cols] mask with
+// no head stride: one super-block of every row when the mask has no batch
+// stride either (its last block may be partial), else one per batch of
+// `heads` whole blocks (a partial last batch keeps the natural order).
+ReuseOrder reuse_order(int64_t rows, int64_t cols, int64_t heads, int64_t mask_stride_b)
+{
+    ReuseOrder o{};
+    const int64_t T = kReuseTile;
+    int64_t sb, kf, rem;
+    if (mask_stride_b == 0) {
+        sb = rows;
+        kf = (rows - 1) / cols;
+        rem = rows - kf * cols;
+    } else {
+        sb = heads * cols;
+        kf = heads - 1;
+        rem = cols;
+    }
+    if (kf < 1 || rows > 0xffffffffll || rows / sb < 1) return o;  // places are 32-bit in the kernel
+    o.rows = rows / sb * sb;
+    o.sb = (uint32_t)sb;
+    o.kf = (uint32_t)kf;
+    const int64_t ta = rem / T, wb = std::min<int64_t>(T, cols - ta * T), rem_b = rem - ta * T;
+    o.ta = (uint32_t)ta;
+    o.wb = (uint32_t)wb;
+    o.rem_b = (uint32_t)rem_b;
+    o.pa = (uint32_t)((kf + 1) * T * ta);
+    o.pb = (uint32_t)(ta * T < cols ? kf * wb + rem_b : 0);
+    o.base_c = (uint32_t)(ta * T + (ta * T < cols ? wb : 0));
+    o.nc = (uint32_t)((cols - o.base_c) / T);
+    o.pc = (uint32_t)(kf * T * o.nc);
+    o.d_sb = FastDiv((uint32_t)sb);
+    o.d_a = FastDiv((uint32_t)((kf + 1) * T));
+    o.d_c = FastDiv((uint32_t)(kf * T));
+    return o;
+}
+
 // Validation and dispatch shared by sms_forward, sms_forward_bool and
 // sms_forward_lengths (`who` names the entry point in error messages;
 // mask_bool: the mask holds one byte per element).
@@ -293,6 +330,17 @@ int forward_impl(const char *who, const void *x, const void *mask, int64_t mask_
     a.lengths = lengths;
     a.mask_bool = (mask && mask_bool) ? 1 : 0;
     a.stall_ns = test_stall_ns();
+    // mask-reuse row order: fp32 rows whose per-block mask (cols x cols) is
+    // at least 64 MB.  Measured on GB300 (fp32 S=4099, a 67 MB mask read
+    // about four times in the natural order: 71% -> 83% of the copy rate).
+    // Below that size enough of the mask stays in L2 in the natural order and
+    // the order's index arithmetic costs more than it saves (fp32 S=2049 and
+    // S=3333: -4 to -5 points), and 16-bit rows, bound by issue, lost 1-4
+    // points at every size.
+    a.reuse = ReuseOrder{};
+    if (mask && mask_stride_h == 0 && eb == 4 &&
+        (double)cols * (double)cols * (mask_bool ? 1 : eb) >= (double)(64 << 20))
+        a.reuse = reuse_order(rows, cols, heads, mask_stride_b);
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (path) {

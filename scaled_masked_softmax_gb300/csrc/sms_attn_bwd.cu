@@ -71,8 +71,11 @@ template <int D> struct BwdCfg {
     static constexpr uint32_t SMEM = OFF_BAR + BAR_BYTES + 1024;
     static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 256 + D, COL_DQ = 128;
     // one block's dQ in fp32, staged over P^T and dS^T: element (query r, column c)
-    // at byte ((c / 4) * 128 + r) * 16 + (c % 4) * 4, the accumulator's tile layout
+    // at byte ((c / 4) * 128 + r) * 16 + (c % 4) * 4, the accumulator's tile layout.
+    // Piece p (columns 32p .. 32p+31, 16 KB at p * 16 KB) overlays atom p % 2 of
+    // P^T (p < 2) or dS^T (p >= 2)
     static constexpr uint32_t DQ_BYTES = kBN * D * 4;
+    static constexpr int DQ_PIECES = D / 32;
     static_assert(DQ_BYTES <= 2 * SQ && OFF_DS == OFF_P + SQ, "dQ staging area");
     static_assert(SMEM <= 232448, "shared memory per CTA");
 };
@@ -80,7 +83,7 @@ template <int D> struct BwdCfg {
 struct BwdBars {
     uint64_t kv_full;
     uint64_t r_full[4], r_empty[4];
-    uint64_t s_full, ds_full, dq_full, dq_free, stage_free;
+    uint64_t s_full, ds_full, dq_full, dq_free, stage_free[2];
     uint64_t mma_drain;
     uint32_t tmem_base;
     int abort;
@@ -229,7 +232,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
         mbar_init(&b.ds_full, kMath / 32);   // one arrival per element-wise warp
         mbar_init(&b.dq_full, 1);
         mbar_init(&b.dq_free, kMath / 32);
-        mbar_init(&b.stage_free, 1);
+        mbar_init(&b.stage_free[0], 1);
+        mbar_init(&b.stage_free[1], 1);
         mbar_init(&b.mma_drain, 1);
         b.abort = 0;
         fence_mbar_init();
@@ -368,7 +372,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             bool staged = true;
 #pragma unroll
             for (int cc = 0; cc < kBN / 64; ++cc) {
-                const int c = half * (kBN / 64) + cc;  // this warp's 32-query chunks
+                // chunk cc of both warps of a lane quarter covers queries 64cc .. 64cc+63: atom cc
+                // of P^T and of dS^T, the ones the dQ pieces of bulk group cc overlay
+                const int c = cc * 2 + half;
                 float m2[32];
                 mask_col<T, MK>(a, mbase, i0 + c * 32, key_ok, m2);
                 uint32_t sv[32], dv[32];
@@ -378,15 +384,16 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 uint32_t pk[16], dk[16];
                 if (pred) p_ds_chunk<T, MK, true>(a, sv, dv, m2, s_lse, s_dsc, c, i0, j, key_ok, sl2, pk, dk);
                 else p_ds_chunk<T, MK, false>(a, sv, dv, m2, s_lse, s_dsc, c, i0, j, key_ok, sl2, pk, dk);
-                if (cc == 0 && n > 0) {
-                    // the previous block's dQ has left the P^T / dS^T area (its bulk add has read
-                    // it) before the first store here; the wait overlaps the first chunk's arithmetic
+                if (n > 0) {
+                    // the previous block's dQ pieces over atom cc have been read by their bulk adds
+                    // (group cc) before the stores here; the waits overlap the chunks' arithmetic
                     if (mt == 0) {
-                        tc::bulk_wait_read();
-                        mbar_arrive(&b.stage_free);
+                        if (cc == 0) tc::bulk_wait_read_but_last();
+                        else tc::bulk_wait_read();
+                        mbar_arrive(&b.stage_free[cc]);
                     }
                     __syncwarp();
-                    if (!warp_wait(&b.stage_free, (uint32_t)((n - 1) & 1), b, a.err)) { staged = false; break; }
+                    if (!warp_wait(&b.stage_free[cc], (uint32_t)((n - 1) & 1), b, a.err)) { staged = false; break; }
                 }
                 unsigned char *pa = smem + C::OFF_P + (c / 2) * kAtom;
                 unsigned char *da = smem + C::OFF_DS + (c / 2) * kAtom;
@@ -423,11 +430,17 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             }
             tc::fence_async_smem();
             named_sync(2, kMath);
-            // one bulk add of the whole tile into the accumulator, by the TMA unit
+            // the tile added into the accumulator by the TMA unit: the pieces over atom 0 of
+            // P^T / dS^T as one bulk group, then those over atom 1 (the next block writes atom 0 first)
             if (mt == 0) {
-                tc::bulk_reduce_add_f32(a.dq_acc + ((int64_t)bh * nqb + qb0 + n) * (kBN * D), s_base + C::OFF_P,
-                                        C::DQ_BYTES);
-                tc::bulk_commit();
+                float *g = a.dq_acc + ((int64_t)bh * nqb + qb0 + n) * (kBN * D);
+#pragma unroll
+                for (int grp = 0; grp < 2; ++grp) {
+#pragma unroll
+                    for (int p = grp; p < C::DQ_PIECES; p += 2)
+                        tc::bulk_reduce_add_f32(g + p * (kBN * 32), s_base + C::OFF_P + p * kAtom, kAtom);
+                    tc::bulk_commit();
+                }
             }
         }
         // the last bulk adds have finished before the CTA's shared memory is released

@@ -14,6 +14,29 @@ enum { kF32 = 0, kF16 = 1, kBF16 = 2 };
 inline int vec_elems(int dtype) { return dtype == kF32 ? 4 : 8; }
 inline int elem_bytes(int dtype) { return dtype == kF32 ? 4 : 2; }
 
+// Mask-reuse row order.  Rows r = k*cols + q of a super-block (the rows that
+// share one [cols, cols] mask: every head of every batch when the mask has
+// no batch or head stride, the heads of one batch when it has only a batch
+// stride) read mask row q.  In the natural order the super-block's blocks
+// k read the whole mask one after another, and a mask too large for L2 is
+// fetched from HBM once per block.  Reordered, the rows go in tiles of
+// kReuseTile query positions, each tile walking every block (the last block
+// as far as its `rem` rows reach), so the reads of a mask row come close
+// together.  Place n of a super-block maps to (k, q) by three regions of
+// tiles: A, tiles the last block covers (kf + 1 blocks of kReuseTile rows);
+// B, the one tile it covers in part (or the narrower last tile); C, tiles it
+// does not reach (kf blocks each; the final tile may be narrower).
+constexpr uint32_t kReuseTile = 64;
+struct ReuseOrder {
+    int64_t rows;              // places reordered (whole super-blocks); 0: natural order
+    uint32_t sb;               // rows per super-block
+    uint32_t kf;               // blocks of the super-block before its last one (>= 1)
+    uint32_t ta, wb, rem_b;    // region B: tile ta, its width, the last block's rows in it
+    uint32_t pa, pb;           // places in regions A and B
+    uint32_t base_c, nc, pc;   // region C: first query position, whole tiles, places in them
+    FastDiv d_sb, d_a, d_c;    // division by sb, (kf + 1) * kReuseTile and kf * kReuseTile
+};
+
 struct FwdArgs {
     const void *x;
     const void *mask;      // nullptr: no mask
@@ -30,6 +53,7 @@ struct FwdArgs {
     int mask_bool;         // 1: the mask holds one byte per element (nonzero = masked), 0: additive, dtype of x
     uint32_t stall_ns;     // test control (sms_set_test_stall): >0 makes a ring group's first wait one on a
                            // barrier nothing arrives at, bounded at this many ns
+    ReuseOrder reuse;      // row order of the register row kernels (fwd_row_kernel)
 };
 
 struct BwdArgs {

@@ -114,31 +114,75 @@ __device__ __forceinline__ RowPos fwd_pos(const FwdArgs &a, int64_t r)
     return p;
 }
 
-template <int NV, bool ALIGNED> struct FwdBuf {
-    uint4 x[NV], m[NV], m2[ALIGNED ? 1 : NV];
+// Misaligned rows on groups of 32 or more lanes may take the contiguous lane
+// mapping (CONTIG, see vec_index) and, with an additive mask, the shuffled
+// realignment (SHUF): the second aligned mask vector of a slot is then not
+// loaded but taken from the neighbouring lane (realign_shfl), and m2[0] is the
+// one vector past the end of the warp's run, loaded by the warp's last lane.
+template <int NV, bool ALIGNED, bool SHUF = false> struct FwdBuf {
+    uint4 x[NV], m[NV], m2[(ALIGNED || SHUF) ? 1 : NV];
 };
+
+// Row vector held by lane gl of the group in slot k.  Slot-major (vector
+// k*G + gl) except with CONTIG, where each warp of the group holds a
+// contiguous run of 32*NV vectors (slot k of lane l: vector k*32 + l of the
+// run), so the vector after a lane's own sits in lane l+1 or, for lane 31, in
+// lane 0's next slot.  Both forms read 512 contiguous bytes per warp and slot.
+template <int G, int NV, bool CONTIG>
+__device__ __forceinline__ int vec_index(int k, int gl)
+{
+    if constexpr (CONTIG && G > 32) return (gl >> 5) * (32 * NV) + k * 32 + (gl & 31);
+    else return k * G + gl;
+}
 
 // Issue every 16-byte load of row p: x, then the mask (two aligned mask
 // vectors per x vector when the mask row is misaligned relative to x).  The
 // per-vector bounds tests of rows at the ends of the buffers live in their
 // own loop: one warp-uniform branch per row keeps them out of the common path.
-template <typename T, int G, int NV, bool ALIGNED, typename M = T>
-__device__ __forceinline__ void fwd_issue(const FwdArgs &a, const RowPos &p, int gl, FwdBuf<NV, ALIGNED> &B)
+template <typename T, int G, int NV, bool ALIGNED, typename M = T, bool SHUF = false, bool CONTIG = SHUF>
+__device__ __forceinline__ void fwd_issue(const FwdArgs &a, const RowPos &p, int gl, FwdBuf<NV, ALIGNED, SHUF> &B)
 {
     constexpr int VEC = Dt<T>::VEC;
     using MIO = MaskIO<T, M>;
     const T *xs = reinterpret_cast<const T *>(a.x) + p.xb;
     const M *mk = reinterpret_cast<const M *>(a.mask) + p.mA;
+    static_assert(!SHUF || (!ALIGNED && G >= 32 && CONTIG), "shuffled realignment: misaligned rows, whole warps");
+    static_assert(!CONTIG || (!ALIGNED && G >= 32), "contiguous mapping: misaligned rows, whole warps");
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
         B.x[k] = make_uint4(0, 0, 0, 0);
         B.m[k] = make_uint4(0, 0, 0, 0);
-        if constexpr (!ALIGNED) B.m2[k] = make_uint4(0, 0, 0, 0);
+        if constexpr (!ALIGNED && !SHUF) B.m2[k] = make_uint4(0, 0, 0, 0);
+    }
+    if constexpr (SHUF) B.m2[0] = make_uint4(0, 0, 0, 0);
+    if constexpr (SHUF) {
+        if (!p.fast) {  // a row at an end of x or of the mask buffer: the mask is read element-wise later
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                const int vi = vec_index<G, NV, CONTIG>(k, gl);
+                if (vi * VEC - p.xoff < p.limit && p.xb + (int64_t)(vi + 1) * VEC <= a.x_total)
+                    B.x[k] = ld_stream(xs + vi * VEC);
+            }
+            return;
+        }
+        // a misaligned mask row also needs the aligned mask vector after the
+        // row's last x vector: mask vectors are read one vector further
+        const int mlim = p.limit + (p.msh ? VEC : 0);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int vi = vec_index<G, NV, CONTIG>(k, gl);
+            const int j0 = vi * VEC - p.xoff;
+            if (j0 < p.limit) B.x[k] = ld_stream(xs + vi * VEC);
+            if (a.mask && j0 < mlim) B.m[k] = MIO::ld(mk + vi * VEC);
+            if (k == NV - 1 && (gl & 31) == 31 && a.mask && p.msh && j0 < p.limit)
+                B.m2[0] = MIO::ld(mk + vi * VEC + VEC);  // the vector after the warp's run
+        }
+        return;
     }
     if (ALIGNED || p.fast) {
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
-            const int vi = k * G + gl;
+            const int vi = vec_index<G, NV, CONTIG>(k, gl);
             if (vi * VEC - p.xoff < p.limit) {
                 B.x[k] = ld_stream(xs + vi * VEC);
                 if (a.mask) {
@@ -152,7 +196,7 @@ __device__ __forceinline__ void fwd_issue(const FwdArgs &a, const RowPos &p, int
     } else if constexpr (!ALIGNED) {  // a row at an end of x or of the mask buffer
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
-            const int vi = k * G + gl;
+            const int vi = vec_index<G, NV, CONTIG>(k, gl);
             if (vi * VEC - p.xoff < p.limit) {
                 if (p.xb + (int64_t)(vi + 1) * VEC <= a.x_total) B.x[k] = ld_stream(xs + vi * VEC);
                 if (a.mask) {
@@ -190,6 +234,43 @@ __device__ __forceinline__ void realign(uint4 (&m)[NV], const uint4 (&m2)[NV], i
     }
 }
 
+// Realignment by shuffles (FwdBuf SHUF): slot k of warp lane l takes the
+// window S elements into (its own aligned mask vector, the next one), the
+// next one coming from lane l+1's slot k, or for lane 31 from lane 0's slot
+// k+1 (from the loaded m2[0] in the last slot).  Slots are done in order, so
+// slot k+1 is still raw when lane 0 hands it over.  Whole warps only.
+template <typename MIO, int NV, int S>
+__device__ __forceinline__ void realign_shfl_fixed(uint4 (&m)[NV], const uint4 &ext, int lane)
+{
+    const int src = (lane + 1) & 31;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const uint4 v = (k + 1 < NV && lane == 0) ? m[k + 1] : m[k];
+        uint4 nx;
+        nx.x = __shfl_sync(0xffffffffu, v.x, src);
+        nx.y = __shfl_sync(0xffffffffu, v.y, src);
+        nx.z = __shfl_sync(0xffffffffu, v.z, src);
+        nx.w = __shfl_sync(0xffffffffu, v.w, src);
+        if (k == NV - 1 && lane == 31) nx = ext;
+        m[k] = MIO::template win<S>(m[k], nx);
+    }
+}
+template <typename MIO, int NV>
+__device__ __forceinline__ void realign_shfl(uint4 (&m)[NV], const uint4 &ext, int s, int lane)
+{
+    constexpr int VEC = MIO::VEC;
+    switch (s) {
+    case 0: break;
+    case 1: realign_shfl_fixed<MIO, NV, 1>(m, ext, lane); break;
+    case 2: realign_shfl_fixed<MIO, NV, 2>(m, ext, lane); break;
+    case 3: realign_shfl_fixed<MIO, NV, 3>(m, ext, lane); break;
+    case 4: realign_shfl_fixed<MIO, NV, 4 % VEC>(m, ext, lane); break;
+    case 5: realign_shfl_fixed<MIO, NV, 5 % VEC>(m, ext, lane); break;
+    case 6: realign_shfl_fixed<MIO, NV, 6 % VEC>(m, ext, lane); break;
+    default: realign_shfl_fixed<MIO, NV, 7 % VEC>(m, ext, lane); break;
+    }
+}
+
 // Scores s = x*scale + mask of one vector (-inf outside [0, limit)), folded
 // into the running max.
 template <int VEC>
@@ -217,9 +298,9 @@ __device__ __forceinline__ void score_vec(const float (&xv)[VEC], const float (&
 
 // Scores of vector slot k on the common path: every vector read lies inside
 // x and the mask, and the mask is already realigned.
-template <typename T, int G, int NV, bool ALIGNED, typename M = T>
+template <typename T, int G, int NV, bool ALIGNED, typename M = T, bool SHUF = false, bool CONTIG = SHUF>
 __device__ __forceinline__ void fwd_scores(const FwdArgs &a, const RowPos &p, int gl, int k,
-                                           const FwdBuf<NV, ALIGNED> &B, float (&s)[Dt<T>::VEC], float &mx)
+                                           const FwdBuf<NV, ALIGNED, SHUF> &B, float (&s)[Dt<T>::VEC], float &mx)
 {
     constexpr int VEC = Dt<T>::VEC;
     float xv[VEC], mv[VEC];
@@ -230,18 +311,18 @@ __device__ __forceinline__ void fwd_scores(const FwdArgs &a, const RowPos &p, in
 #pragma unroll
         for (int e = 0; e < VEC; ++e) mv[e] = 0.f;
     }
-    score_vec<VEC>(xv, mv, a.scale, (k * G + gl) * VEC - p.xoff, p.limit, s, mx);
+    score_vec<VEC>(xv, mv, a.scale, vec_index<G, NV, CONTIG>(k, gl) * VEC - p.xoff, p.limit, s, mx);
 }
 
 // Scores of vector slot k of a row at an end of x or of the mask buffer:
 // partial vectors are read element by element.
-template <typename T, int G, int NV, typename M = T>
+template <typename T, int G, int NV, typename M = T, bool SHUF = false, bool CONTIG = SHUF>
 __device__ __forceinline__ void fwd_scores_edge(const FwdArgs &a, const RowPos &p, int gl, int k,
-                                                const FwdBuf<NV, false> &B, float (&s)[Dt<T>::VEC], float &mx)
+                                                const FwdBuf<NV, false, SHUF> &B, float (&s)[Dt<T>::VEC], float &mx)
 {
     constexpr int VEC = Dt<T>::VEC;
     using MIO = MaskIO<T, M>;
-    const int vi = k * G + gl;
+    const int vi = vec_index<G, NV, CONTIG>(k, gl);
     const int j0 = vi * VEC - p.xoff;
     float xv[VEC], mv[VEC];
     unpack<T>(B.x[k], xv);
@@ -257,8 +338,8 @@ __device__ __forceinline__ void fwd_scores_edge(const FwdArgs &a, const RowPos &
         }
         if (a.mask) {
             const int64_t mb = p.mA + (int64_t)vi * VEC;
-            if (mb >= 0 && mb + (p.msh ? 2 : 1) * VEC <= a.mask_total) {
-                MIO::unpack_m(MIO::win_rt(B.m[k], B.m2[k], p.msh), mv);
+            if (!SHUF && mb >= 0 && mb + (p.msh ? 2 : 1) * VEC <= a.mask_total) {
+                MIO::unpack_m(MIO::win_rt(B.m[k], B.m2[SHUF ? 0 : k], p.msh), mv);
             } else {  // mask vectors at the ends of the mask buffer: element loads
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) {
@@ -350,30 +431,32 @@ __device__ __forceinline__ float fwd_norm(float (&s)[NV][VEC], float mx, int gl,
 // Scores, exponentials and the row's normalisation factor: s holds the
 // exponentials on return.  red_m / red_l: this call's shared slots
 // [group][warp] (multi-warp groups only).
-template <typename T, int G, int NV, bool ALIGNED, typename M = T>
+template <typename T, int G, int NV, bool ALIGNED, typename M = T, bool SHUF = false, bool CONTIG = SHUF>
 __device__ __forceinline__ float fwd_reduce(const FwdArgs &a, const RowPos &p, int gl, int gi,
-                                            FwdBuf<NV, ALIGNED> &B, float (&s)[NV][Dt<T>::VEC],
+                                            FwdBuf<NV, ALIGNED, SHUF> &B, float (&s)[NV][Dt<T>::VEC],
                                             float (*red_m)[G > 32 ? G / 32 : 1], float (*red_l)[G > 32 ? G / 32 : 1],
                                             int bar)
 {
     constexpr int VEC = Dt<T>::VEC;
     float mx = neg_inf();
     if (ALIGNED || p.fast) {
-        if constexpr (!ALIGNED) {
+        if constexpr (SHUF) {
+            if (a.mask) realign_shfl<MaskIO<T, M>, NV>(B.m, B.m2[0], p.msh, threadIdx.x & 31);
+        } else if constexpr (!ALIGNED) {
             if (a.mask) realign<MaskIO<T, M>, NV>(B.m, B.m2, p.msh);
         }
 #pragma unroll
-        for (int k = 0; k < NV; ++k) fwd_scores<T, G, NV, ALIGNED, M>(a, p, gl, k, B, s[k], mx);
+        for (int k = 0; k < NV; ++k) fwd_scores<T, G, NV, ALIGNED, M, SHUF, CONTIG>(a, p, gl, k, B, s[k], mx);
     } else if constexpr (!ALIGNED) {
 #pragma unroll
-        for (int k = 0; k < NV; ++k) fwd_scores_edge<T, G, NV, M>(a, p, gl, k, B, s[k], mx);
+        for (int k = 0; k < NV; ++k) fwd_scores_edge<T, G, NV, M, SHUF, CONTIG>(a, p, gl, k, B, s[k], mx);
     }
 
     return fwd_norm<G, NV, VEC>(s, mx, gl, gi, red_m, red_l, bar);
 }
 
 // y = e * fac for every element the lane holds.
-template <typename T, int G, int NV, bool ALIGNED>
+template <typename T, int G, int NV, bool ALIGNED, bool CONTIG = false>
 __device__ __forceinline__ void fwd_store(const FwdArgs &a, const RowPos &p, int gl, const float (&s)[NV][Dt<T>::VEC],
                                           float fac)
 {
@@ -384,7 +467,7 @@ __device__ __forceinline__ void fwd_store(const FwdArgs &a, const RowPos &p, int
     const float2 f2 = make_float2(fac, fac);
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
-        const int vi = k * G + gl;
+        const int vi = vec_index<G, NV, CONTIG>(k, gl);
         const int j0 = vi * VEC - p.xoff;
         if (j0 >= cols) continue;
         float o[VEC];
@@ -408,14 +491,14 @@ __device__ __forceinline__ void fwd_store(const FwdArgs &a, const RowPos &p, int
 
 // Reduce, normalise and store row p from its loaded buffer (every thread of
 // the CTA calls this equally often when G > 32 and bar == 0).
-template <typename T, int G, int NV, bool ALIGNED, typename M = T>
+template <typename T, int G, int NV, bool ALIGNED, typename M = T, bool SHUF = false, bool CONTIG = SHUF>
 __device__ __forceinline__ void fwd_finish(const FwdArgs &a, const RowPos &p, int gl, int gi,
-                                           FwdBuf<NV, ALIGNED> &B, float (*red_m)[G > 32 ? G / 32 : 1],
+                                           FwdBuf<NV, ALIGNED, SHUF> &B, float (*red_m)[G > 32 ? G / 32 : 1],
                                            float (*red_l)[G > 32 ? G / 32 : 1], int bar = 0)
 {
     float s[NV][Dt<T>::VEC];
-    const float fac = fwd_reduce<T, G, NV, ALIGNED, M>(a, p, gl, gi, B, s, red_m, red_l, bar);
-    fwd_store<T, G, NV, ALIGNED>(a, p, gl, s, fac);
+    const float fac = fwd_reduce<T, G, NV, ALIGNED, M, SHUF, CONTIG>(a, p, gl, gi, B, s, red_m, red_l, bar);
+    fwd_store<T, G, NV, ALIGNED, CONTIG>(a, p, gl, s, fac);
 }
 
 // ------------------------------------------------------------ backward ---

@@ -386,23 +386,83 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_warp_kernel(const BwdArgs a)
     }
 }
 
+// Row at place n of the launch order under the mask-reuse order (ReuseOrder):
+// the super-block, then the region of tiles, then (block k, query q) inside
+// the tile, blocks in order and queries in order within a block.
+__device__ __forceinline__ int64_t reuse_row(const FwdArgs &a, int64_t n)
+{
+    const ReuseOrder &o = a.reuse;
+    if (n >= o.rows) return n;  // natural order (o.rows == 0 when the order is off)
+    constexpr uint32_t T = kReuseTile;
+    const uint32_t S = (uint32_t)a.cols, nn = (uint32_t)n;
+    const uint32_t sb = o.d_sb.div(nn);
+    uint32_t loc = nn - sb * o.sb, k, q;
+    if (loc < o.pa) {  // A: kf + 1 blocks of T rows per tile
+        const uint32_t t = o.d_a.div(loc);
+        const uint32_t j = loc - t * ((o.kf + 1) * T);
+        k = j / T;
+        q = t * T + j % T;
+    } else if ((loc -= o.pa) < o.pb) {  // B: kf blocks of wb rows, then the last block's rem_b
+        if (loc < o.kf * o.wb) {
+            k = loc / o.wb;
+            q = o.ta * T + (loc - k * o.wb);
+        } else {
+            k = o.kf;
+            q = o.ta * T + (loc - o.kf * o.wb);
+        }
+    } else if ((loc -= o.pb) < o.pc) {  // C, whole tiles: kf blocks of T rows
+        const uint32_t t = o.d_c.div(loc);
+        const uint32_t j = loc - t * (o.kf * T);
+        k = j / T;
+        q = o.base_c + t * T + j % T;
+    } else {  // C, the final narrower tile
+        loc -= o.pc;
+        const uint32_t w = S - o.base_c - o.nc * T;
+        k = loc / w;
+        q = o.base_c + o.nc * T + (loc - k * w);
+    }
+    return (int64_t)sb * o.sb + (int64_t)k * S + q;
+}
+
+// Misaligned rows on whole warps take the contiguous lane mapping (each warp
+// a run of consecutive vectors); with an additive mask they also take their
+// second aligned mask vector from the neighbouring lane by shuffle instead of
+// a second load per slot (4*NV fewer registers).  A byte mask's second vector
+// is one or two words, and the shuffles cost it 3-4 points: it keeps the
+// second load, on the same mapping, so that a boolean mask and its additive
+// -inf form give the same bits.  Measured on GB300: 16-bit rows gain 2-4
+// points at every lane count from 32; fp32 rows gain only at 256 x 5 (S =
+// 4097..5120, where the freed registers give four CTAs per SM: 71% -> 77% at
+// S=4099) and lose 1-2 points at 128 x 5 and 256 x 4, which keep the old form.
+template <typename T, int G, int NV, bool ALIGNED> __host__ __device__ constexpr bool fwd_contiguous()
+{
+    return !ALIGNED && G >= 32 && (sizeof(T) == 2 || (G == 256 && NV == 5));
+}
+template <typename T, typename M, int G, int NV, bool ALIGNED> __host__ __device__ constexpr bool fwd_shuffled()
+{
+    return fwd_contiguous<T, G, NV, ALIGNED>() && std::is_same<T, M>::value;
+}
+
 // One row per lane group: the shared row math of sms_rowmath.cuh (one
 // switch per row realigns a misaligned mask, bounds are tested once per row,
-// paired elements use the packed fp32x2 forms).  fp32 rows are held in at
-// most 80 registers, three CTAs per multiprocessor: measured faster than two
-// CTAs with more registers (S=4099: 66% against 43% of the copy rate; S=1024:
-// +5%).  Not for misaligned fp32 rows of 6 or 8 vectors per lane (they would
-// spill).  The 16-bit forms take three CTAs at 5 vectors per lane: the
-// misaligned ones then spill a few hundred bytes and still gain 9-11 points
-// over two CTAs (S=2049, 2500, 4099); at 4, 6 or 8 vectors two CTAs measured
-// no worse.
-template <typename T, int NV, bool ALIGNED> constexpr int fwd_min_ctas()
+// paired elements use the packed fp32x2 forms).  CTAs per SM it is compiled
+// for: the shuffled shapes that fit 64 registers without spilling (G = 256,
+// or at most 4 vectors per lane) take four (measured +6 points at fp32
+// S=4099, 256 x 5; +2 to +4 on 16-bit misaligned rows).  Otherwise fp32 rows
+// are held in at most 80 registers, three CTAs per multiprocessor: measured
+// faster than two CTAs with more registers (S=4099: 66% against 43% of the
+// copy rate; S=1024: +5%); not for misaligned fp32 rows of 6 or 8 vectors per
+// lane (they would spill).  The 16-bit forms take three CTAs at 5 vectors per
+// lane (the misaligned ones gained 9-11 points over two CTAs at S=2049, 2500
+// and 4099); at 4, 6 or 8 vectors two CTAs measured no worse.
+template <typename T, typename M, int G, int NV, bool ALIGNED> constexpr int fwd_min_ctas()
 {
+    if (fwd_shuffled<T, M, G, NV, ALIGNED>() && (G == 256 || NV <= 4)) return 4;
     return (Dt<T>::VEC == 4 && (ALIGNED || NV <= 5)) ? 3 : (NV == 5 ? 3 : 2);
 }
 
 template <typename T, int G, int NV, bool ALIGNED, typename M>
-__global__ void __launch_bounds__(kThreads, fwd_min_ctas<T, NV, ALIGNED>()) fwd_row_kernel(const FwdArgs a)
+__global__ void __launch_bounds__(kThreads, fwd_min_ctas<T, M, G, NV, ALIGNED>()) fwd_row_kernel(const FwdArgs a)
 {
     using namespace rowmath;
     constexpr int GPC = kThreads / G;
@@ -410,10 +470,15 @@ __global__ void __launch_bounds__(kThreads, fwd_min_ctas<T, NV, ALIGNED>()) fwd_
     __shared__ float red_m[GPC][W], red_l[GPC][W];
     const int gl = threadIdx.x % G;
     const int gi = threadIdx.x / G;
-    const RowPos p = fwd_pos<Dt<T>::VEC, ALIGNED>(a, (int64_t)blockIdx.x * GPC + gi);
-    FwdBuf<NV, ALIGNED> B;
-    fwd_issue<T, G, NV, ALIGNED, M>(a, p, gl, B);
-    fwd_finish<T, G, NV, ALIGNED, M>(a, p, gl, gi, B, red_m, red_l);
+    const int64_t n = (int64_t)blockIdx.x * GPC + gi;
+    // the mask-reuse order is only ever set up for fp32 rows of 4096 or more
+    // columns (sms_abi.cu); other shapes leave its arithmetic out
+    constexpr bool REUSE = sizeof(T) == 4 && G * NV * Dt<T>::VEC >= 4096;
+    const RowPos p = fwd_pos<Dt<T>::VEC, ALIGNED>(a, REUSE ? reuse_row(a, n) : n);
+    constexpr bool SHUF = fwd_shuffled<T, M, G, NV, ALIGNED>(), CONTIG = fwd_contiguous<T, G, NV, ALIGNED>();
+    FwdBuf<NV, ALIGNED, SHUF> B;
+    fwd_issue<T, G, NV, ALIGNED, M, SHUF, CONTIG>(a, p, gl, B);
+    fwd_finish<T, G, NV, ALIGNED, M, SHUF, CONTIG>(a, p, gl, gi, B, red_m, red_l);
 }
 
 template <typename T, int G, int NV, bool ALIGNED>

@@ -485,3 +485,20 @@ def test_ring_wait_that_runs_out_reports_and_recovers(direction):
             torch.cuda.synchronize()
             H.check_backward(H.to_np64(dx), y_ok.cpu(), inp["dy"].cpu(), w.scale, torch.float16, "ring bwd after a stall")
     assert sms.sms_device_error(st) == 0
+
+
+@pytest.mark.parametrize("S,kind,rows_cut", [(4099, "B1SS", 77), (4100, "SS", 0), (4099, "SS", 1234)])
+def test_mask_reuse_row_order(S, kind, rows_cut):
+    """fp32 rows whose per-block mask is at least 64 MB go through the register
+    row kernel in the mask-reuse order: every row still comes out once, right,
+    with each batch's heads ([B,1,S,S]) or every head block ([S,S]) as the
+    rows sharing a mask row, including a partial last batch or block."""
+    B, Hh = 2, 3
+    rows = B * Hh * S - rows_cut
+    w = _wl(S, "f32", rows, mask=kind, B=B, Hh=Hh, seed=23)
+    inp = H.make(w)
+    y = _run_fwd(w, inp, "warp")
+    chk = H.check_all_rows(w, inp, y, None, f"reuse order {kind} S={S} rows={rows}")
+    assert chk.rows == rows
+    del inp, y
+    torch.cuda.empty_cache()
