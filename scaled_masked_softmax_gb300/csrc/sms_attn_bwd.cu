@@ -35,6 +35,7 @@
 #include <atomic>
 
 #include "sms_attn.h"
+#include "sms_attn_mask.cuh"
 #include "sms_common.cuh"
 #include "sms_internal.h"
 #include "sms_tc.cuh"
@@ -126,13 +127,17 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, __nv_bfloat16 *)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Mask terms (log2-scaled) of key j for the 32 queries i0 .. i0+31: element
-// (i, j) sits at mrow0 + i*S + j.  Queries at or beyond S read nothing.
+// Mask elements of key j for the 32 queries i0 .. i0+31 (element (i, j) at
+// mbase + i*S), packed: a byte mask four per word, an additive 16-bit mask
+// two per word.  Queries at or beyond S (and keys beyond S) read nothing and
+// count as kept.  Loaded before the block's scores are ready, so that the
+// loads' latency passes while the tensor cores compute them.
 template <typename T, int MK>
-__device__ __forceinline__ void mask_col(const AttnArgs &a, int64_t mbase, int i0, bool key_ok, float (&m2)[32])
+__device__ __forceinline__ void mask_col_load(const AttnArgs &a, int64_t mbase, int i0, bool key_ok,
+                                              uint32_t (&w)[MaskWords<MK>::n])
 {
 #pragma unroll
-    for (int e = 0; e < 32; ++e) m2[e] = 0.f;
+    for (int k = 0; k < MaskWords<MK>::n; ++k) w[k] = 0u;
     if constexpr (MK != 0) {
         if (!key_ok) return;
 #pragma unroll
@@ -140,8 +145,13 @@ __device__ __forceinline__ void mask_col(const AttnArgs &a, int64_t mbase, int i
             const int i = i0 + e;
             if (i < a.S) {
                 const int64_t off = mbase + (int64_t)i * a.S;
-                if constexpr (MK == 1) m2[e] = to_f32<T>(reinterpret_cast<const T *>(a.mask)[off]) * kLog2e;
-                else m2[e] = reinterpret_cast<const uint8_t *>(a.mask)[off] ? neg_inf() : 0.f;
+                if constexpr (MK == 1) {
+                    const uint32_t h = reinterpret_cast<const uint16_t *>(a.mask)[off];
+                    w[e >> 1] |= h << (16 * (e & 1));
+                } else {
+                    const uint32_t bt = reinterpret_cast<const uint8_t *>(a.mask)[off];
+                    w[e >> 2] |= bt << (8 * (e & 3));
+                }
             }
         }
     }
@@ -367,6 +377,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             named_sync(1, kMath);
             fetch(n + 1);
             const bool pred = !key_ok || (i0 + kBN > a.S) || (a.causal && j0 + kBM - 1 > i0);
+            // this block's mask elements (both chunks), fetched while S^T and dP^T are computed
+            uint32_t mw[kBN / 64][MaskWords<MK>::n];
+#pragma unroll
+            for (int cc = 0; cc < kBN / 64; ++cc) mask_col_load<T, MK>(a, mbase, i0 + (cc * 2 + half) * 32, key_ok, mw[cc]);
             if (!warp_wait(&b.s_full, (uint32_t)(n & 1), b, a.err)) { ok = false; break; }
             tc::fence_after_sync();
             bool staged = true;
@@ -376,7 +390,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 // of P^T and of dS^T, the ones the dQ pieces of bulk group cc overlay
                 const int c = cc * 2 + half;
                 float m2[32];
-                mask_col<T, MK>(a, mbase, i0 + c * 32, key_ok, m2);
+                mask_terms<T, MK>(mw[cc], m2);
                 uint32_t sv[32], dv[32];
                 tc::tmem_ld32(tl + C::COL_S + c * 32, sv);
                 tc::tmem_ld32(tl + C::COL_DP + c * 32, dv);

@@ -31,6 +31,7 @@
 #include <atomic>
 
 #include "sms_attn.h"
+#include "sms_attn_mask.cuh"
 #include "sms_common.cuh"
 #include "sms_internal.h"
 #include "sms_tc.cuh"
@@ -119,51 +120,38 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, __nv_bfloat16 *)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// The 32 mask values of columns c0 .. c0+31 of one query row, as additive
-// log2-scaled terms (0 where no mask), in m2[].  MK: 0 none, 1 additive (T),
-// 2 boolean bytes.  Columns at or beyond S read nothing.
+// The 32 mask elements of columns c0 .. c0+31 of one query row, packed
+// (MaskWords): 16-byte loads where the chunk is whole and aligned, element
+// loads otherwise.  Columns at or beyond S read nothing and count as kept.
 template <typename T, int MK>
-__device__ __forceinline__ void mask_chunk(const AttnArgs &a, int64_t mrow, int c0, bool row_ok, float (&m2)[32])
+__device__ __forceinline__ void mask_chunk_load(const AttnArgs &a, int64_t mrow, int c0, bool row_ok,
+                                                uint32_t (&w)[MaskWords<MK>::n])
 {
 #pragma unroll
-    for (int e = 0; e < 32; ++e) m2[e] = 0.f;
-    if constexpr (MK == 0) {
-        return;
-    } else {
+    for (int k = 0; k < MaskWords<MK>::n; ++k) w[k] = 0u;
+    if constexpr (MK != 0) {
         if (!row_ok) return;
         const int64_t base = mrow + c0;
         const int S = a.S;
-        if constexpr (MK == 1) {
-            const T *mp = reinterpret_cast<const T *>(a.mask) + base;
-            const bool vec = (c0 + 32 <= S) && ((reinterpret_cast<uintptr_t>(mp) & 15u) == 0);
-            if (vec) {
+        constexpr int EB = MK == 1 ? 2 : 1;  // bytes per element
+        const unsigned char *mp = reinterpret_cast<const unsigned char *>(a.mask) + base * EB;
+        const bool vec = (c0 + 32 <= S) && ((reinterpret_cast<uintptr_t>(mp) & 15u) == 0);
+        if (vec) {
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    float f[8];
-                    unpack<T>(ld_keep(mp + 8 * v), f);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) m2[8 * v + e] = f[e] * kLog2e;
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    if (c0 + e < S) m2[e] = to_f32<T>(mp[e]) * kLog2e;
+            for (int v = 0; v < 2 * EB; ++v) {
+                const uint4 q = ld_keep(reinterpret_cast<const T *>(mp + 16 * v));
+                w[4 * v] = q.x;
+                w[4 * v + 1] = q.y;
+                w[4 * v + 2] = q.z;
+                w[4 * v + 3] = q.w;
             }
         } else {
-            const uint8_t *mp = reinterpret_cast<const uint8_t *>(a.mask) + base;
-            const bool vec = (c0 + 32 <= S) && ((reinterpret_cast<uintptr_t>(mp) & 15u) == 0);
-            if (vec) {
 #pragma unroll
-                for (int v = 0; v < 2; ++v) {
-                    const uint4 w = ld_keep(mp + 16 * v);
-                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) m2[16 * v + e] = ((ws[e >> 2] >> (8 * (e & 3))) & 0xffu) ? neg_inf() : 0.f;
+            for (int e = 0; e < 32; ++e) {
+                if (c0 + e < S) {
+                    if constexpr (MK == 1) w[e >> 1] |= (uint32_t)reinterpret_cast<const uint16_t *>(mp)[e] << (16 * (e & 1));
+                    else w[e >> 2] |= (uint32_t)mp[e] << (8 * (e & 3));
                 }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    if (c0 + e < S) m2[e] = mp[e] ? neg_inf() : 0.f;
             }
         }
     }
@@ -360,6 +348,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             const int j0 = j * kBN;
             // per-element rules only where a block crosses the diagonal or the end of the keys
             const bool pred = (j0 + kBN > a.S) || (a.causal && j0 + kBN - 1 > qt0);
+            // this block's mask elements: the first 32 keys fetched while the scores are computed;
+            // for a byte mask each next 32 while the previous ones are scored (an additive mask's
+            // 16 words per 32 keys, held twice, would spill the score registers: loaded in place)
+            constexpr bool AHEAD = MK == 2;
+            uint32_t mw[AHEAD ? 2 : 1][MaskWords<MK>::n];
+            mask_chunk_load<T, MK>(a, mrow, j0, row_ok, mw[0]);
             if (!warp_wait(&b.s_full[t], (uint32_t)(j & 1), b, a.err)) { ok = false; break; }
             tc::fence_after_sync();
             // the whole block row in registers, then the score columns go back to the MMA
@@ -372,8 +366,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             float mx = neg_inf();
 #pragma unroll
             for (int c = 0; c < kBN / 32; ++c) {
+                if constexpr (AHEAD) {
+                    if (c + 1 < kBN / 32) mask_chunk_load<T, MK>(a, mrow, j0 + (c + 1) * 32, row_ok, mw[(c + 1) & 1]);
+                } else if (c > 0) {
+                    mask_chunk_load<T, MK>(a, mrow, j0 + c * 32, row_ok, mw[0]);
+                }
                 float m2[32];
-                mask_chunk<T, MK>(a, mrow, j0 + c * 32, row_ok, m2);
+                mask_terms<T, MK>(mw[AHEAD ? (c & 1) : 0], m2);
                 float(&sc)[32] = *reinterpret_cast<float(*)[32]>(sv + 32 * c);
                 mx = pred ? score_chunk<true>(a, sc, m2, j0 + c * 32, i, sl2, mx)
                           : score_chunk<false>(a, sc, m2, j0 + c * 32, i, sl2, mx);
