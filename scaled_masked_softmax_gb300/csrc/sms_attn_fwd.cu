@@ -46,15 +46,19 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAtom = 16384;  // 128 rows x 128 bytes
 
 template <int D> struct FwdCfg {
+    // D = 128: one P buffer for both tiles (they take turns with it, see the
+    // softmax below), which leaves room for two V slots.  A single V slot made
+    // V_{j+1} wait for the last product with V_j and then the whole load.
+    static constexpr bool SHARED_P = D == 128;
     static constexpr int NK = D == 128 ? 2 : 3;        // K slots
-    static constexpr int NV = D == 128 ? 1 : 3;        // V slots
+    static constexpr int NV = D == 128 ? 2 : 3;        // V slots
     static constexpr uint32_t TILE = (D / 64) * kAtom;  // one 128 x D tile (Q, K or V)
     static constexpr uint32_t PBUF = (kBN / 64) * kAtom;
     static constexpr uint32_t OFF_Q = 0;                // two Q tiles
     static constexpr uint32_t OFF_K = OFF_Q + 2 * TILE;
     static constexpr uint32_t OFF_V = OFF_K + NK * TILE;
-    static constexpr uint32_t OFF_P = OFF_V + NV * TILE;  // one P buffer per tile
-    static constexpr uint32_t OFF_BAR = OFF_P + 2 * PBUF;
+    static constexpr uint32_t OFF_P = OFF_V + NV * TILE;  // P buffer(s)
+    static constexpr uint32_t OFF_BAR = OFF_P + (SHARED_P ? 1 : 2) * PBUF;
     static constexpr uint32_t BAR_BYTES = 512;
     static constexpr uint32_t SMEM = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
     // TMEM columns of tile t: scores at t*256, output accumulator at t*256 + 128
@@ -305,7 +309,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 if (!wait_or_flag(&b.p_full[t], (uint32_t)(j & 1), b, a.err)) return false;
                 if (!wait_or_flag(&b.v_full[st], (uint32_t)((j / NV) & 1), b, a.err)) return false;
                 tc::fence_after_sync();
-                const uint32_t p_addr = s_base + C::OFF_P + t * C::PBUF, v_addr = s_base + C::OFF_V + st * C::TILE;
+                const uint32_t p_addr = s_base + C::OFF_P + (C::SHARED_P ? 0 : t * C::PBUF), v_addr = s_base + C::OFF_V + st * C::TILE;
 #pragma unroll
                 for (int k = 0; k < kBN / 16; ++k) {
                     const uint64_t da = tc::desc_sw128(p_addr + (k / 4) * kAtom + (k % 4) * 32, 16, 1024);
@@ -343,7 +347,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
         const int qt0 = q0 + t * kBM;
         float m_run = neg_inf(), l = 0.f;
         bool ok = true;
-        unsigned char *pbuf = smem + C::OFF_P + t * C::PBUF;
+        unsigned char *pbuf = smem + C::OFF_P + (C::SHARED_P ? 0 : t * C::PBUF);
         for (int j = 0; j < n; ++j) {
             const int j0 = j * kBN;
             // per-element rules only where a block crosses the diagonal or the end of the keys
@@ -391,10 +395,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             l = l * alpha + lsum;
             // P of block j - 1 has been consumed (this tile's P buffer is free)
             // and O holds every block before j once that P V is done
-            if (j >= 1) {
-                if (!warp_wait(&b.pv_done[t], (uint32_t)((j - 1) & 1), b, a.err)) { ok = false; break; }
-                tc::fence_after_sync();
+            // with the shared P buffer (taken P_0(j), P_1(j), P_0(j+1), ...) also the other tile's
+            // product that last read it: tile 1 writes block j once P_0(j) V_j is done (tile 0 has
+            // blocks 0 .. nt[0]-1), tile 0 once P_1(j-1) V_{j-1} is.  One wait site for both.
+            bool waited = true;
+#pragma unroll 1
+            for (int w = 0; w < (C::SHARED_P ? 2 : 1); ++w) {
+                int wt = t, wj = j - 1;
+                if (w == 1) {
+                    wt = 1 - t;
+                    wj = t == 1 ? (j < nt[0] ? j : -1) : j - 1;
+                }
+                if (wj >= 0 && !warp_wait(&b.pv_done[wt], (uint32_t)(wj & 1), b, a.err)) { waited = false; break; }
             }
+            if (!waited) { ok = false; break; }
+            tc::fence_after_sync();
 #pragma unroll
             for (int c = 0; c < kBN / 32; ++c) {
                 unsigned char *atom = pbuf + (c / 2) * kAtom;
