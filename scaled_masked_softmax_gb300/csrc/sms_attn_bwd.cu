@@ -396,8 +396,15 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 tc::tmem_ld32(tl + C::COL_DP + c * 32, dv);
                 tc::tmem_wait_ld();
                 uint32_t pk[16], dk[16];
-                if (pred) p_ds_chunk<T, MK, true>(a, sv, dv, m2, s_lse, s_dsc, c, i0, j, key_ok, sl2, pk, dk);
-                else p_ds_chunk<T, MK, false>(a, sv, dv, m2, s_lse, s_dsc, c, i0, j, key_ok, sl2, pk, dk);
+                // a chunk in which no lane of the warp has a masked element (most blocks of a key-padding
+                // mask) takes the unmasked body
+                if (MK == 0 || mask_none<MK>(mw[cc])) {
+                    if (pred) p_ds_chunk<T, 0, true>(a, sv, dv, m2, s_lse, s_dsc, c, i0, j, key_ok, sl2, pk, dk);
+                    else p_ds_chunk<T, 0, false>(a, sv, dv, m2, s_lse, s_dsc, c, i0, j, key_ok, sl2, pk, dk);
+                } else {
+                    if (pred) p_ds_chunk<T, MK, true>(a, sv, dv, m2, s_lse, s_dsc, c, i0, j, key_ok, sl2, pk, dk);
+                    else p_ds_chunk<T, MK, false>(a, sv, dv, m2, s_lse, s_dsc, c, i0, j, key_ok, sl2, pk, dk);
+                }
                 if (n > 0) {
                     // the previous block's dQ pieces over atom cc have been read by their bulk adds
                     // (group cc) before the stores here; the waits overlap the chunks' arithmetic

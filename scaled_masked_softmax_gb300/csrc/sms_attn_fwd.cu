@@ -162,16 +162,16 @@ __device__ __forceinline__ void mask_chunk_load(const AttnArgs &a, int64_t mrow,
 }
 
 // Scores of 32 keys col0 .. col0+31 for query row i, in place, in log2 units:
-// S * scale * log2e + mask; with PR, keys past S or (causal) after i get -inf.
-// Returns the running maximum updated with them.
-template <bool PR>
+// S * scale * log2e (+ the mask terms m2 when MT); with PR, keys past S or
+// (causal) after i get -inf.  Returns the running maximum updated with them.
+template <bool PR, bool MT>
 __device__ __forceinline__ float score_chunk(const AttnArgs &a, float (&s)[32], const float (&m2)[32], int col0, int i,
                                              float sl2, float mx)
 {
 #pragma unroll
     for (int e = 0; e < 32; e += 2) {
-        float s0 = fmaf(s[e], sl2, m2[e]);
-        float s1 = fmaf(s[e + 1], sl2, m2[e + 1]);
+        float s0 = MT ? fmaf(s[e], sl2, m2[e]) : s[e] * sl2;
+        float s1 = MT ? fmaf(s[e + 1], sl2, m2[e + 1]) : s[e + 1] * sl2;
         if constexpr (PR) {
             const int col = col0 + e;
             if (col >= a.S || (a.causal && col > i)) s0 = neg_inf();
@@ -352,12 +352,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             const int j0 = j * kBN;
             // per-element rules only where a block crosses the diagonal or the end of the keys
             const bool pred = (j0 + kBN > a.S) || (a.causal && j0 + kBN - 1 > qt0);
-            // this block's mask elements: the first 32 keys fetched while the scores are computed;
-            // for a byte mask each next 32 while the previous ones are scored (an additive mask's
-            // 16 words per 32 keys, held twice, would spill the score registers: loaded in place)
-            constexpr bool AHEAD = MK == 2;
-            uint32_t mw[AHEAD ? 2 : 1][MaskWords<MK>::n];
-            mask_chunk_load<T, MK>(a, mrow, j0, row_ok, mw[0]);
+            // this block's mask elements: the first 32 keys fetched while the scores are computed, the
+            // others in place (a second chunk of words held ahead spilled the score registers)
+            uint32_t mw[MaskWords<MK>::n];
+            mask_chunk_load<T, MK>(a, mrow, j0, row_ok, mw);
             if (!warp_wait(&b.s_full[t], (uint32_t)(j & 1), b, a.err)) { ok = false; break; }
             tc::fence_after_sync();
             // the whole block row in registers, then the score columns go back to the MMA
@@ -370,16 +368,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             float mx = neg_inf();
 #pragma unroll
             for (int c = 0; c < kBN / 32; ++c) {
-                if constexpr (AHEAD) {
-                    if (c + 1 < kBN / 32) mask_chunk_load<T, MK>(a, mrow, j0 + (c + 1) * 32, row_ok, mw[(c + 1) & 1]);
-                } else if (c > 0) {
-                    mask_chunk_load<T, MK>(a, mrow, j0 + c * 32, row_ok, mw[0]);
-                }
-                float m2[32];
-                mask_terms<T, MK>(mw[AHEAD ? (c & 1) : 0], m2);
+                if (c > 0) mask_chunk_load<T, MK>(a, mrow, j0 + c * 32, row_ok, mw);
                 float(&sc)[32] = *reinterpret_cast<float(*)[32]>(sv + 32 * c);
-                mx = pred ? score_chunk<true>(a, sc, m2, j0 + c * 32, i, sl2, mx)
-                          : score_chunk<false>(a, sc, m2, j0 + c * 32, i, sl2, mx);
+                // no lane of the warp with a masked key in these 32 (most blocks of a key-padding mask):
+                // the unmasked body, no mask terms to decode
+                if (MK == 0 || mask_none<MK>(mw)) {
+                    mx = pred ? score_chunk<true, false>(a, sc, sc, j0 + c * 32, i, sl2, mx)
+                              : score_chunk<false, false>(a, sc, sc, j0 + c * 32, i, sl2, mx);
+                } else {
+                    float m2[32];
+                    mask_terms<T, MK>(mw, m2);
+                    mx = pred ? score_chunk<true, true>(a, sc, m2, j0 + c * 32, i, sl2, mx)
+                              : score_chunk<false, true>(a, sc, m2, j0 + c * 32, i, sl2, mx);
+                }
             }
             const float m_new = fmaxf(m_run, mx);
             const bool resc = m_new > m_run + 8.f;  // false while both are -inf

@@ -30,4 +30,14 @@ __device__ __forceinline__ void mask_terms(const uint32_t (&w)[MaskWords<MK>::n]
     }
 }
 
+// True when no element of the chunk, in any lane of the warp, is masked (all
+// words zero: byte 0 = kept, additive +0).  Called by whole warps.
+template <int MK> __device__ __forceinline__ bool mask_none(const uint32_t (&w)[MaskWords<MK>::n])
+{
+    uint32_t o = 0u;
+#pragma unroll
+    for (int k = 0; k < MaskWords<MK>::n; ++k) o |= w[k];
+    return __all_sync(0xffffffffu, o == 0u);
+}
+
 }  // namespace sms
