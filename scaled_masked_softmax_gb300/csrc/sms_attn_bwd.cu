@@ -33,6 +33,7 @@
 #include <cuda.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "sms_attn.h"
 #include "sms_attn_mask.cuh"
@@ -140,19 +141,18 @@ __device__ __forceinline__ void mask_col_load(const AttnArgs &a, int64_t mbase, 
     for (int k = 0; k < MaskWords<MK>::n; ++k) w[k] = 0u;
     if constexpr (MK != 0) {
         if (!key_ok) return;
+        // all 32 loads first (rows past S clamped to the last row and dropped below), so that they
+        // are in flight together: element by element behind a bounds test they went one at a time
+        using E = std::conditional_t<MK == 1, uint16_t, uint8_t>;
+        const E *col = reinterpret_cast<const E *>(a.mask) + mbase;
+        uint32_t v[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = __ldg(col + (int64_t)min(i0 + e, a.S - 1) * a.S);
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-            const int i = i0 + e;
-            if (i < a.S) {
-                const int64_t off = mbase + (int64_t)i * a.S;
-                if constexpr (MK == 1) {
-                    const uint32_t h = reinterpret_cast<const uint16_t *>(a.mask)[off];
-                    w[e >> 1] |= h << (16 * (e & 1));
-                } else {
-                    const uint32_t bt = reinterpret_cast<const uint8_t *>(a.mask)[off];
-                    w[e >> 2] |= bt << (8 * (e & 3));
-                }
-            }
+            const uint32_t x = (i0 + e < a.S) ? v[e] : 0u;
+            if constexpr (MK == 1) w[e >> 1] |= x << (16 * (e & 1));
+            else w[e >> 2] |= x << (8 * (e & 3));
         }
     }
 }

@@ -161,6 +161,43 @@ __device__ __forceinline__ void mask_chunk_load(const AttnArgs &a, int64_t mrow,
     }
 }
 
+// One bit per element of a packed byte-mask chunk (MaskWords<2>: 8 words of 4
+// bytes): bit e set when element e is nonzero (masked).  Per word the bytes
+// become 0x00 / 0xff and a multiply by 2^21 + 2^14 + 2^7 + 1 moves their top
+// bits to bits 28 .. 31 (the other partial products stay below bit 24).
+__device__ __forceinline__ uint32_t mask_bits(const uint32_t (&w)[8])
+{
+    uint32_t bits = 0u;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t m = __vcmpne4(w[k], 0u) & 0x80808080u;
+        bits |= ((m * 0x00204081u) >> 28) << (4 * k);
+    }
+    return bits;
+}
+
+// Scores of 32 keys col0 .. col0+31 for query row i with a byte mask given as
+// bits (bit e set: key col0 + e masked): as score_chunk, masked keys -inf.
+template <bool PR>
+__device__ __forceinline__ float score_chunk_bits(const AttnArgs &a, float (&s)[32], uint32_t bits, int col0, int i,
+                                                  float sl2, float mx)
+{
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+        float s0 = ((bits >> e) & 1u) ? neg_inf() : s[e] * sl2;
+        float s1 = ((bits >> (e + 1)) & 1u) ? neg_inf() : s[e + 1] * sl2;
+        if constexpr (PR) {
+            const int col = col0 + e;
+            if (col >= a.S || (a.causal && col > i)) s0 = neg_inf();
+            if (col + 1 >= a.S || (a.causal && col + 1 > i)) s1 = neg_inf();
+        }
+        s[e] = s0;
+        s[e + 1] = s1;
+        mx = rowmath_max3(mx, s0, s1);
+    }
+    return mx;
+}
+
 // Scores of 32 keys col0 .. col0+31 for query row i, in place, in log2 units:
 // S * scale * log2e (+ the mask terms m2 when MT); with PR, keys past S or
 // (causal) after i get -inf.  Returns the running maximum updated with them.
@@ -352,10 +389,34 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             const int j0 = j * kBN;
             // per-element rules only where a block crosses the diagonal or the end of the keys
             const bool pred = (j0 + kBN > a.S) || (a.causal && j0 + kBN - 1 > qt0);
-            // this block's mask elements: the first 32 keys fetched while the scores are computed, the
-            // others in place (a second chunk of words held ahead spilled the score registers)
+            // this block's mask elements, fetched while the scores are computed: a byte mask whole,
+            // compressed to one bit per key (mbits[c] bit e: key j0 + 32c + e masked); an additive
+            // mask's first 32 keys (its others in place: more words held ahead spilled the scores)
             uint32_t mw[MaskWords<MK>::n];
-            mask_chunk_load<T, MK>(a, mrow, j0, row_ok, mw);
+            uint32_t mbits[MK == 2 ? kBN / 32 : 1];
+            if constexpr (MK == 2) {
+                const uint8_t *mp = reinterpret_cast<const uint8_t *>(a.mask) + mrow + j0;
+                if (row_ok && j0 + kBN <= a.S && (reinterpret_cast<uintptr_t>(mp) & 15u) == 0) {
+                    // the whole 128-byte row segment: eight 16-byte loads in flight together
+                    uint4 q[kBN / 16];
+#pragma unroll
+                    for (int v = 0; v < kBN / 16; ++v) q[v] = ld_keep(reinterpret_cast<const T *>(mp + 16 * v));
+#pragma unroll
+                    for (int c = 0; c < kBN / 32; ++c) {
+                        const uint32_t w8[8] = {q[2 * c].x, q[2 * c].y, q[2 * c].z, q[2 * c].w,
+                                                q[2 * c + 1].x, q[2 * c + 1].y, q[2 * c + 1].z, q[2 * c + 1].w};
+                        mbits[c] = mask_bits(w8);
+                    }
+                } else {  // a row past S, the ragged end of the keys, or a row that is not 16-byte aligned
+#pragma unroll
+                    for (int c = 0; c < kBN / 32; ++c) {
+                        mask_chunk_load<T, MK>(a, mrow, j0 + c * 32, row_ok, mw);
+                        mbits[c] = mask_bits(mw);
+                    }
+                }
+            } else {
+                mask_chunk_load<T, MK>(a, mrow, j0, row_ok, mw);
+            }
             if (!warp_wait(&b.s_full[t], (uint32_t)(j & 1), b, a.err)) { ok = false; break; }
             tc::fence_after_sync();
             // the whole block row in registers, then the score columns go back to the MMA
@@ -368,11 +429,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             float mx = neg_inf();
 #pragma unroll
             for (int c = 0; c < kBN / 32; ++c) {
-                if (c > 0) mask_chunk_load<T, MK>(a, mrow, j0 + c * 32, row_ok, mw);
+                if (MK == 1 && c > 0) mask_chunk_load<T, MK>(a, mrow, j0 + c * 32, row_ok, mw);
                 float(&sc)[32] = *reinterpret_cast<float(*)[32]>(sv + 32 * c);
                 // no lane of the warp with a masked key in these 32 (most blocks of a key-padding mask):
                 // the unmasked body, no mask terms to decode
-                if (MK == 0 || mask_none<MK>(mw)) {
+                if constexpr (MK == 2) {
+                    if (__all_sync(0xffffffffu, mbits[c] == 0u)) {
+                        mx = pred ? score_chunk<true, false>(a, sc, sc, j0 + c * 32, i, sl2, mx)
+                                  : score_chunk<false, false>(a, sc, sc, j0 + c * 32, i, sl2, mx);
+                    } else {
+                        mx = pred ? score_chunk_bits<true>(a, sc, mbits[c], j0 + c * 32, i, sl2, mx)
+                                  : score_chunk_bits<false>(a, sc, mbits[c], j0 + c * 32, i, sl2, mx);
+                    }
+                } else if (MK == 0 || mask_none<MK>(mw)) {
                     mx = pred ? score_chunk<true, false>(a, sc, sc, j0 + c * 32, i, sl2, mx)
                               : score_chunk<false, false>(a, sc, sc, j0 + c * 32, i, sl2, mx);
                 } else {
