@@ -446,9 +446,10 @@ template <typename T, typename M, int G, int NV, bool ALIGNED> __host__ __device
 // One row per lane group: the shared row math of sms_rowmath.cuh (one
 // switch per row realigns a misaligned mask, bounds are tested once per row,
 // paired elements use the packed fp32x2 forms).  CTAs per SM it is compiled
-// for: the shuffled shapes that fit 64 registers without spilling (G = 256,
-// or at most 4 vectors per lane) take four (measured +6 points at fp32
-// S=4099, 256 x 5; +2 to +4 on 16-bit misaligned rows).  Otherwise fp32 rows
+// for: the shuffled shapes of at most 5 vectors per lane take four, at 64
+// registers (fp32 S=4099, 256 x 5, no spill: +6 points; the 16-bit 32, 64
+// and 128 x 5 shapes spill 212-284 B and still gain 4-5 points over three
+// CTAs at S = 1100, 2049, 2500 and 4099).  Otherwise fp32 rows
 // are held in at most 80 registers, three CTAs per multiprocessor: measured
 // faster than two CTAs with more registers (S=4099: 66% against 43% of the
 // copy rate; S=1024: +5%); not for misaligned fp32 rows of 6 or 8 vectors per
@@ -457,7 +458,7 @@ template <typename T, typename M, int G, int NV, bool ALIGNED> __host__ __device
 // and 4099); at 4, 6 or 8 vectors two CTAs measured no worse.
 template <typename T, typename M, int G, int NV, bool ALIGNED> constexpr int fwd_min_ctas()
 {
-    if (fwd_shuffled<T, M, G, NV, ALIGNED>() && (G == 256 || NV <= 4)) return 4;
+    if (fwd_shuffled<T, M, G, NV, ALIGNED>() && NV <= 5) return 4;
     return (Dt<T>::VEC == 4 && (ALIGNED || NV <= 5)) ? 3 : (NV == 5 ? 3 : 2);
 }
 
