@@ -19,9 +19,10 @@
 //        dV += P^T dO and dK += dS^T Q accumulate in TMEM; dQ_blk = dS K goes
 //        to TMEM (reusing the dP^T columns); the same threads, now one query
 //        row each, copy it into shared memory (the P^T / dS^T area, which the
-//        products have finished with), and one thread hands the whole tile to
-//        the TMA unit as a single bulk add into the fp32 accumulator, which
-//        runs while the next block is computed.
+//        products have finished with), and one thread hands the tile to the
+//        TMA unit as bulk adds into the fp32 accumulator (two groups, in the
+//        order the next block's stores reuse the area), which run while the
+//        next block is computed.
 //      At the end dK and dV leave TMEM once, rounded to the 16-bit dtype;
 //   3. attn_bwd_post: dQ = the accumulator rounded to the 16-bit dtype.
 // Roles: warp 0 one lane issues the TMA loads (K and V once; dO and Q of each

@@ -4,23 +4,27 @@
 // article, pnsm.cn/news/1983787, names in §4.4, with the streaming softmax
 // of "从GEMM到Transformer：手写CUDA算子优化的完整路线与性能调优实践" §2.2).
 //
-// One CTA owns 128 query rows of one (batch, head) and walks the key blocks
-// of 128 keys:
-//   * warp 0, one lane: TMA loads (cp.async.bulk.tensor, 128-byte swizzle)
-//     of the Q tile once and of the K and V tiles into a ring of stages;
-//   * warp 1, one lane: the MMAs, S_j = Q K_j^T into one of two TMEM score
-//     buffers, then O += P_j V_j into the TMEM output accumulator; warp 1
-//     also owns the TMEM allocation;
-//   * warps 2..5 (128 threads, one query row each, row = the warp's TMEM
-//     lane quarter): read S_j from TMEM, apply scale, mask and the causal
-//     rule, keep the running max m and sum l of the online softmax
-//     (m' = max(m, max_j s), l' = l * 2^(m - m') + sum 2^(s - m')), write
-//     P_j = 2^(s - m) as 16-bit values into shared memory in the MMA's
-//     swizzled layout, and rescale O in TMEM when m grows (only when it grows
-//     by more than 2^8, so most blocks skip it: the exponentials stay below
-//     2^8 in between); at the end O / l is stored and lse = (m + log2 l) ln 2.
-// S is double-buffered in TMEM, so the MMA of block j+1 overlaps the softmax
-// of block j, and the P V MMA of block j overlaps the softmax of block j+1.
+// One CTA owns two tiles of 128 query rows of one (batch, head) and walks the
+// key blocks of 128 keys:
+//   * warp 0: lane 0 the TMA loads (cp.async.bulk.tensor, 128-byte swizzle)
+//     of both Q tiles once and of the K blocks into a ring of slots, lane 1
+//     those of the V blocks into their own ring (V slots free up later);
+//   * warp 1, one lane: the MMAs, S_t(j) = Q_t K_j^T into tile t's TMEM score
+//     columns, then O_t += P_t(j) V_j into its TMEM output columns; warp 1
+//     also owns the TMEM allocation (512 columns: per tile 128 for S, D for O);
+//   * warps 2..5 (tile 0) and 6..9 (tile 1), one query row per thread (the
+//     row is the warp's TMEM lane quarter): read S_t(j) from TMEM in one go
+//     and release the columns, apply scale, mask and the causal rule, keep the
+//     running max m and sum l of the online softmax (m' = max(m, max_j s),
+//     l' = l * 2^(m - m') + sum 2^(s - m')), write P = 2^(s - m) as 16-bit
+//     values into shared memory in the MMA's swizzled layout, and rescale O in
+//     TMEM when m grows by more than 8 (log2 units; in between the
+//     exponentials stay below 2^8, so most blocks skip it); at the end O / l
+//     is stored and lse = (m + log2 l) ln 2.
+// The scores of block j+1 are issued before the products of block j, so the
+// tensor cores compute one tile's work while the other tile's softmax runs
+// (the two tiles' softmax phases alternate).  At D = 128 the tiles share one P
+// buffer, taking turns with it, which leaves room for two V slots.
 //
 // Every mbarrier wait is bounded (2 s).  A role whose wait gives up records
 // an error in the device word and stops; before the CTA leaves, the TMA lane
