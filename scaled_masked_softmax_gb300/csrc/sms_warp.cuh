@@ -449,7 +449,9 @@ template <typename T, typename M, int G, int NV, bool ALIGNED> __host__ __device
 // for: the shuffled shapes of at most 5 vectors per lane take four, at 64
 // registers (fp32 S=4099, 256 x 5, no spill: +6 points; the 16-bit 32, 64
 // and 128 x 5 shapes spill 212-284 B and still gain 4-5 points over three
-// CTAs at S = 1100, 2049, 2500 and 4099).  Otherwise fp32 rows
+// CTAs at S = 1100, 2049, 2500 and 4099), those of 6 or 7 take three, at 80
+// (spilling 40-600 B, against two CTAs: f16 S=1500 57% -> 69%, S=1700
+// 59% -> 69%, S=3333 59% -> 66%).  Otherwise fp32 rows
 // are held in at most 80 registers, three CTAs per multiprocessor: measured
 // faster than two CTAs with more registers (S=4099: 66% against 43% of the
 // copy rate; S=1024: +5%); not for misaligned fp32 rows of 6 or 8 vectors per
@@ -459,6 +461,7 @@ template <typename T, typename M, int G, int NV, bool ALIGNED> __host__ __device
 template <typename T, typename M, int G, int NV, bool ALIGNED> constexpr int fwd_min_ctas()
 {
     if (fwd_shuffled<T, M, G, NV, ALIGNED>() && NV <= 5) return 4;
+    if (fwd_shuffled<T, M, G, NV, ALIGNED>() && NV <= 7) return 3;
     return (Dt<T>::VEC == 4 && (ALIGNED || NV <= 5)) ? 3 : (NV == 5 ? 3 : 2);
 }
 
