@@ -430,13 +430,14 @@ __device__ __forceinline__ int64_t reuse_row(const FwdArgs &a, int64_t n)
 // a second load per slot (4*NV fewer registers).  A byte mask's second vector
 // is one or two words, and the shuffles cost it 3-4 points: it keeps the
 // second load, on the same mapping, so that a boolean mask and its additive
-// -inf form give the same bits.  Measured on GB300: 16-bit rows gain 2-4
-// points at every lane count from 32; fp32 rows gain only at 256 x 5 (S =
-// 4097..5120, where the freed registers give four CTAs per SM: 71% -> 77% at
-// S=4099) and lose 1-2 points at 128 x 5 and 256 x 4, which keep the old form.
+// -inf form give the same bits.  Measured on GB300, with the CTAs per SM
+// the freed registers allow (fwd_min_ctas): 16-bit rows gain at every lane
+// count from 32; fp32 rows gain from 128 lanes (S=2049 73% -> 76%, S=3333
+// 73% -> 74%, S=4099 71% -> 77%) and lose 0.5-2 points at 64 lanes, which
+// keep the old form.
 template <typename T, int G, int NV, bool ALIGNED> __host__ __device__ constexpr bool fwd_contiguous()
 {
-    return !ALIGNED && G >= 32 && (sizeof(T) == 2 || (G == 256 && NV == 5));
+    return !ALIGNED && G >= 32 && (sizeof(T) == 2 || G >= 128);
 }
 template <typename T, typename M, int G, int NV, bool ALIGNED> __host__ __device__ constexpr bool fwd_shuffled()
 {
