@@ -52,7 +52,7 @@ constexpr int kBM = 128;          // keys per CTA (the MMA's M for S^T, dP^T, dV
 constexpr int kBN = kAttnBwdQueryBlock;  // queries per block (128)
 constexpr int kThreads = 320;     // warps 0 (TMA), 1 (MMA), 2..9 (element-wise: two warps per TMEM lane quarter)
 constexpr int kMath = 256;
-constexpr int kHeadGroup = 8;     // heads whose CTAs are scheduled together
+constexpr int kHeadGroup = 4;     // heads whose CTAs are scheduled together
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAtom = 16384;
 
